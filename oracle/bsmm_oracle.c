@@ -1,0 +1,322 @@
+/*
+ * bsmm_oracle.c -- plain, slow, obviously-correct CPU oracle for block-sparse
+ * matrix multiplication.  TEST INFRASTRUCTURE ONLY: it exists to check the
+ * CUDA library and may be used only by the tests, the package's smoke check
+ * and the CPU-baseline leg of the benchmark.  The product path never calls it.
+ *
+ * It shares no code, header, table or constant with the CUDA library.
+ *
+ * Source: the blocksparse README (openai/blocksparse, as mirrored on the
+ * kiteco/blocksparse page), section "API Documentation: blocksparse.matmul":
+ *   - BlocksparseMatMul(layout, block_size, feature_axis): layout is a 2-D 0/1
+ *     array of blocks, block_size in {32,16,8}, feature_axis 1 means (N,C)
+ *     activations and 0 means (C,N).
+ *   - block_coord(block): the (c,k) layout coordinate of a block id.
+ *   - w_shape: one bs x bs weight block per nonzero layout entry.
+ *   - __call__(I, W): y = I . W with W the block-sparse (C x K) weight.
+ *   - identity_init: identity initialisation of the weight blocks.
+ *   - group_param_grads: the weight gradients of up to 8 timesteps sharing one
+ *     weight are summed (cast32: in float32 or wider).
+ *
+ * Readings where the page is silent (each one also listed in the design notes):
+ *   - block ids are assigned in row-major scan order of the layout
+ *     (c outer, k inner);
+ *   - weight block b at layout (c,k) holds W[c*bs+i][k*bs+j] at w[b][i][j];
+ *   - identity_init sets blocks with c == k to the bs x bs identity and every
+ *     other block to zero;
+ *   - an output block column (row) with no nonzero block is zero.
+ *
+ * Everything is float64, row-major, no blocking or reordering of the sums
+ * beyond the definition: each output is accumulated over its reduction index
+ * in increasing order.  OpenMP only splits independent outputs across threads.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Number of nonzero blocks of a layout. */
+int64_t oracle_nnz(const uint8_t *L, int R, int S)
+{
+    int64_t n = 0;
+    for (int64_t i = 0; i < (int64_t)R * S; ++i)
+        n += L[i] != 0;
+    return n;
+}
+
+/* Block-id map: bid[c*S+k] = id of block (c,k) in row-major scan order, or -1. */
+static int32_t *block_id_map(const uint8_t *L, int R, int S)
+{
+    int32_t *bid = (int32_t *)malloc(sizeof(int32_t) * (size_t)R * (size_t)S);
+    int32_t next = 0;
+    for (int c = 0; c < R; ++c)
+        for (int k = 0; k < S; ++k)
+            bid[(size_t)c * S + k] = L[(size_t)c * S + k] ? next++ : -1;
+    return bid;
+}
+
+/*
+ * Lookup tables, built by naive scans.
+ *   coord[2b], coord[2b+1]       = (c, k) of block b            (block_coord)
+ *   col_ptr[k] .. col_ptr[k+1]   = entries of output block column k,
+ *   col_ent[2e], col_ent[2e+1]   = (b, c), c increasing
+ *   row_ptr[c] .. row_ptr[c+1]   = entries of input block row c,
+ *   row_ent[e]                   = k, k increasing (the block id is e itself)
+ */
+void oracle_luts(const uint8_t *L, int R, int S,
+                 int32_t *row_ptr, int32_t *row_ent,
+                 int32_t *col_ptr, int32_t *col_ent, int32_t *coord)
+{
+    int32_t *bid = block_id_map(L, R, S);
+    int32_t e = 0;
+    for (int c = 0; c < R; ++c) {
+        row_ptr[c] = e;
+        for (int k = 0; k < S; ++k)
+            if (L[(size_t)c * S + k]) {
+                row_ent[e] = k;
+                coord[2 * e] = c;
+                coord[2 * e + 1] = k;
+                ++e;
+            }
+    }
+    row_ptr[R] = e;
+    e = 0;
+    for (int k = 0; k < S; ++k) {
+        col_ptr[k] = e;
+        for (int c = 0; c < R; ++c)
+            if (L[(size_t)c * S + k]) {
+                col_ent[2 * e] = bid[(size_t)c * S + k];
+                col_ent[2 * e + 1] = c;
+                ++e;
+            }
+    }
+    col_ptr[S] = e;
+    free(bid);
+}
+
+/* Dense C x K weight from the layout and the (nnz, bs, bs) blocks. */
+void oracle_densify(const uint8_t *L, int R, int S, int bs, const double *w, double *Wd)
+{
+    int64_t C = (int64_t)R * bs, K = (int64_t)S * bs;
+    int32_t *bid = block_id_map(L, R, S);
+    for (int64_t cc = 0; cc < C; ++cc)
+        for (int64_t kk = 0; kk < K; ++kk) {
+            int32_t b = bid[(cc / bs) * S + kk / bs];
+            Wd[cc * K + kk] = b < 0 ? 0.0 : w[((int64_t)b * bs + cc % bs) * bs + kk % bs];
+        }
+    free(bid);
+}
+
+/* identity_init: w[b] = I if c_b == k_b else 0. */
+void oracle_identity_init(const uint8_t *L, int R, int S, int bs, double *w)
+{
+    int64_t b = 0;
+    for (int c = 0; c < R; ++c)
+        for (int k = 0; k < S; ++k)
+            if (L[(size_t)c * S + k]) {
+                for (int i = 0; i < bs; ++i)
+                    for (int j = 0; j < bs; ++j)
+                        w[(b * bs + i) * bs + j] = (c == k && i == j) ? 1.0 : 0.0;
+                ++b;
+            }
+}
+
+/* Activation element (n, f) of an (N,F) [fa=1] or (F,N) [fa=0] array. */
+static inline double act(const double *a, int64_t n, int64_t f, int64_t N, int64_t F, int fa)
+{
+    return fa ? a[n * F + f] : a[f * N + n];
+}
+
+static inline double *act_ptr(double *a, int64_t n, int64_t f, int64_t N, int64_t F, int fa)
+{
+    return fa ? &a[n * F + f] : &a[f * N + n];
+}
+
+static void set_threads(int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/*
+ * fprop: y[n][kk] = sum_{cc=0}^{C-1} x[n][cc] * Wd[cc][kk]  (y = x . W).
+ * Rows n in [n_lo, n_hi) only (the rest of y is left untouched).
+ */
+void oracle_fprop(const double *x, const double *Wd, double *y,
+                  int N, int C, int K, int fa, int n_lo, int n_hi, int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int n = n_lo; n < n_hi; ++n)
+        for (int64_t kk = 0; kk < K; ++kk) {
+            double s = 0.0;
+            for (int64_t cc = 0; cc < C; ++cc)
+                s += act(x, n, cc, N, C, fa) * Wd[cc * K + kk];
+            *act_ptr(y, n, kk, N, K, fa) = s;
+        }
+}
+
+/*
+ * bprop: dx[n][cc] = sum_{kk=0}^{K-1} dy[n][kk] * Wd[cc][kk]  (dx = dy . W^T).
+ */
+void oracle_bprop(const double *dy, const double *Wd, double *dx,
+                  int N, int C, int K, int fa, int n_lo, int n_hi, int nthreads)
+{
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int n = n_lo; n < n_hi; ++n)
+        for (int64_t cc = 0; cc < C; ++cc) {
+            double s = 0.0;
+            for (int64_t kk = 0; kk < K; ++kk)
+                s += act(dy, n, kk, N, K, fa) * Wd[cc * K + kk];
+            *act_ptr(dx, n, cc, N, C, fa) = s;
+        }
+}
+
+/*
+ * updat: dw[b][i][j] = sum_{n=0}^{N-1} x[n][c_b*bs+i] * dy[n][k_b*bs+j],
+ * for blocks b in [b_lo, b_hi).  With accumulate != 0 the sum is added to the
+ * value already in dw (one rounding-free float64 add).
+ */
+void oracle_updat(const uint8_t *L, int R, int S, int bs,
+                  const double *x, const double *dy, double *dw,
+                  int N, int fa, int accumulate, int64_t b_lo, int64_t b_hi, int nthreads)
+{
+    int64_t C = (int64_t)R * bs, K = (int64_t)S * bs;
+    int64_t nnz = oracle_nnz(L, R, S);
+    int32_t *cb = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nnz ? nnz : 1));
+    int32_t *kb = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nnz ? nnz : 1));
+    int64_t e = 0;
+    for (int c = 0; c < R; ++c)
+        for (int k = 0; k < S; ++k)
+            if (L[(size_t)c * S + k]) {
+                cb[e] = c;
+                kb[e] = k;
+                ++e;
+            }
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t b = b_lo; b < b_hi; ++b)
+        for (int i = 0; i < bs; ++i)
+            for (int j = 0; j < bs; ++j) {
+                double s = 0.0;
+                for (int64_t n = 0; n < N; ++n)
+                    s += act(x, n, (int64_t)cb[b] * bs + i, N, C, fa) *
+                         act(dy, n, (int64_t)kb[b] * bs + j, N, K, fa);
+                double *o = &dw[(b * bs + i) * bs + j];
+                *o = accumulate ? *o + s : s;
+            }
+    free(cb);
+    free(kb);
+}
+
+/*
+ * Grouped updat (group_param_grads): dw[b] = (accumulate ? dw[b] : 0)
+ *   + sum_{t<G} updat(x_t, dy_t)[b], each step's sum formed first and then
+ * added in timestep order.  xs/dys point to G arrays of the activation shape.
+ */
+void oracle_updat_grouped(const uint8_t *L, int R, int S, int bs,
+                          const double *const *xs, const double *const *dys, int G,
+                          double *dw, int N, int fa, int accumulate, int nthreads)
+{
+    int64_t nnz = oracle_nnz(L, R, S);
+    int64_t sz = nnz * bs * bs;
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)(sz ? sz : 1));
+    if (!accumulate)
+        memset(dw, 0, sizeof(double) * (size_t)sz);
+    for (int t = 0; t < G; ++t) {
+        oracle_updat(L, R, S, bs, xs[t], dys[t], tmp, N, fa, 0, 0, nnz, nthreads);
+        for (int64_t q = 0; q < sz; ++q)
+            dw[q] += tmp[q];
+    }
+    free(tmp);
+}
+
+/*
+ * Single sampled outputs, computed straight from the definition without
+ * densifying W (for checks at sizes where the full product is too slow).
+ *   fprop_at: out[s] = y[n_s][f_s]   = sum_cc x[n][cc] * W(cc, f)
+ *   bprop_at: out[s] = dx[n_s][f_s]  = sum_kk dy[n][kk] * W(f, kk)
+ *   updat_at: out[s] = dw[b_s][i_s][j_s]
+ * W(cc, kk) is looked up through the block-id map.
+ */
+void oracle_fprop_at(const uint8_t *L, int R, int S, int bs, const double *w, const double *x,
+                     int N, int fa, const int64_t *n_s, const int64_t *f_s, int64_t count, double *out)
+{
+    int64_t C = (int64_t)R * bs, K = (int64_t)S * bs;
+    int32_t *bid = block_id_map(L, R, S);
+    for (int64_t s = 0; s < count; ++s) {
+        int64_t n = n_s[s], kk = f_s[s];
+        double acc = 0.0;
+        for (int64_t cc = 0; cc < C; ++cc) {
+            int32_t b = bid[(cc / bs) * S + kk / bs];
+            double wv = b < 0 ? 0.0 : w[((int64_t)b * bs + cc % bs) * bs + kk % bs];
+            acc += act(x, n, cc, N, C, fa) * wv;
+        }
+        out[s] = acc;
+    }
+    (void)K;
+    free(bid);
+}
+
+void oracle_bprop_at(const uint8_t *L, int R, int S, int bs, const double *w, const double *dy,
+                     int N, int fa, const int64_t *n_s, const int64_t *f_s, int64_t count, double *out)
+{
+    int64_t K = (int64_t)S * bs;
+    int32_t *bid = block_id_map(L, R, S);
+    for (int64_t s = 0; s < count; ++s) {
+        int64_t n = n_s[s], cc = f_s[s];
+        double acc = 0.0;
+        for (int64_t kk = 0; kk < K; ++kk) {
+            int32_t b = bid[(cc / bs) * S + kk / bs];
+            double wv = b < 0 ? 0.0 : w[((int64_t)b * bs + cc % bs) * bs + kk % bs];
+            acc += act(dy, n, kk, N, K, fa) * wv;
+        }
+        out[s] = acc;
+    }
+    free(bid);
+}
+
+void oracle_updat_at(const uint8_t *L, int R, int S, int bs, const double *x, const double *dy,
+                     int N, int fa, const int64_t *b_s, const int64_t *i_s, const int64_t *j_s,
+                     int64_t count, double *out)
+{
+    int64_t C = (int64_t)R * bs, K = (int64_t)S * bs;
+    int64_t nnz = oracle_nnz(L, R, S);
+    int32_t *cb = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nnz ? nnz : 1));
+    int32_t *kb = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nnz ? nnz : 1));
+    int64_t e = 0;
+    for (int c = 0; c < R; ++c)
+        for (int k = 0; k < S; ++k)
+            if (L[(size_t)c * S + k]) {
+                cb[e] = c;
+                kb[e] = k;
+                ++e;
+            }
+    for (int64_t s = 0; s < count; ++s) {
+        int64_t b = b_s[s];
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n)
+            acc += act(x, n, (int64_t)cb[b] * bs + i_s[s], N, C, fa) *
+                   act(dy, n, (int64_t)kb[b] * bs + j_s[s], N, K, fa);
+        out[s] = acc;
+    }
+    free(cb);
+    free(kb);
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,276 @@
+"""Pins for the CPU oracle: facts fixed by the blocksparse README and by plain
+mathematics, checked by routes that do not go through the oracle's own code.
+
+Each test names the passage or the property it relies on.  A plausible slip
+in the oracle (a transposed block, a wrong block order, a dropped block, a
+swapped feature_axis) fails at least one of them.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import oracle as o
+from block_sparse_matrix_gb300 import workloads as wk
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_layout(R, S, p, seed):
+    return (np.random.default_rng(seed).random((R, S)) < p).astype(np.uint8)
+
+
+def act(a, fa):
+    """(N, F) view of an activation stored in feature_axis `fa` layout."""
+    return a if fa == 1 else a.T
+
+
+def from_nf(a_nf, fa):
+    return a_nf if fa == 1 else np.ascontiguousarray(a_nf.T)
+
+
+def blocks_of_dense(L, bs, Wfull):
+    """Weight blocks cut out of a dense matrix, one per nonzero, in np.argwhere order."""
+    return np.stack([Wfull[c * bs:(c + 1) * bs, k * bs:(k + 1) * bs] for c, k in np.argwhere(L)]) \
+        if L.any() else np.zeros((0, bs, bs))
+
+
+def mask(L, bs):
+    return np.kron(L.astype(np.float64), np.ones((bs, bs)))
+
+
+# -- lookup tables / block_coord ("block_coord(block)" in the API listing) ----------
+
+@pytest.mark.parametrize("R,S,p,seed", [(8, 8, 0.5, 0), (5, 9, 0.3, 1), (16, 3, 0.7, 2),
+                                         (1, 1, 1.0, 3), (7, 7, 0.0, 4), (32, 32, 0.1, 5)])
+def test_luts_match_brute_force(R, S, p, seed):
+    L = rand_layout(R, S, p, seed)
+    row_ptr, row_ent, col_ptr, col_ent, coord = o.luts(L)
+    ref = np.argwhere(L)                          # row-major scan order
+    assert np.array_equal(coord, ref.astype(np.int32).reshape(-1, 2))
+    assert np.array_equal(row_ptr, np.concatenate([[0], np.cumsum(L.sum(1))]).astype(np.int32))
+    assert np.array_equal(col_ptr, np.concatenate([[0], np.cumsum(L.sum(0))]).astype(np.int32))
+    assert np.array_equal(row_ent, ref[:, 1].astype(np.int32))
+    ids = {tuple(ck): b for b, ck in enumerate(ref)}
+    for k in range(S):
+        seg = col_ent[col_ptr[k]:col_ptr[k + 1]]
+        cs = np.nonzero(L[:, k])[0]
+        assert np.array_equal(seg[:, 1], cs)
+        assert all(seg[i, 0] == ids[(c, k)] for i, c in enumerate(cs))
+
+
+# -- the dense special cases ----------------------------------------------------
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("fa", [0, 1])
+def test_all_ones_layout_is_dense_matmul(bs, fa):
+    """An all-ones layout makes W dense; y = x.W, dx = dy.W^T, dW = x^T.dy (numpy)."""
+    R, S, N = 3, 2, 5
+    rng = np.random.default_rng(bs + fa)
+    L = np.ones((R, S), np.uint8)
+    C, K = R * bs, S * bs
+    Wfull = rng.standard_normal((C, K))
+    w = Wfull.reshape(R, bs, S, bs).transpose(0, 2, 1, 3).reshape(R * S, bs, bs)
+    x_nf, dy_nf = rng.standard_normal((N, C)), rng.standard_normal((N, K))
+    x, dy = from_nf(x_nf, fa), from_nf(dy_nf, fa)
+    np.testing.assert_allclose(act(o.fprop(L, bs, x, w, fa), fa), x_nf @ Wfull, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(act(o.bprop(L, bs, dy, w, fa), fa), dy_nf @ Wfull.T, rtol=1e-12, atol=1e-12)
+    G = x_nf.T @ dy_nf
+    dw_ref = G.reshape(R, bs, S, bs).transpose(0, 2, 1, 3).reshape(R * S, bs, bs)
+    np.testing.assert_allclose(o.updat(L, bs, x, dy, fa), dw_ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("bs,fa,seed", [(8, 1, 0), (16, 0, 1), (32, 1, 2), (8, 0, 3)])
+def test_random_layout_equals_masked_dense(bs, fa, seed):
+    """W = (dense matrix) * (layout expanded to bs x bs); blocks in block_coord order."""
+    R, S, N = 6, 5, 7
+    rng = np.random.default_rng(100 + seed)
+    L = rand_layout(R, S, 0.45, seed)
+    L[0, :] = 0          # an empty block row
+    L[:, 2] = 0          # an empty block column
+    Wfull = rng.standard_normal((R * bs, S * bs))
+    w = blocks_of_dense(L, bs, Wfull)
+    Wm = Wfull * mask(L, bs)
+    x_nf, dy_nf = rng.standard_normal((N, R * bs)), rng.standard_normal((N, S * bs))
+    x, dy = from_nf(x_nf, fa), from_nf(dy_nf, fa)
+    np.testing.assert_allclose(o.densify(L, bs, w), Wm, rtol=0, atol=0)
+    np.testing.assert_allclose(act(o.fprop(L, bs, x, w, fa), fa), x_nf @ Wm, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(act(o.bprop(L, bs, dy, w, fa), fa), dy_nf @ Wm.T, rtol=1e-12, atol=1e-12)
+    dw_ref = blocks_of_dense(L, bs, x_nf.T @ dy_nf)
+    np.testing.assert_allclose(o.updat(L, bs, x, dy, fa), dw_ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("fa", [0, 1])
+def test_all_zero_layout_gives_zeros(fa):
+    L = np.zeros((4, 3), np.uint8)
+    bs, N = 16, 6
+    x = np.random.default_rng(0).standard_normal(wk.act_shape(4 * bs, N, fa))
+    dy = np.random.default_rng(1).standard_normal(wk.act_shape(3 * bs, N, fa))
+    w = np.zeros((0, bs, bs))
+    assert not o.fprop(L, bs, x, w, fa).any()
+    assert not o.bprop(L, bs, dy, w, fa).any()
+    assert o.updat(L, bs, x, dy, fa).shape == (0, bs, bs)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("fa", [0, 1])
+def test_identity_init_block_diagonal_is_identity(bs, fa):
+    """identity_init ("identity_init + layernorm is all you need") on a block-diagonal
+    layout gives y = x and dx = dy exactly; with off-diagonal blocks present they are 0."""
+    R = 4
+    N = 9
+    L = np.eye(R, dtype=np.uint8)
+    w = o.identity_init(L, bs)
+    x = np.random.default_rng(bs).standard_normal(wk.act_shape(R * bs, N, fa))
+    assert np.array_equal(o.fprop(L, bs, x, w, fa), x)
+    assert np.array_equal(o.bprop(L, bs, x, w, fa), x)
+    L2 = L.copy()
+    L2[0, 3] = L2[2, 1] = 1
+    w2 = o.identity_init(L2, bs)
+    assert np.array_equal(o.fprop(L2, bs, x, w2, fa), x)
+    assert np.array_equal(o.densify(L2, bs, w2), np.eye(R * bs))
+    # a missing diagonal block leaves its output block zero
+    L3 = L.copy()
+    L3[1, 1] = 0
+    y3 = act(o.fprop(L3, bs, x, o.identity_init(L3, bs), fa), fa)
+    assert not y3[:, bs:2 * bs].any()
+    assert np.array_equal(y3[:, :bs], act(x, fa)[:, :bs])
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("fa", [0, 1])
+def test_brute_force_2x2_layouts_integers(bs, fa):
+    """All 16 patterns of a 2x2-block layout, small-integer inputs (exact in fp32),
+    against a block-by-block accumulation written independently here."""
+    N = 4
+    for bits in itertools.product([0, 1], repeat=4):
+        L = np.array(bits, np.uint8).reshape(2, 2)
+        z = int(L.sum())
+        rng = np.random.default_rng(int("".join(map(str, bits)), 2) + 10 * bs + fa)
+        w = rng.integers(-1, 2, (z, bs, bs)).astype(np.float64)
+        x_nf = rng.integers(-1, 2, (N, 2 * bs)).astype(np.float64)
+        dy_nf = rng.integers(-1, 2, (N, 2 * bs)).astype(np.float64)
+        y = np.zeros((N, 2 * bs))
+        dx = np.zeros((N, 2 * bs))
+        dw = np.zeros((z, bs, bs))
+        b = 0
+        for c in range(2):
+            for k in range(2):
+                if not L[c, k]:
+                    continue
+                xs, ks = slice(c * bs, (c + 1) * bs), slice(k * bs, (k + 1) * bs)
+                for n in range(N):
+                    for i in range(bs):
+                        for j in range(bs):
+                            y[n, k * bs + j] += x_nf[n, c * bs + i] * w[b, i, j]
+                            dx[n, c * bs + i] += dy_nf[n, k * bs + j] * w[b, i, j]
+                            dw[b, i, j] += x_nf[n, c * bs + i] * dy_nf[n, k * bs + j]
+                b += 1
+        x, dy = from_nf(x_nf, fa), from_nf(dy_nf, fa)
+        assert np.array_equal(act(o.fprop(L, bs, x, w, fa), fa), y)
+        assert np.array_equal(act(o.bprop(L, bs, dy, w, fa), fa), dx)
+        assert np.array_equal(o.updat(L, bs, x, dy, fa), dw)
+
+
+# -- invariants -----------------------------------------------------------------
+
+@pytest.mark.parametrize("bs,fa", [(8, 0), (16, 1), (32, 0)])
+def test_adjoint_identity(bs, fa):
+    """<x.W, dy> = <x, dy.W^T> = <dW, w> where dW = updat(x, dy)."""
+    R, S, N = 5, 4, 6
+    rng = np.random.default_rng(7 * bs + fa)
+    L = rand_layout(R, S, 0.5, bs)
+    w = rng.standard_normal((int(L.sum()), bs, bs))
+    x = rng.standard_normal(wk.act_shape(R * bs, N, fa))
+    dy = rng.standard_normal(wk.act_shape(S * bs, N, fa))
+    a = np.sum(o.fprop(L, bs, x, w, fa) * dy)
+    b = np.sum(x * o.bprop(L, bs, dy, w, fa))
+    c = np.sum(o.updat(L, bs, x, dy, fa) * w)
+    assert abs(a - b) <= 1e-10 * abs(a) + 1e-10
+    assert abs(a - c) <= 1e-10 * abs(a) + 1e-10
+
+
+@pytest.mark.parametrize("bs", [8, 32])
+def test_feature_axis_transpose(bs):
+    """feature_axis=0 on transposed activations gives the transposed feature_axis=1 result."""
+    R, S, N = 3, 4, 5
+    rng = np.random.default_rng(bs)
+    L = rand_layout(R, S, 0.6, 9)
+    w = rng.standard_normal((int(L.sum()), bs, bs))
+    x = rng.standard_normal((N, R * bs))
+    dy = rng.standard_normal((N, S * bs))
+    assert np.array_equal(o.fprop(L, bs, x.T.copy(), w, 0), o.fprop(L, bs, x, w, 1).T)
+    assert np.array_equal(o.bprop(L, bs, dy.T.copy(), w, 0), o.bprop(L, bs, dy, w, 1).T)
+    assert np.array_equal(o.updat(L, bs, x.T.copy(), dy.T.copy(), 0), o.updat(L, bs, x, dy, 1))
+
+
+@pytest.mark.parametrize("fa", [0, 1])
+def test_grouped_is_sum_of_steps_and_concat(fa):
+    """group_param_grads: the grouped weight gradient equals the per-step sum and the
+    single updat over the minibatch concatenation of the steps."""
+    bs, R, S, N, G = 8, 4, 3, 5, 5
+    rng = np.random.default_rng(fa)
+    L = rand_layout(R, S, 0.5, 11)
+    xs = [rng.standard_normal(wk.act_shape(R * bs, N, fa)) for _ in range(G)]
+    dys = [rng.standard_normal(wk.act_shape(S * bs, N, fa)) for _ in range(G)]
+    g = o.updat_grouped(L, bs, xs, dys, fa)
+    s = sum(o.updat(L, bs, a, d, fa) for a, d in zip(xs, dys))
+    ax = 0 if fa == 1 else 1
+    cat = o.updat(L, bs, np.concatenate(xs, axis=ax), np.concatenate(dys, axis=ax), fa)
+    np.testing.assert_allclose(g, s, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g, cat, rtol=1e-12, atol=1e-12)
+    init = rng.standard_normal(g.shape)
+    np.testing.assert_allclose(o.updat_grouped(L, bs, xs, dys, fa, dw_init=init), g + init,
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(o.updat(L, bs, xs[0], dys[0], fa, dw_init=init),
+                               o.updat(L, bs, xs[0], dys[0], fa) + init, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("bs,fa", [(8, 1), (16, 0), (32, 1)])
+def test_sampled_outputs_equal_full(bs, fa):
+    R, S, N = 4, 5, 6
+    rng = np.random.default_rng(3 * bs + fa)
+    L = rand_layout(R, S, 0.5, 21)
+    w = rng.standard_normal((int(L.sum()), bs, bs))
+    x = rng.standard_normal(wk.act_shape(R * bs, N, fa))
+    dy = rng.standard_normal(wk.act_shape(S * bs, N, fa))
+    y, dx, dw = o.fprop(L, bs, x, w, fa), o.bprop(L, bs, dy, w, fa), o.updat(L, bs, x, dy, fa)
+    n = rng.integers(0, N, 50)
+    fk = rng.integers(0, S * bs, 50)
+    fc = rng.integers(0, R * bs, 50)
+    np.testing.assert_allclose(o.fprop_at(L, bs, w, x, fa, n, fk), act(y, fa)[n, fk], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(o.bprop_at(L, bs, w, dy, fa, n, fc), act(dx, fa)[n, fc], rtol=1e-13, atol=1e-13)
+    b = rng.integers(0, len(w), 50)
+    i = rng.integers(0, bs, 50)
+    j = rng.integers(0, bs, 50)
+    np.testing.assert_allclose(o.updat_at(L, bs, x, dy, fa, b, i, j), dw[b, i, j], rtol=1e-13, atol=1e-13)
+
+
+def test_golden_usage_example_ones():
+    """Hand-worked values for the README 'Usage' example pattern (x = ones)."""
+    with open(os.path.join(GOLDEN, "usage_ones.json")) as f:
+        g = json.load(f)
+    L = np.array(g["layout"], np.uint8)
+    bs, N = g["block_size"], g["N"]
+    w = np.stack([np.full((bs, bs), float((b + 1) ** 2)) for b in range(int(L.sum()))])
+    C, K = L.shape[0] * bs, L.shape[1] * bs
+    for fa in (0, 1):
+        y = act(o.fprop(L, bs, np.ones(wk.act_shape(C, N, fa)), w, fa), fa)
+        assert np.array_equal(y, np.tile(g["fprop_x_ones_expected_row"], (N, 1)))
+        dx = act(o.bprop(L, bs, np.ones(wk.act_shape(K, N, fa)), w, fa), fa)
+        assert np.array_equal(dx, np.tile(g["bprop_dy_ones_expected_row"], (N, 1)))
+        dw = o.updat(L, bs, np.ones(wk.act_shape(C, N, fa)), np.ones(wk.act_shape(K, N, fa)), fa)
+        assert np.all(dw == g["updat_ones_expected"])
+
+
+def test_workload_layouts():
+    """The synthetic layouts have the stated structure (diagonal forced, 8 extra per row)."""
+    for name in ("cfg1", "cfg3", "cfg4"):
+        wl = wk.CONFIGS[name]
+        L = wk.make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 1000 * wl.cfg)
+        assert np.all(np.diag(L) == 1)
+    wl = wk.CONFIGS["cfg5"]
+    L = wk.make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 5000)
+    assert np.all(L.sum(1) == 9) and np.all(np.diag(L) == 1)
