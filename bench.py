@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-sparse matmul hot path on GB300.
+
+One step = fprop + bprop + updat of the hidden-4096, block-32, 50%-dense
+layout (128 x 128 Bernoulli(0.5) blocks), bf16 activations in (N, C) layout,
+at minibatch N = 1024 and N = 64 (six passes).  The metric is effective
+TFLOP/s = 2 * N * nnz * bs^2 per pass, summed over the step, divided by the
+device time of the step.
+
+Timing: W warm-up steps, then exactly K timed steps.  Four input/output sets
+(each ~83 MB, together > 2x the 129 MB L2) rotate between steps, so every step
+reads cold inputs.  Steps are enqueued in chunks behind a short device sleep so
+that the host never starves the GPU inside a chunk; CUDA events on the
+launching stream bracket every step and every pass, and the reported device
+time is the sum of the per-step event intervals.
+
+--impl reference times the float64 CPU oracle (the only other implementation
+of the method here) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_matrix_gb300 import workloads as wk  # noqa: E402
+
+METRIC = "effective TFLOP/s per pass (fprop/bprop/updat) and % of roofline on 1 GB300"
+WORKLOAD = ("hidden C=K=4096, block_size=32, 128x128 Bernoulli(0.5) layout, bf16 inputs with fp32 accumulate, "
+            "feature_axis=1 (N,C); one step = fprop+bprop+updat at N=1024 and at N=64")
+NSETS = 4
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---- pass bookkeeping -------------------------------------------------------------------
+
+def pass_list(nnz, bs, C, K, Ns, e=2):
+    """(name, N, effective flops, algorithmic bytes) per pass of one step."""
+    out = []
+    for N in Ns:
+        f = wk.effective_flops(N, nnz, bs)
+        wbytes = nnz * bs * bs * e
+        out.append(("fprop_n%d" % N, N, f, (N * C + N * K) * e + wbytes))
+        out.append(("bprop_n%d" % N, N, f, (N * C + N * K) * e + wbytes))
+        out.append(("updat_n%d" % N, N, f, (N * C + N * K) * e + nnz * bs * bs * 4))
+    return out
+
+
+def roof_time(flops, bytes_, peaks):
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    return max(t_tc, t_hbm), ("tensor" if t_tc >= t_hbm else "hbm")
+
+
+# ---- clocks ------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- our implementation --------------------------------------------------------------------
+
+def traffic_for(kernel_pass):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("src_sha") != source_sha():
+        return None
+    return d.get("passes", {}).get(kernel_pass)
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_sparse_matrix_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def run_ours(args):
+    from block_sparse_matrix_gb300 import bsmm
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = wk.CONFIGS["cfg2_n1024"]
+    Ns = [1024, 64]
+    inp = wk.make_inputs(wl)
+    L, bs, C, K = inp.layout, wl.bs, wl.C, wl.K
+    m = bsmm.BlocksparseMatMul(L, block_size=bs, feature_axis=1)
+    nnz = m.nnz
+    passes = pass_list(nnz, bs, C, K, Ns)
+    step_flops = sum(p[2] for p in passes)
+
+    # Rotating device sets: inputs (x, dy per N, w) and outputs (y, dx per N, dw per N).
+    sets = []
+    for s in range(NSETS):
+        d = {"w": (inp.w if s == 0 else wk.normals(inp.w.shape, 9000 + s, float(np.sqrt(wl.w_var)),
+                                                    wl.dtype)).to(dev)}
+        for N in Ns:
+            d["x%d" % N] = wk.normals((N, C), 9100 + 10 * s + N % 7, 1.0, wl.dtype).to(dev)
+            d["dy%d" % N] = wk.normals((N, K), 9200 + 10 * s + N % 7, 1.0, wl.dtype).to(dev)
+            d["y%d" % N] = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+            d["dx%d" % N] = torch.empty((N, C), dtype=torch.bfloat16, device=dev)
+            d["dw%d" % N] = torch.empty((nnz, bs, bs), dtype=torch.float32, device=dev)
+        sets.append(d)
+    stream = torch.cuda.current_stream()
+
+    def launch_pass(name, d):
+        kind, n = name.split("_n")
+        N = int(n)
+        if kind == "fprop":
+            bsmm.bsmm_fprop(m.handle, d["x%d" % N], d["w"], d["y%d" % N], N)
+        elif kind == "bprop":
+            bsmm.bsmm_bprop(m.handle, d["dy%d" % N], d["w"], d["dx%d" % N], N)
+        else:
+            bsmm.bsmm_updat(m.handle, d["x%d" % N], d["dy%d" % N], d["dw%d" % N], N)
+
+    def step(i):
+        d = sets[i % NSETS]
+        for p in passes:
+            launch_pass(p[0], d)
+
+    # Warm-up (W steps), then count our launches per step.
+    warm = max(3, args.warmup)
+    for i in range(warm):
+        step(i)
+    torch.cuda.synchronize()
+    m.sync_status()
+    c0 = bsmm.launch_count()
+    step(0)
+    torch.cuda.synchronize()
+    launches_per_step = bsmm.launch_count() - c0
+
+    # Host enqueue time per step -> device sleep long enough to cover a chunk.
+    t0 = time.perf_counter()
+    for i in range(20):
+        step(i)
+    host_step_s = (time.perf_counter() - t0) / 20
+    torch.cuda.synchronize()
+    chunk = 50
+    sleep_cycles = int(host_step_s * 1.3 * chunk * 2.1e9) + 100000   # cycles at <= 2.1 GHz
+
+    K_steps = args.steps
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+    ev_pass = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in passes]
+               for _ in range(K_steps)]
+    sampler = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for c0 in range(0, K_steps, chunk):
+        torch.cuda._sleep(sleep_cycles)
+        for i in range(c0, min(K_steps, c0 + chunk)):
+            d = sets[i % NSETS]
+            ev_step[i][0].record(stream)
+            for j, p in enumerate(passes):
+                ev_pass[i][j][0].record(stream)
+                launch_pass(p[0], d)
+                ev_pass[i][j][1].record(stream)
+            ev_step[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    m.sync_status()
+
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    dev_ms = sum(step_ms)
+    pass_us = {}
+    for j, p in enumerate(passes):
+        pass_us[p[0]] = 1000.0 * sum(ev_pass[i][j][0].elapsed_time(ev_pass[i][j][1]) for i in range(K_steps)) / K_steps
+    if ws > 1:
+        t = torch.tensor([dev_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dev_ms = float(t.item())
+    ms_per_step = dev_ms / K_steps
+    value = ws * step_flops * K_steps / (dev_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    per_pass = {}
+    for name, N, f, b in passes:
+        t = pass_us[name] * 1e-6
+        tr, bound = roof_time(f, b, peaks)
+        per_pass[name] = {"us": round(pass_us[name], 3), "tflops": round(f / t / 1e12, 2),
+                          "gbs": round(b / t / 1e9, 1), "roofline_us": round(tr * 1e6, 3), "bound": bound,
+                          "roofline_frac": round(tr / t, 4)}
+    dom = max(passes, key=lambda p: pass_us[p[0]])
+    name, N, f, b = dom
+    t = pass_us[name] * 1e-6
+    tr, bound = roof_time(f, b, peaks)
+    if bound == "tensor":
+        achieved, peak, unit = f / t / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = b / t / 1e9, peaks["hbm_gbs"], "GB/s"
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": traffic_for(name), "kernel": name,
+                "algorithmic_bytes": b, "flops": f, "peak_source": peak_src + " (burst)"}
+
+    e2e = run_e2e(m, inp, Ns, passes, dev, args) if rank == 0 else None
+    cpu = (run_cpu_baseline(wl, inp, Ns, budget_s=args.cpu_budget)
+           if (rank == 0 and ws == 1 and args.cpu_budget > 0) else None)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": K_steps,
+                "warmup": warm, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normals)",
+                "config": {"workload": WORKLOAD, "nnz": nnz, "l2": "4 rotating input/output sets, ~330 MB > 2x L2",
+                           "parallelism": "replicas" if ws > 1 else "single GPU"},
+                "passes": per_pass, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clocks, "gpu_launches": launches_per_step * K_steps,
+                "wall_s_timed_region": round(wall1 - wall0, 3)}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(m, inp, Ns, passes, dev, args):
+    """The same step through the public API from pinned HOST buffers: H2D of the
+    step's inputs, the six passes, D2H of the results, all inside the timed region."""
+    from block_sparse_matrix_gb300 import bsmm
+    wl = wk.CONFIGS["cfg2_n1024"]
+    C, K, bs, nnz = wl.C, wl.K, wl.bs, m.nnz
+    host = {"w": inp.w.pin_memory()}
+    devb = {"w": torch.empty_like(inp.w, device=dev)}
+    for N in Ns:
+        host["x%d" % N] = wk.normals((N, C), 9300 + N, 1.0, wl.dtype).pin_memory()
+        host["dy%d" % N] = wk.normals((N, K), 9400 + N, 1.0, wl.dtype).pin_memory()
+        for k, shape, dt in (("y", (N, K), torch.bfloat16), ("dx", (N, C), torch.bfloat16),
+                             ("dw", (nnz, bs, bs), torch.float32)):
+            host["%s%d" % (k, N)] = torch.empty(shape, dtype=dt).pin_memory()
+        for k in ("x", "dy", "y", "dx", "dw"):
+            devb["%s%d" % (k, N)] = torch.empty_like(host["%s%d" % (k, N)], device=dev)
+    ins = ["w"] + ["x%d" % N for N in Ns] + ["dy%d" % N for N in Ns]
+    outs = ["%s%d" % (k, N) for N in Ns for k in ("y", "dx", "dw")]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in ins)
+    d2h = sum(host[k].numel() * host[k].element_size() for k in outs)
+    steps = max(10, min(args.steps, 200))
+
+    def one():
+        for k in ins:
+            devb[k].copy_(host[k], non_blocking=True)
+        for name, N, _, _ in passes:
+            kind = name.split("_n")[0]
+            if kind == "fprop":
+                bsmm.bsmm_fprop(m.handle, devb["x%d" % N], devb["w"], devb["y%d" % N], N)
+            elif kind == "bprop":
+                bsmm.bsmm_bprop(m.handle, devb["dy%d" % N], devb["w"], devb["dx%d" % N], N)
+            else:
+                bsmm.bsmm_updat(m.handle, devb["x%d" % N], devb["dy%d" % N], devb["dw%d" % N], N)
+        for k in outs:
+            host[k].copy_(devb[k], non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    flops = sum(p[2] for p in passes)
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4), "steps": steps}
+
+
+# ---- CPU oracle --------------------------------------------------------------------------
+
+def oracle_sample(wl, inp, n_rows, n_blocks, nthreads, N):
+    """One bounded sample of the step on the oracle: n_rows minibatch rows of fprop
+    and bprop and n_blocks blocks of updat at minibatch N.  Returns (eff. flops, s)."""
+    from oracle import oracle as o
+    L, bs = inp.layout, wl.bs
+    x = inp.x[:N].double().numpy()
+    dy = inp.dy[:N].double().numpy()
+    w = inp.w.double().numpy()
+    t0 = time.perf_counter()
+    o.fprop(L, bs, x, w, 1, rows=(0, n_rows), nthreads=nthreads)
+    o.bprop(L, bs, dy, w, 1, rows=(0, n_rows), nthreads=nthreads)
+    o.updat(L, bs, x, dy, 1, blocks=(0, n_blocks), nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    nnz = inp.nnz
+    flops = 2 * n_rows * nnz * bs * bs * 2 + 2 * N * n_blocks * bs * bs
+    return flops, dt
+
+
+def run_cpu_baseline(wl, inp, Ns, budget_s=10.0):
+    from oracle import oracle as o
+    o.build()
+    nthreads = len(os.sched_getaffinity(0))
+    # calibrate on one row / a few blocks, then size the sample to the budget
+    f1, t1 = oracle_sample(wl, inp, nthreads, 64, nthreads, 1024)
+    scale = max(1, int(budget_s / max(t1, 1e-3)))
+    rows = min(1024, nthreads * scale)
+    blocks = min(inp.nnz, 64 * scale)
+    f, t = oracle_sample(wl, inp, rows, blocks, nthreads, 1024)
+    return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+            "sample": "float64 dense-W oracle at N=1024: fprop and bprop of %d minibatch rows, updat of %d blocks "
+                      "(%.1f s); effective FLOPs 2*rows*nnz*bs^2 per fwd/bwd + 2*N*bs^2 per block" % (rows, blocks, t)}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import oracle as o
+    o.build()
+    wl = wk.CONFIGS["cfg2_n1024"]
+    inp = wk.make_inputs(wl)
+    nthreads = len(os.sched_getaffinity(0))
+    rows, blocks = nthreads, 128
+    for _ in range(args.warmup):
+        oracle_sample(wl, inp, rows, blocks, nthreads, 1024)
+    tot_f = tot_t = 0.0
+    for _ in range(args.steps):
+        f, t = oracle_sample(wl, inp, rows, blocks, nthreads, 1024)
+        tot_f += f
+        tot_t += t
+    v = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * tot_t / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded normals)",
+            "config": {"workload": WORKLOAD, "nnz": inp.nnz},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+                             "sample": "per step: fprop+bprop of %d rows and updat of %d blocks at N=1024" %
+                                       (rows, blocks)},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

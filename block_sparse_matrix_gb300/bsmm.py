@@ -1,0 +1,290 @@
+"""Thin ctypes binding of libbsmm (include/bsmm.h).
+
+Argument marshalling only: every step of every pass runs in the CUDA library.
+Torch tensors supply device memory and the current stream.  There is no CPU
+fallback: if libbsmm.so is missing or fails to load, every call raises.
+
+Module-level functions carry the C names (bsmm_create, bsmm_fprop, ...);
+``BlocksparseMatMul`` wraps them with the shape helpers of the blocksparse
+README ("API Documentation: blocksparse.matmul": w_shape, i_shape, o_shape,
+block_coord, identity_init, __call__) and of group_param_grads.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbsmm.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_ALIGN, ERR_CUDA, ERR_TIMEOUT, ERR_OOM, ERR_BOUNDS = range(8)
+F32, F16, BF16 = 0, 1, 2
+KERNELS = {"auto": 0, "simt": 1, "tc": 2}
+_DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+_lib = None
+
+
+class BsmmError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__("%s: %s (status %d)" % (what, status_string(code), code))
+
+
+def lib():
+    """Load libbsmm.so (build it first with __graft_entry__.build() or build.py)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libbsmm.so not built at %s; run block_sparse_matrix_gb300/build.py" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        pi, pi64, pi32 = ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+        sig = {
+            "bsmm_create": [ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_uint8), i, i, i, i, vp],
+            "bsmm_destroy": [vp],
+            "bsmm_w_shape": [vp, pi64, pi],
+            "bsmm_layout_info": [vp, pi, pi, pi],
+            "bsmm_block_coord": [vp, i64, pi, pi],
+            "bsmm_get_luts": [vp, pi32, pi32, pi32, pi32, pi32],
+            "bsmm_identity_init": [vp, vp, i, vp],
+            "bsmm_fprop": [vp, vp, vp, vp, i, i, vp],
+            "bsmm_bprop": [vp, vp, vp, vp, i, i, vp],
+            "bsmm_updat": [vp, vp, vp, vp, i, i, i, i, vp],
+            "bsmm_updat_grouped": [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i, i, i, vp, i, vp],
+            "bsmm_set_kernel": [vp, i],
+            "bsmm_sync_status": [vp, vp],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        L.bsmm_status_string.argtypes = [ctypes.c_int]
+        L.bsmm_status_string.restype = ctypes.c_char_p
+        L.bsmm_launch_count.argtypes = []
+        L.bsmm_launch_count.restype = ctypes.c_int64
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().bsmm_status_string(code).decode()
+
+
+def launch_count() -> int:
+    return int(lib().bsmm_launch_count())
+
+
+def _check(code, what):
+    if code != OK:
+        raise BsmmError(code, what)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _dev(t, what):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+
+
+# ---- C-named wrappers --------------------------------------------------------------
+
+def bsmm_create(layout, block_size: int = 32, feature_axis: int = 1, stream=None):
+    lay = np.ascontiguousarray(np.asarray(layout) != 0, dtype=np.uint8)
+    if lay.ndim != 2:
+        raise ValueError("layout must be 2-D")
+    h = ctypes.c_void_p()
+    _check(lib().bsmm_create(ctypes.byref(h), lay.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+                             lay.shape[0], lay.shape[1], block_size, feature_axis, _stream(stream)),
+           "bsmm_create")
+    return h
+
+
+def bsmm_destroy(h):
+    _check(lib().bsmm_destroy(h), "bsmm_destroy")
+
+
+def bsmm_identity_init(h, w, stream=None):
+    _dev(w, "w")
+    _check(lib().bsmm_identity_init(h, _ptr(w), _DT[w.dtype], _stream(stream)), "bsmm_identity_init")
+
+
+def bsmm_fprop(h, x, w, y, N: int, stream=None):
+    _check(lib().bsmm_fprop(h, _ptr(x), _ptr(w), _ptr(y), N, _DT[x.dtype], _stream(stream)), "bsmm_fprop")
+
+
+def bsmm_bprop(h, dy, w, dx, N: int, stream=None):
+    _check(lib().bsmm_bprop(h, _ptr(dy), _ptr(w), _ptr(dx), N, _DT[dy.dtype], _stream(stream)), "bsmm_bprop")
+
+
+def bsmm_updat(h, x, dy, dw, N: int, accumulate: bool = False, stream=None):
+    _check(lib().bsmm_updat(h, _ptr(x), _ptr(dy), _ptr(dw), N, _DT[x.dtype], _DT[dw.dtype], int(accumulate),
+                            _stream(stream)), "bsmm_updat")
+
+
+def bsmm_updat_grouped(h, xs, dys, dw, N: int, accumulate: bool = False, stream=None):
+    G = len(xs)
+    xa = (ctypes.c_void_p * max(G, 1))(*[t.data_ptr() for t in xs])
+    da = (ctypes.c_void_p * max(G, 1))(*[t.data_ptr() for t in dys])
+    dt = _DT[xs[0].dtype] if G else F32
+    _check(lib().bsmm_updat_grouped(h, xa, da, G, N, dt, _ptr(dw), int(accumulate), _stream(stream)),
+           "bsmm_updat_grouped")
+
+
+def bsmm_sync_status(h, stream=None):
+    _check(lib().bsmm_sync_status(h, _stream(stream)), "bsmm_sync_status")
+
+
+# ---- README-style object -------------------------------------------------------------
+
+class BlocksparseMatMul:
+    """BlocksparseMatMul(layout, block_size=32, feature_axis=1) on the current CUDA device."""
+
+    def __init__(self, layout, block_size: int = 32, feature_axis: int = 1):
+        self.layout = np.ascontiguousarray(np.asarray(layout) != 0, dtype=np.uint8)
+        self.block_size = block_size
+        self.feature_axis = feature_axis
+        self._h = bsmm_create(self.layout, block_size, feature_axis)
+        nnz = ctypes.c_int64()
+        bs = ctypes.c_int()
+        _check(lib().bsmm_w_shape(self._h, ctypes.byref(nnz), ctypes.byref(bs)), "bsmm_w_shape")
+        self.nnz = int(nnz.value)
+        self.C = self.layout.shape[0] * block_size
+        self.K = self.layout.shape[1] * block_size
+
+    def close(self):
+        if getattr(self, "_h", None):
+            bsmm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    # shape helpers
+    @property
+    def w_shape(self):
+        return (self.nnz, self.block_size, self.block_size)
+
+    def i_shape(self, N):
+        return (N, self.C) if self.feature_axis == 1 else (self.C, N)
+
+    def o_shape(self, N):
+        return (N, self.K) if self.feature_axis == 1 else (self.K, N)
+
+    def _N(self, a, F):
+        if a.dim() != 2:
+            raise ValueError("activations must be 2-D")
+        if self.feature_axis == 1:
+            if a.shape[1] != F:
+                raise ValueError("activation shape %s does not match feature size %d" % (tuple(a.shape), F))
+            return a.shape[0]
+        if a.shape[0] != F:
+            raise ValueError("activation shape %s does not match feature size %d" % (tuple(a.shape), F))
+        return a.shape[1]
+
+    def block_coord(self, block: int):
+        c, k = ctypes.c_int(), ctypes.c_int()
+        _check(lib().bsmm_block_coord(self._h, int(block), ctypes.byref(c), ctypes.byref(k)), "bsmm_block_coord")
+        return c.value, k.value
+
+    def get_luts(self):
+        R, S = self.layout.shape
+        z = max(self.nnz, 1)
+        row_ptr = np.zeros(R + 1, np.int32)
+        col_ptr = np.zeros(S + 1, np.int32)
+        row_ent = np.zeros(z, np.int32)
+        col_ent = np.zeros(2 * z, np.int32)
+        coord = np.zeros(2 * z, np.int32)
+        p = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        _check(lib().bsmm_get_luts(self._h, p(row_ptr), p(row_ent), p(col_ptr), p(col_ent), p(coord)),
+               "bsmm_get_luts")
+        n = self.nnz
+        return row_ptr, row_ent[:n], col_ptr, col_ent[:2 * n].reshape(n, 2), coord[:2 * n].reshape(n, 2)
+
+    def set_kernel(self, which: str):
+        _check(lib().bsmm_set_kernel(self._h, KERNELS[which]), "bsmm_set_kernel")
+
+    def sync_status(self, stream=None):
+        bsmm_sync_status(self._h, stream)
+
+    def identity_init(self, w=None, dtype=torch.float32, device="cuda"):
+        if w is None:
+            w = torch.empty(self.w_shape, dtype=dtype, device=device)
+        _dev(w, "w")
+        bsmm_identity_init(self._h, w)
+        return w
+
+    def fprop(self, x, w, y=None, stream=None):
+        _dev(x, "x")
+        _dev(w, "w")
+        N = self._N(x, self.C)
+        if y is None:
+            y = torch.empty(self.o_shape(N), dtype=x.dtype, device=x.device)
+        bsmm_fprop(self._h, x, w, y, N, stream)
+        return y
+
+    __call__ = fprop
+
+    def bprop(self, dy, w, dx=None, stream=None):
+        _dev(dy, "dy")
+        _dev(w, "w")
+        N = self._N(dy, self.K)
+        if dx is None:
+            dx = torch.empty(self.i_shape(N), dtype=dy.dtype, device=dy.device)
+        bsmm_bprop(self._h, dy, w, dx, N, stream)
+        return dx
+
+    def updat(self, x, dy, dw=None, accumulate=False, dw_dtype=torch.float32, stream=None):
+        _dev(x, "x")
+        _dev(dy, "dy")
+        N = self._N(x, self.C)
+        if self._N(dy, self.K) != N:
+            raise ValueError("x and dy minibatch sizes differ")
+        if dw is None:
+            dw = torch.empty(self.w_shape, dtype=dw_dtype, device=x.device)
+        bsmm_updat(self._h, x, dy, dw, N, accumulate, stream)
+        return dw
+
+    def updat_grouped(self, xs, dys, dw=None, accumulate=False, stream=None):
+        if len(xs) != len(dys) or not 1 <= len(xs) <= 8:
+            raise ValueError("need 1..8 (x, dy) pairs")
+        for a in list(xs) + list(dys):
+            _dev(a, "activation")
+        N = self._N(xs[0], self.C)
+        if dw is None:
+            dw = torch.empty(self.w_shape, dtype=torch.float32, device=xs[0].device)
+        bsmm_updat_grouped(self._h, xs, dys, dw, N, accumulate, stream)
+        return dw
+
+
+def group_param_grads(bsmm: BlocksparseMatMul, xs, dys, group_size: int = 8, dw=None, accumulate=False):
+    """Sum of the weight gradients of all timesteps (x_t, dy_t) sharing one weight,
+    computed group_size (<= 8) timesteps per call into one float32 dW."""
+    if not 1 <= group_size <= 8:
+        raise ValueError("group_size must be in 1..8")
+    for g0 in range(0, len(xs), group_size):
+        dw = bsmm.updat_grouped(xs[g0:g0 + group_size], dys[g0:g0 + group_size], dw=dw,
+                                accumulate=accumulate or g0 > 0)
+    return dw

@@ -1,0 +1,76 @@
+// Internal declarations shared by the libbsmm translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <vector>
+
+#include "bsmm.h"
+
+// Per-handle state.  Device tables are built once by bsmm_create and then only read.
+struct bsmm_ctx {
+    int R = 0, S = 0, bs = 0, fa = 1;
+    int64_t nnz = 0;
+    int device = 0;
+    int sm_count = 0;
+    bsmm_kernel kernel = BSMM_KERNEL_AUTO;
+
+    uint8_t *d_layout = nullptr;   // R*S
+    int32_t *d_row_ptr = nullptr;  // R+1
+    int32_t *d_row_ent = nullptr;  // nnz: k of each block (row-major order)
+    int32_t *d_col_ptr = nullptr;  // S+1
+    int32_t *d_col_ent = nullptr;  // 2*nnz: (block id, c) per column, c increasing
+    int32_t *d_coord = nullptr;    // 2*nnz: (c, k) per block id
+    int32_t *d_bid = nullptr;      // R*S: block id or -1
+    int32_t *d_status = nullptr;   // sticky device error word
+
+    // Host mirrors of the tables (block_coord lookups, tensor-core schedules).
+    std::vector<int32_t> h_row_ptr, h_row_ent, h_col_ptr, h_col_ent, h_coord;
+
+    // Tensor-core schedules (built lazily by the tcgen05 path).
+    void *tc = nullptr;
+};
+
+extern std::atomic<int64_t> g_bsmm_launches;
+
+static inline int dtype_size(bsmm_dtype t) { return t == BSMM_F32 ? 4 : 2; }
+
+#define BSMM_CUDA_TRY(expr)                              \
+    do {                                                 \
+        cudaError_t e_ = (expr);                         \
+        if (e_ != cudaSuccess) return BSMM_ERR_CUDA;     \
+    } while (0)
+
+// Grouped-gradient pointer pack, passed by value to kernels.
+struct GroupPtrs {
+    const void *x[8];
+    const void *dy[8];
+    int G;
+};
+
+// LUT / init kernels (bsmm_lut.cu)
+bsmm_status lut_build(bsmm_ctx *h, const uint8_t *layout_host, cudaStream_t s);
+bsmm_status launch_identity_init(bsmm_ctx *h, void *w, bsmm_dtype t, cudaStream_t s);
+bsmm_status launch_zero(void *p, size_t bytes, cudaStream_t s);
+
+// IEEE SIMT kernels, any dtype (bsmm_simt.cu)
+bsmm_status simt_fprop(bsmm_ctx *h, const void *x, const void *w, void *y, int N, bsmm_dtype t,
+                       cudaStream_t s);
+bsmm_status simt_bprop(bsmm_ctx *h, const void *dy, const void *w, void *dx, int N, bsmm_dtype t,
+                       cudaStream_t s);
+bsmm_status simt_updat(bsmm_ctx *h, const GroupPtrs &g, void *dw, int N, bsmm_dtype t,
+                       bsmm_dtype dw_t, int accumulate, cudaStream_t s);
+
+// tcgen05 tensor-core kernels, 16-bit inputs (bsmm_tc.cu)
+bool tc_supported(bsmm_ctx *h, bsmm_dtype t);
+bsmm_status tc_fprop(bsmm_ctx *h, const void *x, const void *w, void *y, int N, bsmm_dtype t,
+                     cudaStream_t s);
+bsmm_status tc_bprop(bsmm_ctx *h, const void *dy, const void *w, void *dx, int N, bsmm_dtype t,
+                     cudaStream_t s);
+bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dtype t,
+                     int accumulate, cudaStream_t s);
+void tc_release(bsmm_ctx *h);

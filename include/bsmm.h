@@ -1,0 +1,162 @@
+/*
+ * bsmm.h -- C ABI of libbsmm, block-sparse matrix multiplication on GB300
+ * (sm_103a).
+ *
+ * The operation is OpenAI blocksparse's BlocksparseMatMul, as documented in the
+ * blocksparse README, section "API Documentation: blocksparse.matmul":
+ *
+ *   layout       R x S array of ones and zeros; R = C/bs input block rows (c),
+ *                S = K/bs output block columns (k).
+ *   block_size   bs in {32, 16, 8}.
+ *   feature_axis 1: activations are (N, C) / (N, K) row-major;
+ *                0: activations are (C, N) / (K, N) row-major.
+ *   w            (nnz, bs, bs): one dense block per nonzero layout entry ("w_shape").
+ *                Block ids follow the row-major scan of the layout (c outer, k
+ *                inner); block b at layout (c, k) holds W[c*bs+i][k*bs+j] at
+ *                w[b][i][j], W being the dense C x K block-sparse weight.
+ *   fprop        y  = x  . W                         ("__call__(I, W)")
+ *   bprop        dx = dy . W^T                       (gradient w.r.t. the input)
+ *   updat        dw[b] = x[:, c_b block]^T . dy[:, k_b block]  (gradient w.r.t. W,
+ *                float32 by default: "dw_dtype")
+ *   updat_grouped  dw = sum over G <= 8 timesteps of updat(x_t, dy_t)
+ *                ("group_param_grads(param_grad, group_size=8, cast32=True)")
+ *
+ * Conventions common to every call below:
+ *   - Pointers named x, w, y, dx, dy, dw, xs[i], dys[i] are DEVICE pointers on
+ *     the handle's device, owned by the caller, 16-byte aligned.  The library
+ *     never frees or keeps them after the call returns.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*, NULL = legacy default stream).  Inputs must stay valid until the
+ *     work completes.
+ *   - Host-side argument checks run first and return an error synchronously,
+ *     without enqueuing anything.  Errors detected on the device (a bounded
+ *     wait that gave up) are recorded in a sticky per-handle status word that
+ *     bsmm_sync_status() reads and clears.  No call traps the device.
+ *   - N (minibatch) may be 0 (no work).  With feature_axis = 0 the row pitch is
+ *     N elements, so N * sizeof(element) must be a multiple of 16 bytes.
+ *   - Outputs of empty block columns (fprop) or empty block rows (bprop) are
+ *     written as zeros.
+ *   - A handle may be used from several streams at once (its tables are read
+ *     only after creation), but not while bsmm_destroy runs.
+ */
+#ifndef BSMM_H
+#define BSMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct bsmm_ctx *bsmm_t;
+
+typedef enum {
+    BSMM_OK = 0,
+    BSMM_ERR_INVALID = 1,      /* bad argument (null pointer, bad shape, G out of range, ...) */
+    BSMM_ERR_UNSUPPORTED = 2,  /* valid but not implemented (block size, dtype combination) */
+    BSMM_ERR_ALIGN = 3,        /* pointer or row pitch not 16-byte aligned */
+    BSMM_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    BSMM_ERR_TIMEOUT = 5,      /* a device-side bounded wait gave up (sticky) */
+    BSMM_ERR_OOM = 6,          /* device allocation failed */
+    BSMM_ERR_BOUNDS = 7        /* a device-side index check failed (sticky) */
+} bsmm_status;
+
+typedef enum { BSMM_F32 = 0, BSMM_F16 = 1, BSMM_BF16 = 2 } bsmm_dtype;
+
+/* Kernel family used by the compute calls.  AUTO picks the tcgen05 tensor-core
+ * kernels for 16-bit inputs and the IEEE fp32 SIMT kernels for fp32. */
+typedef enum { BSMM_KERNEL_AUTO = 0, BSMM_KERNEL_SIMT = 1, BSMM_KERNEL_TC = 2 } bsmm_kernel;
+
+/*
+ * BlocksparseMatMul(layout, block_size, feature_axis)  [README: "class BlocksparseMatMul"]
+ * layout_host: HOST pointer to R*S bytes, row-major, nonzero = block present
+ * (copied; the caller keeps ownership).  Builds the per-output-column,
+ * per-input-row and block-coordinate tables on the device with kernels on
+ * `stream`, and waits for them.  On success *out owns device memory freed by
+ * bsmm_destroy.  Errors: INVALID (null, R or S < 1, feature_axis not 0/1),
+ * UNSUPPORTED (block_size not 8/16/32), OOM, CUDA.
+ */
+bsmm_status bsmm_create(bsmm_t *out, const uint8_t *layout_host, int R, int S,
+                        int block_size, int feature_axis, void *stream);
+
+/* Frees everything the handle owns.  Waits for the device first.  NULL is OK. */
+bsmm_status bsmm_destroy(bsmm_t h);
+
+/* w_shape [README: "self.w_shape"]: the weight is (nnz, bs, bs).  Also R, S, feature_axis. */
+bsmm_status bsmm_w_shape(bsmm_t h, int64_t *nnz, int *block_size);
+bsmm_status bsmm_layout_info(bsmm_t h, int *R, int *S, int *feature_axis);
+
+/* block_coord(block) [README]: layout coordinates (c, k) of block id `block`
+ * (host lookup).  INVALID if block is outside [0, nnz). */
+bsmm_status bsmm_block_coord(bsmm_t h, int64_t block, int *c, int *k);
+
+/*
+ * Copies the device lookup tables to HOST buffers (any may be NULL):
+ *   row_ptr[R+1], row_ent[nnz] = k of each block (row-major order, so the
+ *   block id of entry e of row c is e itself), col_ptr[S+1],
+ *   col_ent[2*nnz] = (block id, c) pairs per output column with c increasing,
+ *   coord[2*nnz] = (c, k) per block id.  Synchronous.
+ */
+bsmm_status bsmm_get_luts(bsmm_t h, int32_t *row_ptr, int32_t *row_ent, int32_t *col_ptr,
+                          int32_t *col_ent, int32_t *coord);
+
+/*
+ * identity_init(gpu=True) [README: "identity_init + layernorm is all you need",
+ * "with gpu=True the init is performed by kernel on the device"]:
+ * w[b] = I (bs x bs) when c_b == k_b, else 0.  w: (nnz, bs, bs) of type t.
+ */
+bsmm_status bsmm_identity_init(bsmm_t h, void *w, bsmm_dtype t, void *stream);
+
+/*
+ * fprop [README: "__call__(I, W)"]: y = x . W.
+ * x: (N, C) if feature_axis = 1 else (C, N); y: (N, K) or (K, N); w: (nnz, bs, bs).
+ * x, w, y share dtype t; accumulation is float32; y is rounded to nearest-even
+ * once.  fp32 uses IEEE FMA (no TF32).  y must not overlap x or w.
+ */
+bsmm_status bsmm_fprop(bsmm_t h, const void *x, const void *w, void *y, int N, bsmm_dtype t,
+                       void *stream);
+
+/*
+ * bprop (gradient of __call__ w.r.t. I): dx = dy . W^T.
+ * dy: (N, K) or (K, N); dx: (N, C) or (C, N).  Same dtype and rounding rules as fprop.
+ */
+bsmm_status bsmm_bprop(bsmm_t h, const void *dy, const void *w, void *dx, int N, bsmm_dtype t,
+                       void *stream);
+
+/*
+ * updat (gradient of __call__ w.r.t. W, "dw_dtype"):
+ * dw[b][i][j] (+)= sum_n x[n][c_b*bs+i] * dy[n][k_b*bs+j].
+ * x, dy of dtype t; dw of dtype dw_t (BSMM_F32, the README's default, or t).
+ * accumulate = 0: dw = result; 1: dw += result (float32 add, then one rounding
+ * to dw_t).  dw must not overlap x or dy.
+ */
+bsmm_status bsmm_updat(bsmm_t h, const void *x, const void *dy, void *dw, int N, bsmm_dtype t,
+                       bsmm_dtype dw_t, int accumulate, void *stream);
+
+/*
+ * Grouped updat [README: "group_param_grads(param_grad, group_size=8, cast32=True)"]:
+ * dw (+)= sum_{t<G} sum_n x_t[n][c_b*bs+i] * dy_t[n][k_b*bs+j], all in float32.
+ * xs, dys: HOST arrays of G DEVICE pointers (read during the call only), each
+ * of the activation shape with minibatch N.  G in [1, 8].  dw: float32.
+ */
+bsmm_status bsmm_updat_grouped(bsmm_t h, const void *const *xs, const void *const *dys, int G,
+                               int N, bsmm_dtype t, float *dw, int accumulate, void *stream);
+
+/* Kernel family for later calls on this handle (testing / comparison). */
+bsmm_status bsmm_set_kernel(bsmm_t h, bsmm_kernel which);
+
+/* Waits for `stream`, then returns and clears the handle's sticky device
+ * status (OK, TIMEOUT or BOUNDS), or CUDA if the stream reports an error. */
+bsmm_status bsmm_sync_status(bsmm_t h, void *stream);
+
+/* Static description of a status code. */
+const char *bsmm_status_string(bsmm_status s);
+
+/* Number of kernels this library has launched since load (all handles). */
+int64_t bsmm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSMM_H */

@@ -1,0 +1,67 @@
+"""The C-ABI library loads, exports every symbol include/bsmm.h declares, and
+rejects bad arguments on the host (no GPU needed: these checks run before any
+CUDA call)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from block_sparse_matrix_gb300 import bsmm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "bsmm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsmm_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("bsmm_create", "bsmm_destroy", "bsmm_fprop", "bsmm_bprop", "bsmm_updat",
+                     "bsmm_updat_grouped", "bsmm_identity_init", "bsmm_block_coord", "bsmm_w_shape",
+                     "bsmm_get_luts", "bsmm_sync_status", "bsmm_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(bsmm.LIB_PATH)
+    missing = [n for n in declared_symbols() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    for code in range(8):
+        assert bsmm.status_string(code)
+    assert "align" in bsmm.status_string(bsmm.ERR_ALIGN)
+
+
+def _create(layout, bs, fa, R=None, S=None):
+    L = bsmm.lib()
+    lay = np.ascontiguousarray(layout, dtype=np.uint8)
+    h = ctypes.c_void_p()
+    R = lay.shape[0] if R is None else R
+    S = lay.shape[1] if S is None else S
+    return L.bsmm_create(ctypes.byref(h), lay.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), R, S, bs, fa, None)
+
+
+def test_create_rejects_bad_arguments_on_host():
+    lay = np.ones((2, 2), np.uint8)
+    assert _create(lay, 12, 1) == bsmm.ERR_UNSUPPORTED        # block size not in {32,16,8}
+    assert _create(lay, 64, 1) == bsmm.ERR_UNSUPPORTED
+    assert _create(lay, 32, 2) == bsmm.ERR_INVALID            # feature_axis not 0/1
+    assert _create(lay, 32, 1, R=0) == bsmm.ERR_INVALID
+    assert _create(lay, 32, 1, S=-1) == bsmm.ERR_INVALID
+    L = bsmm.lib()
+    assert L.bsmm_create(None, None, 2, 2, 32, 1, None) == bsmm.ERR_INVALID
+
+
+def test_null_handle_rejected():
+    L = bsmm.lib()
+    assert L.bsmm_fprop(None, None, None, None, 4, 0, None) == bsmm.ERR_INVALID
+    assert L.bsmm_updat_grouped(None, None, None, 1, 4, 0, None, 0, None) == bsmm.ERR_INVALID
+    assert L.bsmm_destroy(None) == bsmm.OK
+    assert L.bsmm_set_kernel(None, 0) == bsmm.ERR_INVALID

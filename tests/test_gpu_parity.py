@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA library (through its C ABI) against the float64 oracle.
+
+Bit-exact for the lookup tables, block_coord, identity_init, the all-zero and
+identity cases and small-integer inputs; relative Frobenius error within the
+stated tolerance otherwise.  Every compute test runs both kernel families:
+"simt" (IEEE fp32 FFMA) and "auto" (tcgen05 tensor cores for 16-bit inputs).
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_matrix_gb300 import bsmm, workloads as wk
+from block_sparse_matrix_gb300.bsmm import BlocksparseMatMul
+from oracle import oracle as o
+
+from _util import TOL, TOL_DW, act_nf, cpu64, problem, rand_layout, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+# Tighter bound than TOL for one float32-accumulated dot product rounded once
+# to the output type (RMS relative rounding error of bf16 ~1e-3, fp16 ~1.5e-4).
+TIGHT = {"f32": 1e-5, "f16": 2e-3, "bf16": 8e-3}
+KERNELS = ["simt", "auto"]
+DT = wk.DTYPES
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def make(L, bs, fa, kernel="auto"):
+    m = BlocksparseMatMul(L, block_size=bs, feature_axis=fa)
+    m.set_kernel(kernel)
+    return m
+
+
+# ---- tables -----------------------------------------------------------------------
+
+@pytest.mark.parametrize("R,S,p,seed", [(8, 8, 0.5, 0), (5, 9, 0.3, 1), (33, 17, 0.7, 2), (1, 1, 1.0, 3),
+                                         (6, 6, 0.0, 4), (512, 512, 0.1, 5), (192, 192, 0.05, 6)])
+def test_luts_bit_exact(R, S, p, seed):
+    L = rand_layout(R, S, p, seed)
+    m = make(L, 16, 1)
+    got = m.get_luts()
+    ref = o.luts(L)
+    for g, r in zip(got, ref):
+        assert np.array_equal(g, r)
+    for b in np.random.default_rng(seed).integers(0, max(1, m.nnz), 20) if m.nnz else []:
+        assert m.block_coord(int(b)) == tuple(ref[4][b])
+    with pytest.raises(bsmm.BsmmError):
+        m.block_coord(m.nnz)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_identity_init_bit_exact(bs, dtype):
+    L = rand_layout(7, 7, 0.4, bs, diag=True)
+    L[3, 3] = 0
+    m = make(L, bs, 1)
+    w = m.identity_init(dtype=DT[dtype])
+    assert np.array_equal(cpu64(w), o.identity_init(L, bs))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("bs,fa,dtype", [(32, 1, "bf16"), (16, 0, "f16"), (8, 0, "bf16"), (32, 1, "f32"),
+                                         (8, 1, "f16"), (16, 1, "bf16"), (32, 0, "f16")])
+def test_identity_layer_is_exact(kernel, bs, fa, dtype):
+    """identity_init on a block-diagonal layout: y = x and dx = dy bit for bit."""
+    R, N = 6, 136
+    L = np.eye(R, dtype=np.uint8)
+    m = make(L, bs, fa, kernel)
+    w = m.identity_init(dtype=DT[dtype])
+    x = wk.normals(wk.act_shape(R * bs, N, fa), 5, 1.0, dtype).cuda()
+    assert torch.equal(m.fprop(x, w), x)
+    assert torch.equal(m.bprop(x, w), x)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("bs,fa,dtype", [(32, 1, "bf16"), (16, 0, "f16"), (8, 0, "bf16"), (8, 1, "f32")])
+def test_all_zero_layout(kernel, bs, fa, dtype):
+    L = np.zeros((4, 5), np.uint8)
+    m = make(L, bs, fa, kernel)
+    assert m.nnz == 0
+    N = 72
+    x = wk.normals(wk.act_shape(4 * bs, N, fa), 1, 1.0, dtype).cuda()
+    dy = wk.normals(wk.act_shape(5 * bs, N, fa), 2, 1.0, dtype).cuda()
+    w = torch.empty((0, bs, bs), dtype=DT[dtype], device="cuda")
+    y = torch.full(m.o_shape(N), float("nan"), dtype=DT[dtype], device="cuda")
+    dx = torch.full(m.i_shape(N), float("nan"), dtype=DT[dtype], device="cuda")
+    m.fprop(x, w, y)
+    m.bprop(dy, w, dx)
+    assert not torch.any(y != 0) and not torch.any(dx != 0)
+    m.updat(x, dy)
+    m.sync_status()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("fa", [0, 1])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_brute_force_2x2_integer_exact(kernel, bs, fa, dtype):
+    """All 16 patterns of a 2x2-block layout with entries in {-1,0,1}: every product
+    and partial sum is an integer below 2^8, exact in every dtype, so GPU == oracle."""
+    N = 144
+    for pattern in range(16):
+        L = np.array([(pattern >> q) & 1 for q in range(4)], np.uint8).reshape(2, 2)
+        m = make(L, bs, fa, kernel)
+        seed = 100 * pattern + bs + fa
+        x = wk.small_ints(wk.act_shape(2 * bs, N, fa), seed, dtype).cuda()
+        dy = wk.small_ints(wk.act_shape(2 * bs, N, fa), seed + 1, dtype).cuda()
+        w = wk.small_ints((m.nnz, bs, bs), seed + 2, dtype).cuda()
+        y = m.fprop(x, w)
+        dx = m.bprop(dy, w)
+        dw = m.updat(x, dy)
+        m.sync_status()
+        assert np.array_equal(cpu64(y), o.fprop(L, bs, x.cpu(), w.cpu(), fa)), pattern
+        assert np.array_equal(cpu64(dx), o.bprop(L, bs, dy.cpu(), w.cpu(), fa)), pattern
+        assert np.array_equal(cpu64(dw), o.updat(L, bs, x.cpu(), dy.cpu(), fa)), pattern
+
+
+# ---- seeded random problems spanning several tiles with a ragged tail ---------------
+
+@functools.lru_cache(maxsize=None)
+def small_case(bs, fa, dtype):
+    R = S = {32: 12, 16: 20, 8: 36}[bs]
+    N = 200                                   # 200 = 128 + 72: a full tile plus a ragged tail
+    L, x, w, dy = problem(R, S, bs, N, fa, dtype, p=0.4, seed=7 * bs + fa)
+    L[:, 1] = 0                               # an empty output block column
+    L[2, :] = 0                               # an empty input block row
+    nnz = int(L.sum())
+    w = w[:nnz] if w.shape[0] >= nnz else wk.normals((nnz, bs, bs), 9, 0.05, dtype)
+    w = wk.normals((nnz, bs, bs), 7 * bs + fa + 2, float(1 / np.sqrt(R * bs * 0.4)), dtype)
+    ref_y = o.fprop(L, bs, x, w, fa)
+    ref_dx = o.bprop(L, bs, dy, w, fa)
+    ref_dw = o.updat(L, bs, x, dy, fa)
+    return L, x, w, dy, ref_y, ref_dx, ref_dw
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("fa", [0, 1])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_parity_small(kernel, bs, fa, dtype):
+    L, x, w, dy, ref_y, ref_dx, ref_dw = small_case(bs, fa, dtype)
+    m = make(L, bs, fa, kernel)
+    xc, wc, dyc = x.cuda(), w.cuda(), dy.cuda()
+    y = torch.full(m.o_shape(200), float("nan"), dtype=DT[dtype], device="cuda")
+    dx = torch.full(m.i_shape(200), float("nan"), dtype=DT[dtype], device="cuda")
+    m.fprop(xc, wc, y)
+    m.bprop(dyc, wc, dx)
+    dw = m.updat(xc, dyc)
+    m.sync_status()
+    for got, ref in ((y, ref_y), (dx, ref_dx)):
+        e = rel_fro(cpu64(got), ref)
+        assert e <= TOL[dtype] and e <= TIGHT[dtype], e
+    e = rel_fro(cpu64(dw), ref_dw)
+    assert e <= TOL_DW[dtype], e
+    # accumulate: dw += updat
+    dw2 = dw.clone()
+    m.updat(xc, dyc, dw=dw2, accumulate=True)
+    m.sync_status()
+    assert rel_fro(cpu64(dw2), 2 * ref_dw) <= TOL_DW[dtype]
+    # 16-bit dW output when the dtype allows it (dw_dtype of the README)
+    if dtype != "f32" and kernel == "simt":
+        dwh = m.updat(xc, dyc, dw_dtype=DT[dtype])
+        assert rel_fro(cpu64(dwh), ref_dw) <= TIGHT[dtype]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("fa,bs,dtype", [(1, 32, "bf16"), (0, 16, "f16"), (0, 8, "bf16"), (1, 8, "f32")])
+@pytest.mark.parametrize("G", [1, 3, 8])
+def test_grouped_updat(kernel, fa, bs, dtype, G):
+    R, S, N = 10, 9, 96
+    L = rand_layout(R, S, 0.5, G + bs)
+    m = make(L, bs, fa, kernel)
+    xs = [wk.normals(wk.act_shape(R * bs, N, fa), 50 + t, 1.0, dtype) for t in range(G)]
+    dys = [wk.normals(wk.act_shape(S * bs, N, fa), 70 + t, 1.0, dtype) for t in range(G)]
+    ref = o.updat_grouped(L, bs, xs, dys, fa)
+    dw = m.updat_grouped([a.cuda() for a in xs], [a.cuda() for a in dys])
+    m.sync_status()
+    assert rel_fro(cpu64(dw), ref) <= TOL_DW[dtype]
+    m.updat_grouped([a.cuda() for a in xs], [a.cuda() for a in dys], dw=dw, accumulate=True)
+    m.sync_status()
+    assert rel_fro(cpu64(dw), 2 * ref) <= TOL_DW[dtype]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_deterministic(kernel):
+    L, x, w, dy, *_ = small_case(16, 0, "f16")
+    m = make(L, 16, 0, kernel)
+    xc, wc, dyc = x.cuda(), w.cuda(), dy.cuda()
+    a = (m.fprop(xc, wc), m.bprop(dyc, wc), m.updat(xc, dyc))
+    b = (m.fprop(xc, wc), m.bprop(dyc, wc), m.updat(xc, dyc))
+    for p, q in zip(a, b):
+        assert torch.equal(p, q)
+
+
+# ---- the five benchmark configurations, full size, sampled outputs -------------------
+
+def _sample_check(m, L, bs, fa, dtype, x, w, dy, y, dx, dw, rng, n_samples=384):
+    N = x.shape[0] if fa == 1 else x.shape[1]
+    C, K = L.shape[0] * bs, L.shape[1] * bs
+    n = rng.integers(0, N, n_samples)
+    fk = rng.integers(0, K, n_samples)
+    fc = rng.integers(0, C, n_samples)
+    y_nf, dx_nf = act_nf(y, fa), act_nf(dx, fa)
+    gy = y_nf[torch.from_numpy(n).cuda(), torch.from_numpy(fk).cuda()].double().cpu().numpy()
+    gdx = dx_nf[torch.from_numpy(n).cuda(), torch.from_numpy(fc).cuda()].double().cpu().numpy()
+    ry = o.fprop_at(L, bs, w, x, fa, n, fk)
+    rdx = o.bprop_at(L, bs, w, dy, fa, n, fc)
+    assert rel_fro(gy, ry) <= min(TOL[dtype], TIGHT[dtype] * 2)
+    assert rel_fro(gdx, rdx) <= min(TOL[dtype], TIGHT[dtype] * 2)
+    if dw is not None:
+        b = rng.integers(0, m.nnz, n_samples)
+        i = rng.integers(0, bs, n_samples)
+        j = rng.integers(0, bs, n_samples)
+        gdw = dw[torch.from_numpy(b).cuda(), torch.from_numpy(i).cuda(), torch.from_numpy(j).cuda()]
+        rdw = o.updat_at(L, bs, x, dy, fa, b, i, j)
+        assert rel_fro(gdw.double().cpu().numpy(), rdw) <= TOL_DW[dtype]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name", ["cfg1", "cfg2_n64", "cfg2_n1024", "cfg3", "cfg4"])
+def test_config_full_size(kernel, name):
+    wl = wk.CONFIGS[name]
+    inp = wk.make_inputs(wl)
+    L = inp.layout
+    m = make(L, wl.bs, wl.feature_axis, kernel)
+    x, w, dy = inp.x.cuda(), inp.w.cuda(), inp.dy.cuda()
+    y, dx, dw = m.fprop(x, w), m.bprop(dy, w), m.updat(x, dy)
+    m.sync_status()
+    _sample_check(m, L, wl.bs, wl.feature_axis, wl.dtype, inp.x, inp.w, inp.dy, y, dx, dw,
+                  np.random.default_rng(wl.cfg))
+    if name == "cfg1":   # small enough for the full oracle
+        assert rel_fro(cpu64(y), o.fprop(L, wl.bs, inp.x, inp.w, 1)) <= TOL["f32"]
+        assert rel_fro(cpu64(dx), o.bprop(L, wl.bs, inp.dy, inp.w, 1)) <= TOL["f32"]
+        assert rel_fro(cpu64(dw), o.updat(L, wl.bs, inp.x, inp.dy, 1)) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_config5_recurrent_grouped(kernel):
+    """16 timesteps share W: per-step fprop/bprop, weight gradient grouped 8 steps per
+    call and summed into one float32 dW (group_param_grads)."""
+    wl = wk.CONFIGS["cfg5"]
+    inp = wk.make_inputs(wl)
+    L, bs = inp.layout, wl.bs
+    m = make(L, bs, 1, kernel)
+    w = inp.w.cuda()
+    xs = [a.cuda() for a in inp.xs]
+    dys = [a.cuda() for a in inp.dys]
+    rng = np.random.default_rng(55)
+    for t in (0, 15):
+        y, dx = m.fprop(xs[t], w), m.bprop(dys[t], w)
+        _sample_check(m, L, bs, 1, wl.dtype, inp.xs[t], inp.w, inp.dys[t], y, dx, None, rng)
+    dw = bsmm.group_param_grads(m, xs, dys, group_size=8)
+    m.sync_status()
+    b = rng.integers(0, m.nnz, 256)
+    i = rng.integers(0, bs, 256)
+    j = rng.integers(0, bs, 256)
+    ref = sum(o.updat_at(L, bs, inp.xs[t], inp.dys[t], 1, b, i, j) for t in range(16))
+    got = dw[torch.from_numpy(b).cuda(), torch.from_numpy(i).cuda(), torch.from_numpy(j).cuda()]
+    assert rel_fro(got.double().cpu().numpy(), ref) <= TOL_DW[wl.dtype]
+
+
+# ---- host-side argument errors with a live handle --------------------------------------
+
+def test_errors_reported():
+    L = rand_layout(4, 4, 0.6, 1, diag=True)
+    m = make(L, 16, 0)
+    x = torch.zeros((64, 72), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(m.w_shape, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((64, 72), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(bsmm.BsmmError) as e:           # fa=0 row pitch 70*2 bytes: not 16B aligned
+        bsmm.bsmm_fprop(m.handle, x, w, y, 70)
+    assert e.value.code == bsmm.ERR_ALIGN
+    flat = torch.zeros(64 * 72 + 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(bsmm.BsmmError) as e:           # base pointer off by 2 bytes
+        bsmm.bsmm_fprop(m.handle, flat[1:], w, y, 72)
+    assert e.value.code == bsmm.ERR_ALIGN
+    with pytest.raises(bsmm.BsmmError) as e:
+        bsmm.bsmm_updat_grouped(m.handle, [x] * 9, [x] * 9, torch.zeros(m.w_shape, device="cuda"), 72)
+    assert e.value.code == bsmm.ERR_INVALID
+    with pytest.raises(bsmm.BsmmError) as e:           # dW as fp16 for bf16 inputs
+        bsmm.bsmm_updat(m.handle, x, x, torch.zeros(m.w_shape, dtype=torch.float16, device="cuda"), 72)
+    assert e.value.code == bsmm.ERR_UNSUPPORTED
+    m.sync_status()
