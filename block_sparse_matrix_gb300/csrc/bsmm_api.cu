@@ -4,6 +4,7 @@
 // call's contract.
 #include "bsmm_internal.cuh"
 
+#include <cstdlib>
 #include <new>
 
 std::atomic<int64_t> g_bsmm_launches{0};
@@ -68,6 +69,7 @@ bsmm_status bsmm_create(bsmm_t *out, const uint8_t *layout_host, int R, int S, i
     h->S = S;
     h->bs = block_size;
     h->fa = feature_axis;
+    if (const char *e = getenv("BSMM_TC_WLOG")) h->tc_wlog = atoi(e);
     if (cudaGetDevice(&h->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
         delete h;
@@ -164,7 +166,10 @@ bsmm_status bsmm_fprop(bsmm_t h, const void *x, const void *w, void *y, int N, b
     if (!x || !y || (h->nnz > 0 && !w)) return BSMM_ERR_INVALID;
     if (!aligned16(x) || !aligned16(y) || (h->nnz > 0 && !aligned16(w))) return BSMM_ERR_ALIGN;
     cudaStream_t s = (cudaStream_t)stream;
-    if (use_tc(h, t)) return tc_fprop(h, x, w, y, N, t, s);
+    if (use_tc(h, t)) {
+        st = tc_fprop(h, x, w, y, N, t, s);
+        if (st != BSMM_ERR_UNSUPPORTED) return st;
+    }
     return simt_fprop(h, x, w, y, N, t, s);
 }
 
@@ -176,7 +181,10 @@ bsmm_status bsmm_bprop(bsmm_t h, const void *dy, const void *w, void *dx, int N,
     if (!dy || !dx || (h->nnz > 0 && !w)) return BSMM_ERR_INVALID;
     if (!aligned16(dy) || !aligned16(dx) || (h->nnz > 0 && !aligned16(w))) return BSMM_ERR_ALIGN;
     cudaStream_t s = (cudaStream_t)stream;
-    if (use_tc(h, t)) return tc_bprop(h, dy, w, dx, N, t, s);
+    if (use_tc(h, t)) {
+        st = tc_bprop(h, dy, w, dx, N, t, s);
+        if (st != BSMM_ERR_UNSUPPORTED) return st;
+    }
     return simt_bprop(h, dy, w, dx, N, t, s);
 }
 

@@ -33,6 +33,7 @@ struct bsmm_ctx {
 
     // Tensor-core schedules (built lazily by the tcgen05 path).
     void *tc = nullptr;
+    int tc_wlog = -1;   // fprop/bprop window size override (log2), from BSMM_TC_WLOG; -1 = automatic
 };
 
 extern std::atomic<int64_t> g_bsmm_launches;

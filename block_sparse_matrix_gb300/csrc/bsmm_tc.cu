@@ -30,6 +30,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 using namespace tc;
@@ -40,32 +41,52 @@ namespace {
 // Host-side schedules
 // ---------------------------------------------------------------------------------------
 
-// One entry of a fprop/bprop window: the source block index (coarse c for fprop,
-// coarse k for bprop) and the range of its (slot, ids) records.
+// Schedule of fprop/bprop: one packed word stream per window of W output blocks, cut
+// into chunks; a chunk is what one pipeline stage holds.
+//   chunk header: (ne << 8) | nr     -- ne entries then nr records follow; 0 ends the stream
+//   entry word:   (src << 8) | nrec  -- src = source block (coarse c for fprop, coarse k for
+//                 bprop) whose activation panel is loaded into the stage; its nrec records are
+//                 the next nrec records of the chunk
+//   record (bs 32/16): ((block id + 1) << 5) | slot
+//   record (bs 8, coarse 16x16 block): 4 words, ((id00 + 1) << 5) | slot, id01 + 1,
+//                 id10 + 1, id11 + 1, where idXY is the 8x8 block (2c'+X, 2k'+Y), 0 = absent
+// Streams start on 16-byte boundaries and are padded to a multiple of 4 words so a CTA
+// can bulk-copy its window into shared memory.
 struct FbSched {
-    int W = 0;                 // output slots per window
-    int nwin = 0;              // windows
-    int Fslots = 0;            // output blocks (coarse) of the pass
-    int32_t *d_win_ptr = nullptr;   // nwin+1, into ents
-    int32_t *d_ents = nullptr;      // 3 per entry: src, rec_off, nrec
-    int32_t *d_recs = nullptr;      // 5 per record: slot, id(0,0), id(0,1), id(1,0), id(1,1)
-    int32_t *d_win_order = nullptr; // nwin, windows by decreasing work
-    uint32_t *d_win_mask = nullptr; // nwin, slots that receive at least one block
-    size_t bytes = 0;
+    int W = 0;                      // output slots per window
+    int nwin = 0;                   // windows
+    int Fslots = 0;                 // output blocks (coarse) of the pass
+    int max_words = 0;              // longest window stream
+    uint32_t *d_stream = nullptr;
+    int32_t *d_win_off = nullptr;   // nwin: word offset of each window stream
+    int32_t *d_win_len = nullptr;   // nwin: padded length in words
+    int32_t *d_win_order = nullptr; // nwin: windows by decreasing work
+    uint32_t *d_win_mask = nullptr; // nwin: slots that receive at least one block
     bool built = false;
+    bool too_big = false;           // a window stream exceeds the shared-memory budget
 };
 
+// Schedule of updat: units of up to 128/bs (coarse) blocks of one block column, dealt
+// round-robin to persistent CTAs.  Each CTA's units sit in one fixed-size table that the
+// CTA bulk-copies into shared memory:
+//   table word 0: number of units; unit u at word 4 + u * kUnitWords:
+//     k' (coarse block column), nrec, then nrec records of 5 words:
+//     c' (coarse block row), id00, id01, id10, id11 (block ids of the 8x8 sub-blocks for
+//     bs 8, id00 = the block for bs 32/16, -1 = absent)
+constexpr int kUnitWords = 44;
+constexpr int kUnitsPerCta = 64;
+constexpr int kTableWords = 4 + kUnitsPerCta * kUnitWords;
+
 struct UpSched {
-    int nunits = 0;
-    int32_t *d_units = nullptr;     // 3 per unit: coarse column k', rec_off, nrec
-    int32_t *d_recs = nullptr;      // 5 per record: coarse c', id(0,0), id(0,1), id(1,0), id(1,1)
+    int ctas = 0;
+    int32_t *d_table = nullptr;     // ctas * kTableWords
     bool built = false;
 };
 
 struct TcState {
-    FbSched fb[2][6]; // [pass: 0 fprop, 1 bprop][log2 of the window size]
+    std::map<uint64_t, FbSched> fb;   // key: pass, window log2, chunk entries, chunk records
     UpSched up;
-    void *d_zero = nullptr;   // 16x16 bf16 zeros for absent 8x8 sub-blocks
+    void *d_zero = nullptr;   // zero buffer: 8x8 zero tiles for absent sub-blocks of 16x16 coarse blocks
     std::mutex mu;
 };
 
@@ -109,13 +130,6 @@ CUtensorMapSwizzle swz_for_row_bytes(int bytes)
                                                                  : CU_TENSOR_MAP_SWIZZLE_NONE;
 }
 
-int pow2_at_least(int v)
-{
-    int p = 32;
-    while (p < v) p <<= 1;
-    return p;
-}
-
 template <typename T> bool upload(T **d, const std::vector<T> &h)
 {
     size_t n = std::max<size_t>(h.size(), 1);
@@ -150,72 +164,104 @@ void fb_shape(const bsmm_ctx *h, bool bwd, int &Fslots, int &Fsrc, int &bse)
 }
 
 // Window size (log2): at most 256 TMEM columns, shrunk until windows x minibatch tiles
-// give about two CTAs per SM.
+// give at least one CTA per SM.  Larger windows load each activation panel for more
+// output blocks, smaller ones spread the work over more SMs.
 int choose_wlog(const bsmm_ctx *h, bool bwd, int n_tiles)
 {
     int Fslots, Fsrc, bse;
     fb_shape(h, bwd, Fslots, Fsrc, bse);
     int wl = 0;
     while ((2 << wl) * bse <= 256 && (1 << wl) < Fslots) ++wl;
-    const int64_t target = 2 * (int64_t)std::max(1, h->sm_count);
+    const int64_t target = (int64_t)std::max(1, h->sm_count);
     while (wl > 0 && (int64_t)((Fslots + (1 << wl) - 1) >> wl) * n_tiles < target) --wl;
     return wl;
 }
 
-// Builds the window schedule of fprop (bwd=false) or bprop (bwd=true) for windows of W slots.
-bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W)
+// Builds the window schedule of fprop (bwd=false) or bprop (bwd=true) for windows of W
+// slots.  A chunk holds at most e_max entries and r_max records and issues at most 32 TMA
+// loads (a_ops per entry, b_ops per record), one per lane of the producer warp.  Sets
+// too_big when a window's stream would exceed max_words.
+bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W, int e_max, int r_max, int a_ops, int b_ops,
+              int max_words)
 {
+    if (e_max < 1 || r_max < 1 || a_ops + r_max * b_ops > 32) return false;
     const bool coarse = h->bs == 8;
     const int f = coarse ? 2 : 1;                       // fine blocks per coarse block edge
+    const int rw = coarse ? 4 : 1;                      // words per record
     int Fslots, Fsrc, bse;
     fb_shape(h, bwd, Fslots, Fsrc, bse);
     W = std::min(W, Fslots);
     const int nwin = (Fslots + W - 1) / W;
     BidLookup bid{h};
 
-    std::vector<int32_t> win_ptr(nwin + 1, 0), ents, recs, order(nwin);
-    std::vector<uint32_t> mask(nwin, 0);
+    std::vector<uint32_t> stream, mask(nwin, 0);
+    std::vector<int32_t> off(nwin), len(nwin), order(nwin);
     std::vector<int64_t> work(nwin, 0);
-    std::vector<int32_t> ids(4);
+    int32_t ids[4];
+    int longest = 0;
+    struct Ent { int src; std::vector<uint32_t> recs; };
     for (int w = 0; w < nwin; ++w) {
-        win_ptr[w] = (int32_t)(ents.size() / 3);
+        off[w] = (int32_t)stream.size();
+        // entries of this window, each split so that no entry has more than r_max records
+        std::vector<Ent> ents;
         for (int src = 0; src < Fsrc; ++src) {
-            int nrec = 0;
-            int rec_off = (int)(recs.size() / 5);
-            for (int s = 0; s < W; ++s) {
-                int o = w * W + s;
+            Ent e{src, {}};
+            for (int sl = 0; sl < W; ++sl) {
+                const int o = w * W + sl;
                 if (o >= Fslots) break;
-                // coarse (c', k') of this (src, out) pair
-                int cc = bwd ? o : src, kc = bwd ? src : o;
+                const int cc = bwd ? o : src, kc = bwd ? src : o;   // coarse (c', k')
                 bool any = false;
                 for (int cs = 0; cs < f; ++cs)
                     for (int ks = 0; ks < f; ++ks) {
-                        int b = bid(cc * f + cs, kc * f + ks);
-                        ids[cs * 2 + ks] = b;
-                        any |= b >= 0;
+                        ids[cs * 2 + ks] = bid(cc * f + cs, kc * f + ks);
+                        any |= ids[cs * 2 + ks] >= 0;
                     }
-                if (!coarse) ids[1] = ids[2] = ids[3] = -1;
                 if (!any) continue;
-                recs.push_back(s);
-                for (int q = 0; q < 4; ++q) recs.push_back(ids[q]);
-                ++nrec;
-                mask[w] |= 1u << s;
+                e.recs.push_back(((uint32_t)(ids[0] + 1) << 5) | (uint32_t)sl);
+                if (coarse)
+                    for (int q = 1; q < 4; ++q) e.recs.push_back((uint32_t)(ids[q] + 1));
+                mask[w] |= 1u << sl;
             }
-            if (nrec) {
-                ents.push_back(src);
-                ents.push_back(rec_off);
-                ents.push_back(nrec);
-                work[w] += nrec + 2;
+            const int n = (int)e.recs.size() / rw;
+            for (int r0 = 0; r0 < n; r0 += r_max) {
+                const int r1 = std::min(n, r0 + r_max);
+                ents.push_back(Ent{src, std::vector<uint32_t>(e.recs.begin() + r0 * rw, e.recs.begin() + r1 * rw)});
             }
+            work[w] += n ? n + 2 : 0;
         }
+        // greedy packing into chunks
+        size_t i = 0;
+        while (i < ents.size()) {
+            int ne = 0, nr = 0;
+            size_t j = i;
+            while (j < ents.size()) {
+                const int er = (int)ents[j].recs.size() / rw;
+                if (ne + 1 > e_max || nr + er > r_max || (ne + 1) * a_ops + (nr + er) * b_ops > 32) break;
+                ++ne;
+                nr += er;
+                ++j;
+            }
+            if (ne == 0) return false;                           // limits admit no entry
+            stream.push_back(((uint32_t)ne << 8) | (uint32_t)nr);
+            for (size_t q = i; q < j; ++q)
+                stream.push_back(((uint32_t)ents[q].src << 8) | (uint32_t)(ents[q].recs.size() / rw));
+            for (size_t q = i; q < j; ++q) stream.insert(stream.end(), ents[q].recs.begin(), ents[q].recs.end());
+            i = j;
+        }
+        stream.push_back(0);                                     // end marker
+        while (stream.size() % 4) stream.push_back(0);
+        len[w] = (int32_t)(stream.size() - off[w]);
+        longest = std::max(longest, len[w]);
     }
-    win_ptr[nwin] = (int32_t)(ents.size() / 3);
+    fs.too_big = longest > max_words;
+    if (fs.too_big) return true;
     for (int w = 0; w < nwin; ++w) order[w] = w;
     std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return work[a] > work[b]; });
     fs.W = W;
     fs.nwin = nwin;
     fs.Fslots = Fslots;
-    if (!upload(&fs.d_win_ptr, win_ptr) || !upload(&fs.d_ents, ents) || !upload(&fs.d_recs, recs) ||
+    fs.max_words = longest;
+    if (!upload(&fs.d_stream, stream) || !upload(&fs.d_win_off, off) || !upload(&fs.d_win_len, len) ||
         !upload(&fs.d_win_order, order) || !upload(&fs.d_win_mask, mask))
         return false;
     fs.built = true;
@@ -229,33 +275,43 @@ bool build_up(bsmm_ctx *h, UpSched &us)
     const int Rc = (h->R + f - 1) / f, Sc = (h->S + f - 1) / f;
     const int MS = coarse ? 8 : 128 / h->bs;           // blocks stacked along M
     BidLookup bid{h};
-    std::vector<int32_t> units, recs;
-    std::vector<int32_t> ids(4);
+    std::vector<std::vector<int32_t>> units;           // kUnitWords each
+    int32_t ids[4];
     for (int kc = 0; kc < Sc; ++kc) {
-        std::vector<int32_t> col;   // records of this coarse column
+        std::vector<int32_t> col;                      // 5 words per record of this coarse column
         for (int cc = 0; cc < Rc; ++cc) {
             bool any = false;
             for (int cs = 0; cs < f; ++cs)
                 for (int ks = 0; ks < f; ++ks) {
-                    int b = bid(cc * f + cs, kc * f + ks);
-                    ids[cs * 2 + ks] = b;
-                    any |= b >= 0;
+                    ids[cs * 2 + ks] = bid(cc * f + cs, kc * f + ks);
+                    any |= ids[cs * 2 + ks] >= 0;
                 }
-            if (!coarse) ids[1] = ids[2] = ids[3] = -1;
             if (!any) continue;
             col.push_back(cc);
             for (int q = 0; q < 4; ++q) col.push_back(ids[q]);
         }
-        int n = (int)col.size() / 5;
+        const int n = (int)col.size() / 5;
         for (int s0 = 0; s0 < n; s0 += MS) {
-            units.push_back(kc);
-            units.push_back((int)(recs.size() / 5) + s0);
-            units.push_back(std::min(MS, n - s0));
+            std::vector<int32_t> u(kUnitWords, 0);
+            const int m = std::min(MS, n - s0);
+            u[0] = kc;
+            u[1] = m;
+            for (int q = 0; q < 5 * m; ++q) u[2 + q] = col[5 * s0 + q];
+            units.push_back(u);
         }
-        recs.insert(recs.end(), col.begin(), col.end());
     }
-    us.nunits = (int)units.size() / 3;
-    if (!upload(&us.d_units, units) || !upload(&us.d_recs, recs)) return false;
+    const int nunits = (int)units.size();
+    int ctas = std::max(1, std::min(nunits, 2 * std::max(1, h->sm_count)));
+    ctas = std::max(ctas, (nunits + kUnitsPerCta - 1) / kUnitsPerCta);
+    std::vector<int32_t> table((size_t)ctas * kTableWords, 0);
+    for (int u = 0; u < nunits; ++u) {
+        const int b = u % ctas, i = u / ctas;
+        int32_t *t = table.data() + (size_t)b * kTableWords;
+        t[0] = i + 1;
+        std::copy(units[u].begin(), units[u].end(), t + 4 + i * kUnitWords);
+    }
+    us.ctas = nunits ? ctas : 0;
+    if (!upload(&us.d_table, table)) return false;
     us.built = true;
     return true;
 }
@@ -274,6 +330,8 @@ TcState *state(bsmm_ctx *h)
 // ---------------------------------------------------------------------------------------
 
 constexpr int kThreads = 192;
+constexpr int kZeroTiles = 2048;                 // 8x8 zero tiles in the zero buffer (256 KB)
+constexpr int kZeroBytes = kZeroTiles * 128;
 
 __device__ __forceinline__ bool elect_one()
 {
@@ -307,13 +365,9 @@ template <> __device__ __forceinline__ uint16_t cvt1<false>(float a)
     return *reinterpret_cast<uint16_t *>(&v);
 }
 
-// Compile-time geometry of the fprop/bprop kernel for a (coarse) block edge BSE.
+// Compile-time descriptor geometry of the fprop/bprop kernel for a (coarse) block edge BSE.
 template <int BSE, int FA> struct FbGeo {
-    static constexpr int A_BYTES = 128 * BSE * 2;                    // activation panel (128 rows x BSE)
-    static constexpr int B_BYTES = BSE * BSE * 2;                    // one (coarse) weight block
-    static constexpr int SA = BSE == 32 ? 6 : 8;                     // activation stages
-    static constexpr int SB = BSE == 32 ? 24 : 32;                   // weight stages
-    static constexpr int SMEM = SA * A_BYTES + SB * B_BYTES;
+    static constexpr int B_SLOT = BSE * BSE * 2;                     // one (coarse) weight block
     static constexpr int KSTEPS = BSE / 16;
     // A operand descriptor parameters
     static constexpr uint32_t A_SWZ = FA ? (BSE == 32 ? SW_64 : SW_32) : SW_128;
@@ -322,9 +376,23 @@ template <int BSE, int FA> struct FbGeo {
     static constexpr uint32_t A_KSTEP = FA ? 32 : (16 * 128);
 };
 
+constexpr int kMaxStages = 16;
+constexpr int kMaxSmem = 216 * 1024;         // largest dynamic request (static shared memory counts against 227 KB)
+constexpr int kSchedWords = 3072;                                    // window stream budget (12 KB)
+
+// Runtime stage geometry: a stage holds one chunk of up to e_slots activation panels
+// (a_slot bytes each) and r_slots weight blocks.  With half = 1 (minibatch <= 64) a panel
+// is 64 rows: the MMA still reads 128 rows, the upper 64 come from the next slot (or the
+// padding after the last stage) and only feed accumulator rows that are never stored.
+struct FbStages {
+    int e_slots, r_slots, stages, half;
+    int a_slot, stage_bytes, b_off;
+};
+
 struct FbParams {
     void *out;
-    const int32_t *win_ptr, *ents, *recs, *win_order;
+    const uint32_t *stream;
+    const int32_t *win_off, *win_len, *win_order;
     const uint32_t *win_mask;
     int32_t *status;
     int N;          // minibatch
@@ -332,6 +400,7 @@ struct FbParams {
     int W;          // slots per window
     int Fslots;     // output (coarse) blocks
     int n_tiles;
+    FbStages g;
 };
 
 // fprop (BWD=false) / bprop (BWD=true).  BS = fine block size, BSE = 16 when BS = 8.
@@ -343,6 +412,8 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
     constexpr int BSE = BS == 8 ? 16 : BS;
     using G = FbGeo<BSE, FA>;
     constexpr bool COARSE = BS == 8;
+    constexpr int RW = COARSE ? 4 : 1;                                // words per record
+    constexpr int B_OPS = COARSE ? 4 : 1;                             // TMA boxes per record
     // B operand: fprop reads w[b] as B[K=i][N=j] (MN-major), bprop as B[K=j][N=i] (K-major).
     constexpr uint32_t B_SWZ = COARSE ? SW_NONE : (BS == 32 ? SW_64 : SW_32);
     constexpr uint32_t B_LBO = COARSE ? 128 : 16;
@@ -352,31 +423,29 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + G::SA * G::A_BYTES;
-    __shared__ __align__(8) uint64_t fullA[G::SA], emptyA[G::SA], fullB[G::SB], emptyB[G::SB], acc_full;
+    const FbStages g = p.g;
+    const int a_ops = (FA || g.half) ? 1 : 2;                         // TMA boxes per activation panel
+    const uint32_t *sched = reinterpret_cast<const uint32_t *>(smem + g.stages * g.stage_bytes + g.a_slot);
+    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], acc_full, sched_full;
     __shared__ uint32_t tmem_base;
     __shared__ volatile int aborted;
 
     const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
     const int unit = blockIdx.x;
     const int win = p.win_order[unit / p.n_tiles];
     const int n0 = (unit % p.n_tiles) * 128;
-    const int e_begin = p.win_ptr[win], e_end = p.win_ptr[win + 1];
     const int ncols = p.W * BSE;
     const uint32_t alloc_cols = ncols <= 32 ? 32 : ncols <= 64 ? 64 : ncols <= 128 ? 128 : 256;
 
     if (threadIdx.x == 0) {
         aborted = 0;
-        for (int i = 0; i < G::SA; ++i) {
-            mbar_init(&fullA[i], 1);
-            mbar_init(&emptyA[i], 1);
-        }
-        for (int i = 0; i < G::SB; ++i) {
-            mbar_init(&fullB[i], 1);
-            mbar_init(&emptyB[i], 1);
+        for (int i = 0; i < g.stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
         }
         mbar_init(&acc_full, 1);
+        mbar_init(&sched_full, 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base, alloc_cols);
@@ -386,97 +455,104 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
     const uint32_t tmem = tmem_base;
 
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (elect_one()) {
+        // ---------------- TMA producer: one load per lane per chunk ----------------
+        const uint64_t pol_act = policy_evict_last();
+        const uint64_t pol_w = policy_evict_first();
+        if (lane == 0) {
+            const int len = p.win_len[win];
+            mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
+            if (len > 0) bulk_load((void *)sched, p.stream + p.win_off[win], (uint32_t)len * 4u, &sched_full, pol_act);
             prefetch_tmap(&tm_act);
             prefetch_tmap(&tm_w);
-            const uint64_t pol_act = policy_evict_last();
-            const uint64_t pol_w = policy_evict_first();
-            int ia = 0, ib = 0;
-            for (int e = e_begin; e < e_end && !aborted; ++e) {
-                const int src = p.ents[3 * e], roff = p.ents[3 * e + 1], nrec = p.ents[3 * e + 2];
-                const int sa = ia % G::SA;
-                if (ia >= G::SA && !mbar_wait(&emptyA[sa], ((ia / G::SA) - 1) & 1, p.status)) {
+        }
+        if (!mbar_wait(&sched_full, 0, p.status)) aborted = 1;
+        __syncwarp();
+        int chunk = 0;
+        for (int pos = 0; !aborted; ++chunk) {
+            const uint32_t hdr = sched[pos];
+            const int ne = (int)(hdr >> 8), nr = (int)(hdr & 0xFFu);
+            if (ne == 0) break;
+            const int st = chunk % g.stages;
+            if (lane == 0) {
+                if (chunk >= g.stages && !mbar_wait(&empty[st], ((chunk / g.stages) - 1) & 1, p.status))
                     aborted = 1;
-                    break;
-                }
-                mbar_arrive_expect_tx(&fullA[sa], G::A_BYTES);
-                uint8_t *dstA = sA + sa * G::A_BYTES;
-                if (FA) {
-                    tma_load_2d(dstA, &tm_act, &fullA[sa], src * BSE, n0, pol_act);
+                else
+                    mbar_arrive_expect_tx(&full[st], (uint32_t)(ne * g.a_slot + nr * G::B_SLOT));
+            }
+            __syncwarp();
+            if (aborted) break;
+            uint8_t *stage = smem + st * g.stage_bytes;
+            const int na = ne * a_ops;
+            if (lane < na) {
+                const int e = lane / a_ops, hf = lane % a_ops;
+                const int src = (int)(sched[pos + 1 + e] >> 8);
+                uint8_t *dst = stage + e * g.a_slot;
+                if (FA) tma_load_2d(dst, &tm_act, &full[st], src * BSE, n0, pol_act);
+                else tma_load_2d(dst + hf * BSE * 128, &tm_act, &full[st], n0 + 64 * hf, src * BSE, pol_act);
+            } else if (lane < na + nr * B_OPS) {
+                const int q = lane - na, r = q / B_OPS, sub = q % B_OPS;
+                const uint32_t *rec = sched + pos + 1 + ne + r * RW;
+                uint8_t *dst = stage + g.b_off + r * G::B_SLOT;
+                if (!COARSE) {
+                    tma_load_2d(dst, &tm_w, &full[st], 0, ((int)(rec[0] >> 5) - 1) * BS, pol_w);
                 } else {
-                    tma_load_2d(dstA, &tm_act, &fullA[sa], n0, src * BSE, pol_act);
-                    tma_load_2d(dstA + BSE * 128, &tm_act, &fullA[sa], n0 + 64, src * BSE, pol_act);
-                }
-                ++ia;
-                for (int r = 0; r < nrec; ++r) {
-                    const int32_t *rec = p.recs + 5 * (roff + r);
-                    const int sb = ib % G::SB;
-                    if (ib >= G::SB && !mbar_wait(&emptyB[sb], ((ib / G::SB) - 1) & 1, p.status)) {
-                        aborted = 1;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&fullB[sb], G::B_BYTES);
-                    uint8_t *dstB = sB + sb * G::B_BYTES;
-                    if (!COARSE) {
-                        tma_load_2d(dstB, &tm_w, &fullB[sb], 0, rec[1] * BS, pol_w);
+                    // sub-block (cs, ks) -> core matrix at (N-group)*256 + (K-group)*128
+                    const int cs = sub >> 1, ks = sub & 1;
+                    const int ng = BWD ? cs : ks, kg = BWD ? ks : cs;
+                    const int id = (int)(sub == 0 ? (rec[0] >> 5) : rec[sub]) - 1;
+                    if (id >= 0) {
+                        tma_load_2d(dst + ng * 256 + kg * 128, &tm_w, &full[st], 0, id * 8, pol_w);
                     } else {
-                        // sub-block (cs, ks) -> core matrix at (N-group)*256 + (K-group)*128
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int cs = q >> 1, ks = q & 1;
-                            const int ng = BWD ? cs : ks, kg = BWD ? ks : cs;
-                            uint8_t *d = dstB + ng * 256 + kg * 128;
-                            const int32_t id = rec[1 + q];
-                            if (id >= 0) tma_load_2d(d, &tm_w, &fullB[sb], 0, id * 8, pol_w);
-                            else tma_load_2d(d, &tm_zero, &fullB[sb], 0, 0, pol_w);
-                        }
+                        // zero tiles are spread over the zero buffer so they hit many L2 lines
+                        const int zr = (int)((blockIdx.x * 61u + (unsigned)chunk * 32u + (unsigned)lane) % kZeroTiles) * 8;
+                        tma_load_2d(dst + ng * 256 + kg * 128, &tm_zero, &full[st], 0, zr, pol_w);
                     }
-                    ++ib;
                 }
             }
-            // Drain: wait until every issued load has landed before the CTA may exit.
-            for (int i = std::max(0, ia - G::SA); i < ia; ++i) mbar_wait(&fullA[i % G::SA], (i / G::SA) & 1, p.status);
-            for (int i = std::max(0, ib - G::SB); i < ib; ++i) mbar_wait(&fullB[i % G::SB], (i / G::SB) & 1, p.status);
+            pos += 1 + ne + nr * RW;
         }
+        // Drain: wait until every issued load has landed before the CTA may exit.
+        if (lane == 0)
+            for (int i = chunk > g.stages ? chunk - g.stages : 0; i < chunk; ++i)
+                mbar_wait(&full[i % g.stages], (i / g.stages) & 1, p.status);
         __syncwarp();
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (elect_one()) {
             uint32_t inited = 0;
-            int ia = 0, ib = 0;
-            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-            for (int e = e_begin; e < e_end && !aborted; ++e) {
-                const int roff = p.ents[3 * e + 1], nrec = p.ents[3 * e + 2];
-                const int sa = ia % G::SA;
-                if (!mbar_wait(&fullA[sa], (ia / G::SA) & 1, p.status)) {
+            const uint32_t s_base = smem_u32(smem);
+            if (!mbar_wait(&sched_full, 0, p.status)) aborted = 1;
+            int chunk = 0;
+            for (int pos = 0; !aborted; ++chunk) {
+                const uint32_t hdr = sched[pos];
+                const int ne = (int)(hdr >> 8), nr = (int)(hdr & 0xFFu);
+                if (ne == 0) break;
+                const int st = chunk % g.stages;
+                if (!mbar_wait(&full[st], (chunk / g.stages) & 1, p.status)) {
                     aborted = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a_addr = a_base + sa * G::A_BYTES;
-                for (int r = 0; r < nrec; ++r) {
-                    const int slot = p.recs[5 * (roff + r)];
-                    const int sb = ib % G::SB;
-                    if (!mbar_wait(&fullB[sb], (ib / G::SB) & 1, p.status)) {
-                        aborted = 1;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t b_addr = b_base + sb * G::B_BYTES;
-                    const uint32_t d = tmem + slot * BSE;
+                const uint32_t stage = s_base + st * g.stage_bytes;
+                int r = 0;
+                for (int e = 0; e < ne; ++e) {
+                    const int nrec = (int)(sched[pos + 1 + e] & 0xFFu);
+                    const uint32_t a_addr = stage + e * g.a_slot;
+                    for (int j = 0; j < nrec; ++j, ++r) {
+                        const int slot = (int)(sched[pos + 1 + ne + r * RW] & 31u);
+                        const uint32_t b_addr = stage + g.b_off + r * G::B_SLOT;
+                        const uint32_t d = tmem + slot * BSE;
 #pragma unroll
-                    for (int ks = 0; ks < G::KSTEPS; ++ks) {
-                        uint64_t ad = sdesc(a_addr + ks * G::A_KSTEP, G::A_LBO, G::A_SBO, G::A_SWZ);
-                        uint64_t bd = sdesc(b_addr + ks * B_KSTEP, B_LBO, B_SBO, B_SWZ);
-                        mma_ss(d, ad, bd, IDESC, ((inited >> slot) & 1u) | (ks > 0 ? 1u : 0u));
+                        for (int ks = 0; ks < G::KSTEPS; ++ks) {
+                            uint64_t ad = sdesc(a_addr + ks * G::A_KSTEP, G::A_LBO, G::A_SBO, G::A_SWZ);
+                            uint64_t bd = sdesc(b_addr + ks * B_KSTEP, B_LBO, B_SBO, B_SWZ);
+                            mma_ss(d, ad, bd, IDESC, ((inited >> slot) & 1u) | (ks > 0 ? 1u : 0u));
+                        }
+                        inited |= 1u << slot;
                     }
-                    inited |= 1u << slot;
-                    mma_commit(&emptyB[sb]);
-                    ++ib;
                 }
-                mma_commit(&emptyA[sa]);
-                ++ia;
+                mma_commit(&empty[st]);
+                pos += 1 + ne + nr * RW;
             }
             mma_commit(&acc_full);
         }
@@ -484,7 +560,7 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
-        const int row = q * 32 + (threadIdx.x & 31);
+        const int row = q * 32 + lane;
         const int n = n0 + row;
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full, 0, p.status));
         tc_fence_after();
@@ -522,7 +598,9 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
                             *reinterpret_cast<uint4 *>(dst + j) = pk;
                         }
                     } else {
-                        for (int j = 0; j < BSE && f0 + j < p.Fout; ++j) dst[j] = cvt1<BF16>(v[j]);
+#pragma unroll
+                        for (int j = 0; j < BSE; ++j)
+                            if (f0 + j < p.Fout) dst[j] = cvt1<BF16>(v[j]);
                     }
                 } else {
 #pragma unroll
@@ -548,18 +626,18 @@ struct UpMaps {
 
 struct UpParams {
     float *dw;
-    const int32_t *units, *recs;
+    const int32_t *table;
     int32_t *status;
     int N, G, accumulate;
 };
 
 template <int BSE, int FA> struct UpGeo {
     static constexpr int TK = 64;                                   // minibatch rows per stage
-    static constexpr int A_BYTES = 128 * TK * 2;                    // 8 stacked panels max (16 KB)
+    static constexpr int A_BYTES = 128 * TK * 2;                    // up to 128/BSE stacked panels (16 KB)
     static constexpr int B_BYTES = TK * BSE * 2;
     static constexpr int PANEL = TK * BSE * 2;                      // one stacked panel
-    static constexpr int STAGES = BSE == 32 ? 5 : 6;
-    static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES);
+    static constexpr int STAGES = BSE == 32 ? 4 : 5;
+    static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + kTableWords * 4;
     // fa=1: A MN-major (rows n, BSE features contiguous); fa=0: A K-major (rows = features, n contiguous).
     static constexpr uint32_t A_SWZ = FA ? (BSE == 32 ? SW_64 : SW_32) : SW_128;
     static constexpr uint32_t A_LBO = FA ? PANEL : 16;
@@ -571,13 +649,15 @@ template <int BSE, int FA> struct UpGeo {
     static constexpr uint32_t B_KSTEP = A_KSTEP;
 };
 
+// Persistent weight-gradient kernel: each CTA walks its unit table; TMA loads stream
+// through the stage ring across unit boundaries; two TMEM accumulators let the epilogue of
+// one unit overlap the MMAs of the next.
 template <int BS, int FA, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
 k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
 {
     constexpr int BSE = BS == 8 ? 16 : BS;
     constexpr bool COARSE = BS == 8;
-    constexpr int MS = 128 / BSE;
     using G = UpGeo<BSE, FA>;
     constexpr uint32_t IDESC = idesc_f16(128, BSE, BF16, FA == 1, FA == 1);
 
@@ -585,16 +665,15 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + G::STAGES * G::A_BYTES;
-    __shared__ __align__(8) uint64_t full[G::STAGES], empty[G::STAGES], acc_full;
+    int32_t *tab = reinterpret_cast<int32_t *>(sB + G::STAGES * G::B_BYTES);
+    __shared__ __align__(8) uint64_t full[G::STAGES], empty[G::STAGES], acc_full[2], acc_empty[2], tab_full;
     __shared__ uint32_t tmem_base;
     __shared__ volatile int aborted;
 
     const int warp = threadIdx.x / 32;
-    const int kc = p.units[3 * blockIdx.x];
-    const int roff = p.units[3 * blockIdx.x + 1];
-    const int nrec = p.units[3 * blockIdx.x + 2];
+    const int lane = threadIdx.x & 31;
     const int chunks = (p.N + G::TK - 1) / G::TK;
-    const int total = chunks * p.G;
+    const int total = chunks * p.G;                 // stages per unit
 
     if (threadIdx.x == 0) {
         aborted = 0;
@@ -602,120 +681,151 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        mbar_init(&acc_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);            // one arrival per epilogue warp
+        }
+        mbar_init(&tab_full, 1);
         fence_barrier_init();
     }
-    if (warp == 1) tmem_alloc(&tmem_base, 32);
+    if (warp == 1) tmem_alloc(&tmem_base, 64);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    const int32_t *gtab = p.table + (size_t)blockIdx.x * kTableWords;
+    if (warp == 0 && lane == 0) {
+        const int nu = gtab[0];
+        const uint32_t bytes = (uint32_t)(4 + nu * kUnitWords) * 4u;
+        mbar_arrive_expect_tx(&tab_full, bytes);
+        bulk_load(tab, gtab, bytes, &tab_full, policy_evict_first());
+    }
+    const bool tab_ok = mbar_wait(&tab_full, 0, p.status);
+    const int nunits = tab_ok ? tab[0] : 0;
 
     if (warp == 0) {
-        if (elect_one()) {
-            const uint64_t pol = policy_evict_last();
+        // TMA producer: lane r < nrec loads stacked panel r, lane nrec the dy panel.
+        const uint64_t pol = policy_evict_last();
+        int it = 0;
+        for (int u = 0; u < nunits && !aborted; ++u) {
+            const int32_t *ut = tab + 4 + u * kUnitWords;
+            const int kc = ut[0], nrec = ut[1];
+            const int cc = lane < nrec ? ut[2 + 5 * lane] : 0;
             const uint32_t bytes = nrec * G::PANEL + G::B_BYTES;
-            int it = 0;
-            for (; it < total && !aborted; ++it) {
-                const int t = it / chunks, n0 = (it % chunks) * G::TK;
+            for (int c = 0; c < total; ++c, ++it) {
+                const int t = c / chunks, n0 = (c % chunks) * G::TK;
                 const int s = it % G::STAGES;
-                if (it >= G::STAGES && !mbar_wait(&empty[s], ((it / G::STAGES) - 1) & 1, p.status)) {
-                    aborted = 1;
-                    break;
+                if (lane == 0) {
+                    if (it >= G::STAGES && !mbar_wait(&empty[s], ((it / G::STAGES) - 1) & 1, p.status)) aborted = 1;
+                    else mbar_arrive_expect_tx(&full[s], bytes);
                 }
-                mbar_arrive_expect_tx(&full[s], bytes);
-                uint8_t *a = sA + s * G::A_BYTES;
-                for (int r = 0; r < nrec; ++r) {
-                    const int cc = p.recs[5 * (roff + r)];
-                    if (FA) tma_load_2d(a + r * G::PANEL, &maps.x[t], &full[s], cc * BSE, n0, pol);
-                    else tma_load_2d(a + r * G::PANEL, &maps.x[t], &full[s], n0, cc * BSE, pol);
+                __syncwarp();
+                if (aborted) break;
+                if (lane < nrec) {
+                    uint8_t *a = sA + s * G::A_BYTES + lane * G::PANEL;
+                    if (FA) tma_load_2d(a, &maps.x[t], &full[s], cc * BSE, n0, pol);
+                    else tma_load_2d(a, &maps.x[t], &full[s], n0, cc * BSE, pol);
+                } else if (lane == nrec) {
+                    uint8_t *b = sB + s * G::B_BYTES;
+                    if (FA) tma_load_2d(b, &maps.dy[t], &full[s], kc * BSE, n0, pol);
+                    else tma_load_2d(b, &maps.dy[t], &full[s], n0, kc * BSE, pol);
                 }
-                uint8_t *b = sB + s * G::B_BYTES;
-                if (FA) tma_load_2d(b, &maps.dy[t], &full[s], kc * BSE, n0, pol);
-                else tma_load_2d(b, &maps.dy[t], &full[s], n0, kc * BSE, pol);
             }
-            for (int i = std::max(0, it - G::STAGES); i < it; ++i)
-                mbar_wait(&full[i % G::STAGES], (i / G::STAGES) & 1, p.status);
         }
+        if (lane == 0)
+            for (int i = it > G::STAGES ? it - G::STAGES : 0; i < it; ++i)
+                mbar_wait(&full[i % G::STAGES], (i / G::STAGES) & 1, p.status);
         __syncwarp();
     } else if (warp == 1) {
         if (elect_one()) {
             const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-            for (int it = 0; it < total && !aborted; ++it) {
-                const int s = it % G::STAGES;
-                if (!mbar_wait(&full[s], (it / G::STAGES) & 1, p.status)) {
+            int it = 0;
+            for (int u = 0; u < nunits && !aborted; ++u) {
+                const int buf = u & 1;
+                if (u >= 2 && !mbar_wait(&acc_empty[buf], ((u >> 1) - 1) & 1, p.status)) {
                     aborted = 1;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t d = tmem + buf * 32;
+                for (int c = 0; c < total; ++c, ++it) {
+                    const int s = it % G::STAGES;
+                    if (!mbar_wait(&full[s], (it / G::STAGES) & 1, p.status)) {
+                        aborted = 1;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < G::TK / 16; ++ks) {
-                    uint64_t ad = sdesc(a_base + s * G::A_BYTES + ks * G::A_KSTEP, G::A_LBO, G::A_SBO, G::A_SWZ);
-                    uint64_t bd = sdesc(b_base + s * G::B_BYTES + ks * G::B_KSTEP, G::B_LBO, G::B_SBO, G::B_SWZ);
-                    mma_ss(tmem, ad, bd, IDESC, (it > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < G::TK / 16; ++ks) {
+                        uint64_t ad = sdesc(a_base + s * G::A_BYTES + ks * G::A_KSTEP, G::A_LBO, G::A_SBO, G::A_SWZ);
+                        uint64_t bd = sdesc(b_base + s * G::B_BYTES + ks * G::B_KSTEP, G::B_LBO, G::B_SBO, G::B_SWZ);
+                        mma_ss(d, ad, bd, IDESC, (c > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&empty[s]);
                 }
-                mma_commit(&empty[s]);
+                mma_commit(&acc_full[buf]);
             }
-            mma_commit(&acc_full);
         }
         __syncwarp();
     } else {
         const int q = warp & 3;
-        const int row = q * 32 + (threadIdx.x & 31);
+        const int row = q * 32 + lane;
         const int slot = row / BSE, i = row % BSE;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full, 0, p.status));
-        tc_fence_after();
-        float v[BSE];
-        if (ok && total > 0) {
+        for (int u = 0; u < nunits; ++u) {
+            const int buf = u & 1;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (u >> 1) & 1, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            float v[BSE];
 #pragma unroll
             for (int c0 = 0; c0 < BSE; c0 += 16) {
                 uint32_t r[16];
-                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, r);
+                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + buf * 32 + c0, r);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[c0 + j] = __uint_as_float(r[j]);
             }
-        } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            const int32_t *ut = tab + 4 + u * kUnitWords;
+            if (slot < ut[1] && !aborted) {
+                const int32_t *rec = ut + 2 + 5 * slot;
+                if (!COARSE) {
+                    float *dst = p.dw + ((size_t)rec[1] * BS + i) * BS;
 #pragma unroll
-            for (int j = 0; j < BSE; ++j) v[j] = 0.f;
-        }
-        if (slot < nrec && ok) {
-            const int32_t *rec = p.recs + 5 * (roff + slot);
-            if (!COARSE) {
-                float *dst = p.dw + ((size_t)rec[1] * BS + i) * BS;
-#pragma unroll
-                for (int j = 0; j < BS; j += 4) {
-                    float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                    if (p.accumulate) {
-                        float4 a = *reinterpret_cast<float4 *>(dst + j);
-                        o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
-                    }
-                    *reinterpret_cast<float4 *>(dst + j) = o;
-                }
-            } else {
-                const int cs = i / 8, i8 = i % 8;
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    const int32_t id = rec[1 + cs * 2 + ks];
-                    if (id < 0) continue;
-                    float *dst = p.dw + ((size_t)id * 8 + i8) * 8;
-#pragma unroll
-                    for (int j = 0; j < 8; j += 4) {
-                        float4 o = make_float4(v[ks * 8 + j], v[ks * 8 + j + 1], v[ks * 8 + j + 2], v[ks * 8 + j + 3]);
+                    for (int j = 0; j < BS; j += 4) {
+                        float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
                         if (p.accumulate) {
                             float4 a = *reinterpret_cast<float4 *>(dst + j);
                             o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
                         }
                         *reinterpret_cast<float4 *>(dst + j) = o;
                     }
+                } else {
+                    const int cs = i / 8, i8 = i % 8;
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const int32_t id = rec[1 + cs * 2 + ks];
+                        if (id < 0) continue;
+                        float *dst = p.dw + ((size_t)id * 8 + i8) * 8;
+#pragma unroll
+                        for (int j = 0; j < 8; j += 4) {
+                            float4 o = make_float4(v[ks * 8 + j], v[ks * 8 + j + 1], v[ks * 8 + j + 2], v[ks * 8 + j + 3]);
+                            if (p.accumulate) {
+                                float4 a = *reinterpret_cast<float4 *>(dst + j);
+                                o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
+                            }
+                            *reinterpret_cast<float4 *>(dst + j) = o;
+                        }
+                    }
                 }
             }
         }
-        (void)MS;
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, 32);
+    if (warp == 1) tmem_dealloc(tmem, 64);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -723,29 +833,28 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
 // ---------------------------------------------------------------------------------------
 
 template <int BS, int FA, bool BWD, bool BF16>
-bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const void *act, const void *w, void *out, int N, bsmm_dtype t,
-                      cudaStream_t s)
+bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const FbStages &geo, const void *act, const void *w, void *out,
+                      int N, bsmm_dtype t, cudaStream_t s)
 {
     constexpr int BSE = BS == 8 ? 16 : BS;
-    using G = FbGeo<BSE, FA>;
     TcState *st = state(h);
     const int C = h->R * BS, K = h->S * BS;
     const int Fin = BWD ? K : C, Fout = BWD ? C : K;
     CUtensorMap m_act, m_w, m_zero;
     bool ok;
-    if (FA) ok = make_map2d(&m_act, act, t, Fin, N, BSE, 128, swz_for_row_bytes(BSE * 2));
+    if (FA) ok = make_map2d(&m_act, act, t, Fin, N, BSE, geo.half ? 64 : 128, swz_for_row_bytes(BSE * 2));
     else ok = make_map2d(&m_act, act, t, N, Fin, 64, BSE, CU_TENSOR_MAP_SWIZZLE_128B);
     const uint64_t wrows = (uint64_t)std::max<int64_t>(h->nnz, 1) * BS;
     const void *wp = h->nnz > 0 ? w : st->d_zero;
     if (BS == 8) ok = ok && make_map2d(&m_w, wp, t, 8, h->nnz > 0 ? wrows : 16, 8, 8, CU_TENSOR_MAP_SWIZZLE_NONE);
     else ok = ok && make_map2d(&m_w, wp, t, BS, h->nnz > 0 ? wrows : BS, BS, BS, swz_for_row_bytes(BS * 2));
-    ok = ok && make_map2d(&m_zero, st->d_zero, t, 8, 16, 8, 8, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok = ok && make_map2d(&m_zero, st->d_zero, t, 8, kZeroTiles * 8, 8, 8, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return BSMM_ERR_CUDA;
     FbParams p;
     p.out = out;
-    p.win_ptr = fs.d_win_ptr;
-    p.ents = fs.d_ents;
-    p.recs = fs.d_recs;
+    p.stream = fs.d_stream;
+    p.win_off = fs.d_win_off;
+    p.win_len = fs.d_win_len;
     p.win_order = fs.d_win_order;
     p.win_mask = fs.d_win_mask;
     p.status = h->d_status;
@@ -754,10 +863,15 @@ bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const void *act, const void *w, 
     p.W = fs.W;
     p.Fslots = fs.Fslots;
     p.n_tiles = (N + 127) / 128;
-    const int smem = G::SMEM + 1024;
+    p.g = geo;
+    const int smem = geo.stages * geo.stage_bytes + geo.a_slot + kSchedWords * 4 + 1024;
     auto kern = k_tc_fb<BS, FA, BWD, BF16>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return BSMM_ERR_CUDA;
+    static std::atomic<int> attr_set{-1};     // device ordinal the attribute was last set for
+    if (attr_set.load() != h->device) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
+            return BSMM_ERR_CUDA;
+        attr_set.store(h->device);
+    }
     dim3 grid(fs.nwin * p.n_tiles);
     kern<<<grid, kThreads, smem, s>>>(m_act, m_w, m_zero, p);
     g_bsmm_launches += 1;
@@ -786,40 +900,85 @@ bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, float *dw, i
     }
     UpParams p;
     p.dw = dw;
-    p.units = us.d_units;
-    p.recs = us.d_recs;
+    p.table = us.d_table;
     p.status = h->d_status;
     p.N = N;
     p.G = g.G;
     p.accumulate = acc;
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat<BS, FA, BF16>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return BSMM_ERR_CUDA;
-    kern<<<us.nunits, kThreads, smem, s>>>(maps, p);
+    static std::atomic<int> attr_set{-1};
+    if (attr_set.load() != h->device) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return BSMM_ERR_CUDA;
+        attr_set.store(h->device);
+    }
+    kern<<<us.ctas, kThreads, smem, s>>>(maps, p);
     g_bsmm_launches += 1;
     return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+}
+
+// Stage geometry for a call: chunk sizes per block size, as many stages as fit.  When
+// every unit gets its own SM the CTA takes most of shared memory, otherwise two CTAs
+// share an SM so one's epilogue overlaps the other's main loop.
+FbStages choose_stages(const bsmm_ctx *h, int N, int64_t units)
+{
+    const int bse = h->bs == 8 ? 16 : h->bs;
+    FbStages g;
+    g.half = N <= 64 ? 1 : 0;
+    g.a_slot = (g.half ? 64 : 128) * bse * 2;
+    const int b_slot = bse * bse * 2;
+    const int a_ops = (h->fa || g.half) ? 1 : 2, b_ops = h->bs == 8 ? 4 : 1;
+    g.e_slots = h->bs == 32 ? 2 : 4;
+    g.r_slots = h->bs == 32 ? 4 : h->bs == 16 ? 8 : 7;
+    g.r_slots = std::min(g.r_slots, (32 - g.e_slots * a_ops) / b_ops);
+    g.b_off = g.e_slots * g.a_slot;
+    g.stage_bytes = (g.b_off + g.r_slots * b_slot + 1023) & ~1023;
+    const int budget = units <= h->sm_count ? 196 * 1024 : 96 * 1024;
+    g.stages = std::max(2, std::min(kMaxStages, (budget - g.a_slot) / g.stage_bytes));
+    return g;
 }
 
 template <bool BWD>
 bsmm_status fb_dispatch(bsmm_ctx *h, const void *act, const void *w, void *out, int N, bsmm_dtype t, cudaStream_t s)
 {
     TcState *st = state(h);
-    const int wl = choose_wlog(h, BWD, (N + 127) / 128);
-    FbSched &fs = st->fb[BWD ? 1 : 0][wl];
+    const int a_ops = (h->fa || N <= 64) ? 1 : 2, b_ops = h->bs == 8 ? 4 : 1;
+    const int wl_max = h->bs == 32 ? 3 : 4;
+    const int n_tiles = (N + 127) / 128;
+    int wl = h->tc_wlog >= 0 ? std::min(h->tc_wlog, wl_max) : choose_wlog(h, BWD, n_tiles);
+    FbSched *fs = nullptr;
+    FbStages geo{};
     {
         std::lock_guard<std::mutex> lk(st->mu);
         if (!st->d_zero) {
-            if (cudaMalloc(&st->d_zero, 4096) != cudaSuccess) return BSMM_ERR_OOM;
-            if (cudaMemset(st->d_zero, 0, 4096) != cudaSuccess) return BSMM_ERR_CUDA;
+            if (cudaMalloc(&st->d_zero, kZeroBytes) != cudaSuccess) return BSMM_ERR_OOM;
+            if (cudaMemset(st->d_zero, 0, kZeroBytes) != cudaSuccess) return BSMM_ERR_CUDA;
         }
-        if (!fs.built && !build_fb(h, fs, BWD, 1 << wl)) return BSMM_ERR_OOM;
+        // Shrink the window until its schedule stream fits the shared-memory budget.
+        for (; wl >= 0; --wl) {
+            int Fslots, Fsrc, bse;
+            fb_shape(h, BWD, Fslots, Fsrc, bse);
+            const int W = std::min(1 << wl, Fslots);
+            geo = choose_stages(h, N, (int64_t)((Fslots + W - 1) / W) * n_tiles);
+            const uint64_t key = (uint64_t)BWD | ((uint64_t)wl << 1) | ((uint64_t)geo.e_slots << 8) |
+                                 ((uint64_t)geo.r_slots << 16) | ((uint64_t)a_ops << 24);
+            FbSched &c = st->fb[key];
+            if (!c.built && !c.too_big &&
+                !build_fb(h, c, BWD, 1 << wl, geo.e_slots, geo.r_slots, a_ops, b_ops, kSchedWords))
+                return BSMM_ERR_OOM;
+            if (c.built) {
+                fs = &c;
+                break;
+            }
+        }
     }
+    if (!fs) return BSMM_ERR_UNSUPPORTED;     // caller falls back to the SIMT kernels
     const bool bf = t == BSMM_BF16;
 #define FB_CASE(BS_, FA_)                                                                                   \
     if (h->bs == BS_ && h->fa == FA_)                                                                       \
-        return bf ? launch_fb<BS_, FA_, BWD, true>(h, fs, act, w, out, N, t, s)                            \
-                  : launch_fb<BS_, FA_, BWD, false>(h, fs, act, w, out, N, t, s);
+        return bf ? launch_fb<BS_, FA_, BWD, true>(h, *fs, geo, act, w, out, N, t, s)                      \
+                  : launch_fb<BS_, FA_, BWD, false>(h, *fs, geo, act, w, out, N, t, s);
     FB_CASE(32, 1)
     FB_CASE(32, 0)
     FB_CASE(16, 1)
@@ -860,7 +1019,7 @@ bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dty
         std::lock_guard<std::mutex> lk(st->mu);
         if (!st->up.built && !build_up(h, st->up)) return BSMM_ERR_OOM;
     }
-    if (st->up.nunits == 0) return BSMM_OK;
+    if (st->up.ctas == 0) return BSMM_OK;
     const bool bf = t == BSMM_BF16;
 #define UP_CASE(BS_, FA_)                                                                         \
     if (h->bs == BS_ && h->fa == FA_)                                                             \
@@ -880,16 +1039,15 @@ void tc_release(bsmm_ctx *h)
 {
     if (!h->tc) return;
     TcState *st = static_cast<TcState *>(h->tc);
-    for (auto &pass : st->fb)
-        for (auto &f : pass) {
-        cudaFree(f.d_win_ptr);
-        cudaFree(f.d_ents);
-        cudaFree(f.d_recs);
+    for (auto &kv : st->fb) {
+        FbSched &f = kv.second;
+        cudaFree(f.d_stream);
+        cudaFree(f.d_win_off);
+        cudaFree(f.d_win_len);
         cudaFree(f.d_win_order);
         cudaFree(f.d_win_mask);
-        }
-    cudaFree(st->up.d_units);
-    cudaFree(st->up.d_recs);
+    }
+    cudaFree(st->up.d_table);
     cudaFree(st->d_zero);
     delete st;
     h->tc = nullptr;

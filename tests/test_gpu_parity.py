@@ -288,3 +288,22 @@ def test_errors_reported():
         bsmm.bsmm_updat(m.handle, x, x, torch.zeros(m.w_shape, dtype=torch.float16, device="cuda"), 72)
     assert e.value.code == bsmm.ERR_UNSUPPORTED
     m.sync_status()
+
+
+@pytest.mark.parametrize("bs,fa,dtype", [(32, 1, "bf16"), (16, 0, "f16"), (8, 0, "bf16"), (8, 1, "f16")])
+def test_window_sizes_bit_identical(monkeypatch, bs, fa, dtype):
+    """The tensor-core fprop/bprop split output blocks into windows; each output is
+    accumulated over its source blocks in the same order for every window size, so
+    every window size gives the same bits (and matches the oracle)."""
+    L, x, w, dy, ref_y, ref_dx, _ = small_case(bs, fa, dtype)
+    xc, wc, dyc = x.cuda(), w.cuda(), dy.cuda()
+    outs = []
+    for wlog in range(0, 5):
+        monkeypatch.setenv("BSMM_TC_WLOG", str(wlog))
+        m = make(L, bs, fa, "auto")
+        outs.append((m.fprop(xc, wc), m.bprop(dyc, wc)))
+        m.sync_status()
+    for y, dx in outs[1:]:
+        assert torch.equal(y, outs[0][0]) and torch.equal(dx, outs[0][1])
+    assert rel_fro(cpu64(outs[0][0]), ref_y) <= TIGHT[dtype]
+    assert rel_fro(cpu64(outs[0][1]), ref_dx) <= TIGHT[dtype]
