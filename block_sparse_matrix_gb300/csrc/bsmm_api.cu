@@ -70,6 +70,7 @@ bsmm_status bsmm_create(bsmm_t *out, const uint8_t *layout_host, int R, int S, i
     h->bs = block_size;
     h->fa = feature_axis;
     if (const char *e = getenv("BSMM_TC_WLOG")) h->tc_wlog = atoi(e);
+    if (const char *e = getenv("BSMM_TC_STAGE_KB")) h->tc_stage_kb = atoi(e);
     if (cudaGetDevice(&h->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
         delete h;

@@ -34,6 +34,7 @@ struct bsmm_ctx {
     // Tensor-core schedules (built lazily by the tcgen05 path).
     void *tc = nullptr;
     int tc_wlog = -1;   // fprop/bprop window size override (log2), from BSMM_TC_WLOG; -1 = automatic
+    int tc_stage_kb = -1;  // fprop/bprop per-CTA stage budget override (KB), from BSMM_TC_STAGE_KB
 };
 
 extern std::atomic<int64_t> g_bsmm_launches;

@@ -44,12 +44,14 @@ namespace {
 // Schedule of fprop/bprop: one packed word stream per window of W output blocks, cut
 // into chunks; a chunk is what one pipeline stage holds.
 //   chunk header: (ne << 8) | nr     -- ne entries then nr records follow; 0 ends the stream
-//   entry word:   (src << 8) | nrec  -- src = source block (coarse c for fprop, coarse k for
-//                 bprop) whose activation panel is loaded into the stage; its nrec records are
-//                 the next nrec records of the chunk
-//   record (bs 32/16): ((block id + 1) << 5) | slot
-//   record (bs 8, coarse 16x16 block): 4 words, ((id00 + 1) << 5) | slot, id01 + 1,
-//                 id10 + 1, id11 + 1, where idXY is the 8x8 block (2c'+X, 2k'+Y), 0 = absent
+//   entry word:   (src << 8) | nrec  -- src = source panel group whose activations are loaded
+//                 into the stage; its nrec records are the next nrec records of the chunk.  With
+//                 (N,C) activations a group is the 128/(2 bs) adjacent source blocks (coarse c for
+//                 fprop, coarse k for bprop) that make one 128-byte row; with (C,N) it is one block
+//   record (bs 32/16): ((block id + 1) << 7) | (sub << 5) | slot, sub = block within the group
+//   record (bs 8, coarse 16x16 block): 4 words, ((id00 + 1) << 7) | (sub << 5) | slot,
+//                 id01 + 1, id10 + 1, id11 + 1, where idXY is the 8x8 block (2c'+X, 2k'+Y),
+//                 0 = absent
 // Streams start on 16-byte boundaries and are padded to a multiple of 4 words so a CTA
 // can bulk-copy its window into shared memory.
 struct FbSched {
@@ -190,6 +192,7 @@ bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W, int e_max, int r_max, i
     const int rw = coarse ? 4 : 1;                      // words per record
     int Fslots, Fsrc, bse;
     fb_shape(h, bwd, Fslots, Fsrc, bse);
+    const int gc = h->fa ? 128 / (2 * bse) : 1;         // source blocks per 128-byte activation row
     W = std::min(W, Fslots);
     const int nwin = (Fslots + W - 1) / W;
     BidLookup bid{h};
@@ -204,28 +207,33 @@ bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W, int e_max, int r_max, i
         off[w] = (int32_t)stream.size();
         // entries of this window, each split so that no entry has more than r_max records
         std::vector<Ent> ents;
-        for (int src = 0; src < Fsrc; ++src) {
-            Ent e{src, {}};
-            for (int sl = 0; sl < W; ++sl) {
-                const int o = w * W + sl;
-                if (o >= Fslots) break;
-                const int cc = bwd ? o : src, kc = bwd ? src : o;   // coarse (c', k')
-                bool any = false;
-                for (int cs = 0; cs < f; ++cs)
-                    for (int ks = 0; ks < f; ++ks) {
-                        ids[cs * 2 + ks] = bid(cc * f + cs, kc * f + ks);
-                        any |= ids[cs * 2 + ks] >= 0;
-                    }
-                if (!any) continue;
-                e.recs.push_back(((uint32_t)(ids[0] + 1) << 5) | (uint32_t)sl);
-                if (coarse)
-                    for (int q = 1; q < 4; ++q) e.recs.push_back((uint32_t)(ids[q] + 1));
-                mask[w] |= 1u << sl;
+        for (int grp = 0; grp * gc < Fsrc; ++grp) {
+            Ent e{grp, {}};
+            // records by sub-block then slot, so every output sees its sources in increasing order
+            for (int sub = 0; sub < gc; ++sub) {
+                const int src = grp * gc + sub;
+                if (src >= Fsrc) break;
+                for (int sl = 0; sl < W; ++sl) {
+                    const int o = w * W + sl;
+                    if (o >= Fslots) break;
+                    const int cc = bwd ? o : src, kc = bwd ? src : o;   // coarse (c', k')
+                    bool any = false;
+                    for (int cs = 0; cs < f; ++cs)
+                        for (int ks = 0; ks < f; ++ks) {
+                            ids[cs * 2 + ks] = bid(cc * f + cs, kc * f + ks);
+                            any |= ids[cs * 2 + ks] >= 0;
+                        }
+                    if (!any) continue;
+                    e.recs.push_back(((uint32_t)(ids[0] + 1) << 7) | ((uint32_t)sub << 5) | (uint32_t)sl);
+                    if (coarse)
+                        for (int q = 1; q < 4; ++q) e.recs.push_back((uint32_t)(ids[q] + 1));
+                    mask[w] |= 1u << sl;
+                }
             }
             const int n = (int)e.recs.size() / rw;
             for (int r0 = 0; r0 < n; r0 += r_max) {
                 const int r1 = std::min(n, r0 + r_max);
-                ents.push_back(Ent{src, std::vector<uint32_t>(e.recs.begin() + r0 * rw, e.recs.begin() + r1 * rw)});
+                ents.push_back(Ent{grp, std::vector<uint32_t>(e.recs.begin() + r0 * rw, e.recs.begin() + r1 * rw)});
             }
             work[w] += n ? n + 2 : 0;
         }
@@ -329,7 +337,10 @@ TcState *state(bsmm_ctx *h)
 // Device side
 // ---------------------------------------------------------------------------------------
 
-constexpr int kThreads = 192;
+constexpr int kProducers = 4;                    // fprop/bprop: producer+epilogue warps, then the MMA warp
+constexpr int kFbThreads = 32 * (kProducers + 1);
+constexpr int kUpThreads = 32 * (kProducers + 5);        // updat: producers, MMA warp, 4 epilogue warps
+static_assert(16 % kProducers == 0, "stage counts must be multiples of the producer count");
 constexpr int kZeroTiles = 2048;                 // 8x8 zero tiles in the zero buffer (256 KB)
 constexpr int kZeroBytes = kZeroTiles * 128;
 
@@ -369,14 +380,17 @@ template <> __device__ __forceinline__ uint16_t cvt1<false>(float a)
 template <int BSE, int FA> struct FbGeo {
     static constexpr int B_SLOT = BSE * BSE * 2;                     // one (coarse) weight block
     static constexpr int KSTEPS = BSE / 16;
-    // A operand descriptor parameters
-    static constexpr uint32_t A_SWZ = FA ? (BSE == 32 ? SW_64 : SW_32) : SW_128;
+    // A operand descriptor parameters.  (N,C) activations: K-major rows of 128 bytes holding
+    // GC = 64/BSE adjacent source blocks; block `sub` starts sub*BSE*2 bytes into the row.
+    // (C,N) activations: MN-major, two 64-row atoms of one block.
+    static constexpr uint32_t A_SWZ = SW_128;
     static constexpr uint32_t A_LBO = FA ? 16 : (BSE * 128);         // MN-major: distance of the two 64-row atoms
-    static constexpr uint32_t A_SBO = FA ? (8 * BSE * 2) : 1024;
+    static constexpr uint32_t A_SBO = 1024;
     static constexpr uint32_t A_KSTEP = FA ? 32 : (16 * 128);
+    static constexpr uint32_t A_SUB = BSE * 2;                       // byte offset of block `sub` in a row
 };
 
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 16;                   // a multiple of kProducers
 constexpr int kMaxSmem = 216 * 1024;         // largest dynamic request (static shared memory counts against 227 KB)
 constexpr int kSchedWords = 3072;                                    // window stream budget (12 KB)
 
@@ -387,6 +401,7 @@ constexpr int kSchedWords = 3072;                                    // window s
 struct FbStages {
     int e_slots, r_slots, stages, half;
     int a_slot, stage_bytes, b_off;
+    int producers;      // producer warps (1, 2 or 4), a divisor of stages
 };
 
 struct FbParams {
@@ -405,7 +420,7 @@ struct FbParams {
 
 // fprop (BWD=false) / bprop (BWD=true).  BS = fine block size, BSE = 16 when BS = 8.
 template <int BS, int FA, bool BWD, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFbThreads, 1)
 k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
         const __grid_constant__ CUtensorMap tm_zero, const FbParams p)
 {
@@ -425,6 +440,11 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const FbStages g = p.g;
     const int a_ops = (FA || g.half) ? 1 : 2;                         // TMA boxes per activation panel
+    if (g.producers < 1 || g.producers > kProducers || g.stages % g.producers != 0 || g.stages > kMaxStages) {
+        // the host guarantees this; refuse otherwise
+        if (threadIdx.x == 0) atomicExch(p.status, (int32_t)BSMM_ERR_INVALID);
+        return;
+    }
     const uint32_t *sched = reinterpret_cast<const uint32_t *>(smem + g.stages * g.stage_bytes + g.a_slot);
     __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], acc_full, sched_full;
     __shared__ uint32_t tmem_base;
@@ -448,30 +468,34 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
         mbar_init(&sched_full, 1);
         fence_barrier_init();
     }
-    if (warp == 1) tmem_alloc(&tmem_base, alloc_cols);
+    if (warp == kProducers) tmem_alloc(&tmem_base, alloc_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
 
-    if (warp == 0) {
-        // ---------------- TMA producer: one load per lane per chunk ----------------
+    if (warp < kProducers) {
+        // ---------------- TMA producers: warp w < P issues chunks w, w+P, ...; one load per lane ----
         const uint64_t pol_act = policy_evict_last();
         const uint64_t pol_w = policy_evict_first();
-        if (lane == 0) {
+        if (warp == 0 && lane == 0) {
             const int len = p.win_len[win];
             mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
             if (len > 0) bulk_load((void *)sched, p.stream + p.win_off[win], (uint32_t)len * 4u, &sched_full, pol_act);
             prefetch_tmap(&tm_act);
             prefetch_tmap(&tm_w);
         }
-        if (!mbar_wait(&sched_full, 0, p.status)) aborted = 1;
+        if (!mbar_wait_warp(&sched_full, 0, p.status, 64)) aborted = 1;
         __syncwarp();
-        int chunk = 0;
+        int chunk = 0, last = -1;
         for (int pos = 0; !aborted; ++chunk) {
             const uint32_t hdr = sched[pos];
             const int ne = (int)(hdr >> 8), nr = (int)(hdr & 0xFFu);
             if (ne == 0) break;
+            if (chunk % g.producers != warp) {
+                pos += 1 + ne + nr * RW;
+                continue;
+            }
             const int st = chunk % g.stages;
             if (lane == 0) {
                 if (chunk >= g.stages && !mbar_wait(&empty[st], ((chunk / g.stages) - 1) & 1, p.status))
@@ -481,25 +505,26 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
             }
             __syncwarp();
             if (aborted) break;
+            last = chunk;
             uint8_t *stage = smem + st * g.stage_bytes;
             const int na = ne * a_ops;
             if (lane < na) {
                 const int e = lane / a_ops, hf = lane % a_ops;
                 const int src = (int)(sched[pos + 1 + e] >> 8);
                 uint8_t *dst = stage + e * g.a_slot;
-                if (FA) tma_load_2d(dst, &tm_act, &full[st], src * BSE, n0, pol_act);
+                if (FA) tma_load_2d(dst, &tm_act, &full[st], src * 64, n0, pol_act);
                 else tma_load_2d(dst + hf * BSE * 128, &tm_act, &full[st], n0 + 64 * hf, src * BSE, pol_act);
             } else if (lane < na + nr * B_OPS) {
                 const int q = lane - na, r = q / B_OPS, sub = q % B_OPS;
                 const uint32_t *rec = sched + pos + 1 + ne + r * RW;
                 uint8_t *dst = stage + g.b_off + r * G::B_SLOT;
                 if (!COARSE) {
-                    tma_load_2d(dst, &tm_w, &full[st], 0, ((int)(rec[0] >> 5) - 1) * BS, pol_w);
+                    tma_load_2d(dst, &tm_w, &full[st], 0, ((int)(rec[0] >> 7) - 1) * BS, pol_w);
                 } else {
                     // sub-block (cs, ks) -> core matrix at (N-group)*256 + (K-group)*128
                     const int cs = sub >> 1, ks = sub & 1;
                     const int ng = BWD ? cs : ks, kg = BWD ? ks : cs;
-                    const int id = (int)(sub == 0 ? (rec[0] >> 5) : rec[sub]) - 1;
+                    const int id = (int)(sub == 0 ? (rec[0] >> 7) : rec[sub]) - 1;
                     if (id >= 0) {
                         tma_load_2d(dst + ng * 256 + kg * 128, &tm_w, &full[st], 0, id * 8, pol_w);
                     } else {
@@ -511,16 +536,20 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
             }
             pos += 1 + ne + nr * RW;
         }
-        // Drain: wait until every issued load has landed before the CTA may exit.
-        if (lane == 0)
-            for (int i = chunk > g.stages ? chunk - g.stages : 0; i < chunk; ++i)
-                mbar_wait(&full[i % g.stages], (i / g.stages) & 1, p.status);
+        // After an abort, wait (bounded) for this warp's last loads before the CTA may exit.
+        // Normally the MMA warp has waited on every stage, so nothing is left in flight.
+        if (aborted && lane == 0 && last >= 0)
+            mbar_wait(&full[last % g.stages], (last / g.stages) & 1, nullptr);
         __syncwarp();
-    } else if (warp == 1) {
+    } else {
         // ---------------- MMA issuer ----------------
         if (elect_one()) {
             uint32_t inited = 0;
             const uint32_t s_base = smem_u32(smem);
+            // Descriptors of the smem base; an operand at byte offset o is base + (o >> 4)
+            // (the start address is the low 14-bit field, in 16-byte units).
+            const uint64_t a_desc0 = sdesc(s_base, G::A_LBO, G::A_SBO, G::A_SWZ);
+            const uint64_t b_desc0 = sdesc(s_base, B_LBO, B_SBO, B_SWZ);
             if (!mbar_wait(&sched_full, 0, p.status)) aborted = 1;
             int chunk = 0;
             for (int pos = 0; !aborted; ++chunk) {
@@ -533,21 +562,23 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
                     break;
                 }
                 tc_fence_after();
-                const uint32_t stage = s_base + st * g.stage_bytes;
+                const uint32_t stage_off = st * g.stage_bytes;
+                const uint32_t *rec = sched + pos + 1 + ne;
                 int r = 0;
                 for (int e = 0; e < ne; ++e) {
                     const int nrec = (int)(sched[pos + 1 + e] & 0xFFu);
-                    const uint32_t a_addr = stage + e * g.a_slot;
+                    const uint32_t a_off = stage_off + e * g.a_slot;
                     for (int j = 0; j < nrec; ++j, ++r) {
-                        const int slot = (int)(sched[pos + 1 + ne + r * RW] & 31u);
-                        const uint32_t b_addr = stage + g.b_off + r * G::B_SLOT;
+                        const uint32_t rw0 = rec[r * RW];
+                        const uint32_t slot = rw0 & 31u;
+                        const uint64_t ad = a_desc0 + ((a_off + ((rw0 >> 5) & 3u) * G::A_SUB) >> 4);
+                        const uint64_t bd = b_desc0 + ((stage_off + g.b_off + r * G::B_SLOT) >> 4);
                         const uint32_t d = tmem + slot * BSE;
+                        const uint32_t acc = (inited >> slot) & 1u;
 #pragma unroll
-                        for (int ks = 0; ks < G::KSTEPS; ++ks) {
-                            uint64_t ad = sdesc(a_addr + ks * G::A_KSTEP, G::A_LBO, G::A_SBO, G::A_SWZ);
-                            uint64_t bd = sdesc(b_addr + ks * B_KSTEP, B_LBO, B_SBO, B_SWZ);
-                            mma_ss(d, ad, bd, IDESC, ((inited >> slot) & 1u) | (ks > 0 ? 1u : 0u));
-                        }
+                        for (int ks = 0; ks < G::KSTEPS; ++ks)
+                            mma_ss(d, ad + ((ks * G::A_KSTEP) >> 4), bd + ((ks * B_KSTEP) >> 4), IDESC,
+                                   ks > 0 ? 1u : acc);
                         inited |= 1u << slot;
                     }
                 }
@@ -557,12 +588,13 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
             mma_commit(&acc_full);
         }
         __syncwarp();
-    } else {
-        // ---------------- epilogue (warps 2..5) ----------------
+    }
+    if (warp < kProducers) {
+        // ---------------- epilogue (producer warps 0..3, one TMEM lane quarter each) ----
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
         const int n = n0 + row;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full, 0, p.status));
+        const bool ok = mbar_wait_warp(&acc_full, 0, p.status, 256);
         tc_fence_after();
         const uint32_t mask = p.win_mask[win];
         uint16_t *out = static_cast<uint16_t *>(p.out);
@@ -612,7 +644,7 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, alloc_cols);
+    if (warp == kProducers) tmem_dealloc(tmem, alloc_cols);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -636,7 +668,7 @@ template <int BSE, int FA> struct UpGeo {
     static constexpr int A_BYTES = 128 * TK * 2;                    // up to 128/BSE stacked panels (16 KB)
     static constexpr int B_BYTES = TK * BSE * 2;
     static constexpr int PANEL = TK * BSE * 2;                      // one stacked panel
-    static constexpr int STAGES = BSE == 32 ? 4 : 5;
+    static constexpr int STAGES = 4;                                 // a multiple of kProducers
     static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + kTableWords * 4;
     // fa=1: A MN-major (rows n, BSE features contiguous); fa=0: A K-major (rows = features, n contiguous).
     static constexpr uint32_t A_SWZ = FA ? (BSE == 32 ? SW_64 : SW_32) : SW_128;
@@ -653,12 +685,13 @@ template <int BSE, int FA> struct UpGeo {
 // through the stage ring across unit boundaries; two TMEM accumulators let the epilogue of
 // one unit overlap the MMAs of the next.
 template <int BS, int FA, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kUpThreads, 1)
 k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
 {
     constexpr int BSE = BS == 8 ? 16 : BS;
     constexpr bool COARSE = BS == 8;
     using G = UpGeo<BSE, FA>;
+    static_assert(G::STAGES % kProducers == 0, "producer warp w must own stages w, w+4, ...");
     constexpr uint32_t IDESC = idesc_f16(128, BSE, BF16, FA == 1, FA == 1);
 
     extern __shared__ uint8_t smem_raw[];
@@ -688,7 +721,7 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
         mbar_init(&tab_full, 1);
         fence_barrier_init();
     }
-    if (warp == 1) tmem_alloc(&tmem_base, 64);
+    if (warp == kProducers) tmem_alloc(&tmem_base, 64);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -700,19 +733,21 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
         mbar_arrive_expect_tx(&tab_full, bytes);
         bulk_load(tab, gtab, bytes, &tab_full, policy_evict_first());
     }
-    const bool tab_ok = mbar_wait(&tab_full, 0, p.status);
+    const bool tab_ok = mbar_wait_warp(&tab_full, 0, p.status, 64);
     const int nunits = tab_ok ? tab[0] : 0;
 
-    if (warp == 0) {
-        // TMA producer: lane r < nrec loads stacked panel r, lane nrec the dy panel.
+    if (warp < kProducers) {
+        // TMA producers: warp w issues stage iterations w, w+4, ...; in each, lane r < nrec
+        // loads stacked panel r and lane nrec the dy panel.
         const uint64_t pol = policy_evict_last();
-        int it = 0;
+        int it = 0, last = -1;
         for (int u = 0; u < nunits && !aborted; ++u) {
             const int32_t *ut = tab + 4 + u * kUnitWords;
             const int kc = ut[0], nrec = ut[1];
             const int cc = lane < nrec ? ut[2 + 5 * lane] : 0;
             const uint32_t bytes = nrec * G::PANEL + G::B_BYTES;
             for (int c = 0; c < total; ++c, ++it) {
+                if (it % kProducers != warp) continue;
                 const int t = c / chunks, n0 = (c % chunks) * G::TK;
                 const int s = it % G::STAGES;
                 if (lane == 0) {
@@ -721,6 +756,7 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
                 }
                 __syncwarp();
                 if (aborted) break;
+                last = it;
                 if (lane < nrec) {
                     uint8_t *a = sA + s * G::A_BYTES + lane * G::PANEL;
                     if (FA) tma_load_2d(a, &maps.x[t], &full[s], cc * BSE, n0, pol);
@@ -732,13 +768,14 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
                 }
             }
         }
-        if (lane == 0)
-            for (int i = it > G::STAGES ? it - G::STAGES : 0; i < it; ++i)
-                mbar_wait(&full[i % G::STAGES], (i / G::STAGES) & 1, p.status);
+        // After an abort, wait (bounded) for this warp's last loads before the CTA may exit.
+        if (aborted && lane == 0 && last >= 0)
+            mbar_wait(&full[last % G::STAGES], (last / G::STAGES) & 1, nullptr);
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == kProducers) {
         if (elect_one()) {
-            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+            const uint64_t a_desc0 = sdesc(smem_u32(sA), G::A_LBO, G::A_SBO, G::A_SWZ);
+            const uint64_t b_desc0 = sdesc(smem_u32(sB), G::B_LBO, G::B_SBO, G::B_SWZ);
             int it = 0;
             for (int u = 0; u < nunits && !aborted; ++u) {
                 const int buf = u & 1;
@@ -755,12 +792,12 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
                         break;
                     }
                     tc_fence_after();
+                    const uint64_t ad = a_desc0 + ((s * G::A_BYTES) >> 4);
+                    const uint64_t bd = b_desc0 + ((s * G::B_BYTES) >> 4);
 #pragma unroll
-                    for (int ks = 0; ks < G::TK / 16; ++ks) {
-                        uint64_t ad = sdesc(a_base + s * G::A_BYTES + ks * G::A_KSTEP, G::A_LBO, G::A_SBO, G::A_SWZ);
-                        uint64_t bd = sdesc(b_base + s * G::B_BYTES + ks * G::B_KSTEP, G::B_LBO, G::B_SBO, G::B_SWZ);
-                        mma_ss(d, ad, bd, IDESC, (c > 0 || ks > 0) ? 1u : 0u);
-                    }
+                    for (int ks = 0; ks < G::TK / 16; ++ks)
+                        mma_ss(d, ad + ((ks * G::A_KSTEP) >> 4), bd + ((ks * G::B_KSTEP) >> 4), IDESC,
+                               (c > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(&empty[s]);
                 }
                 mma_commit(&acc_full[buf]);
@@ -773,7 +810,7 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
         const int slot = row / BSE, i = row % BSE;
         for (int u = 0; u < nunits; ++u) {
             const int buf = u & 1;
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (u >> 1) & 1, p.status));
+            const bool ok = mbar_wait_warp(&acc_full[buf], (u >> 1) & 1, p.status, 128);
             if (!ok) break;
             tc_fence_after();
             float v[BSE];
@@ -825,7 +862,7 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, 64);
+    if (warp == kProducers) tmem_dealloc(tmem, 64);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -842,7 +879,7 @@ bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const FbStages &geo, const void 
     const int Fin = BWD ? K : C, Fout = BWD ? C : K;
     CUtensorMap m_act, m_w, m_zero;
     bool ok;
-    if (FA) ok = make_map2d(&m_act, act, t, Fin, N, BSE, geo.half ? 64 : 128, swz_for_row_bytes(BSE * 2));
+    if (FA) ok = make_map2d(&m_act, act, t, Fin, N, 64, geo.half ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_128B);
     else ok = make_map2d(&m_act, act, t, N, Fin, 64, BSE, CU_TENSOR_MAP_SWIZZLE_128B);
     const uint64_t wrows = (uint64_t)std::max<int64_t>(h->nnz, 1) * BS;
     const void *wp = h->nnz > 0 ? w : st->d_zero;
@@ -873,7 +910,7 @@ bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const FbStages &geo, const void 
         attr_set.store(h->device);
     }
     dim3 grid(fs.nwin * p.n_tiles);
-    kern<<<grid, kThreads, smem, s>>>(m_act, m_w, m_zero, p);
+    kern<<<grid, kFbThreads, smem, s>>>(m_act, m_w, m_zero, p);
     g_bsmm_launches += 1;
     return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
@@ -913,29 +950,53 @@ bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, float *dw, i
             return BSMM_ERR_CUDA;
         attr_set.store(h->device);
     }
-    kern<<<us.ctas, kThreads, smem, s>>>(maps, p);
+    kern<<<us.ctas, kUpThreads, smem, s>>>(maps, p);
     g_bsmm_launches += 1;
     return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
-// Stage geometry for a call: chunk sizes per block size, as many stages as fit.  When
-// every unit gets its own SM the CTA takes most of shared memory, otherwise two CTAs
-// share an SM so one's epilogue overlaps the other's main loop.
-FbStages choose_stages(const bsmm_ctx *h, int N, int64_t units)
+// Stage geometry for a call.  P producer warps share the chunks (chunk c -> warp c mod P)
+// and P divides the stage count: warp w then owns stages w, w+P, ... and waits on each
+// stage's `empty` barrier one phase at a time, which is what a parity wait requires.
+// Chunks hold the expected records of one activation entry (window size x blocks per
+// panel group x layout density) so entries are rarely split.  Two CTAs share an SM when
+// there are more units than SMs and two stages fit in half of shared memory (one CTA's
+// prologue and epilogue then overlap the other's main loop); otherwise one CTA takes most
+// of shared memory.
+FbStages choose_stages(const bsmm_ctx *h, int N, int64_t units, int W)
 {
     const int bse = h->bs == 8 ? 16 : h->bs;
     FbStages g;
     g.half = N <= 64 ? 1 : 0;
-    g.a_slot = (g.half ? 64 : 128) * bse * 2;
+    g.a_slot = (g.half ? 64 : 128) * (h->fa ? 128 : bse * 2);
     const int b_slot = bse * bse * 2;
     const int a_ops = (h->fa || g.half) ? 1 : 2, b_ops = h->bs == 8 ? 4 : 1;
-    g.e_slots = h->bs == 32 ? 2 : 4;
-    g.r_slots = h->bs == 32 ? 4 : h->bs == 16 ? 8 : 7;
-    g.r_slots = std::min(g.r_slots, (32 - g.e_slots * a_ops) / b_ops);
-    g.b_off = g.e_slots * g.a_slot;
-    g.stage_bytes = (g.b_off + g.r_slots * b_slot + 1023) & ~1023;
-    const int budget = units <= h->sm_count ? 196 * 1024 : 96 * 1024;
-    g.stages = std::max(2, std::min(kMaxStages, (budget - g.a_slot) / g.stage_bytes));
+    const int gc = h->fa ? 128 / (2 * bse) : 1;
+    const double density = (double)h->nnz / ((double)h->R * h->S);
+    const double coarse_density = h->bs == 8 ? std::min(1.0, 4.0 * density) : density;
+    const int expect_r = (int)(1.25 * W * gc * coarse_density) + 1;
+    g.e_slots = h->fa ? (g.half ? 2 : 1) : (h->bs == 32 ? 2 : 4);
+    const int r_cap = (32 - g.e_slots * a_ops) / b_ops;
+    g.r_slots = std::max(2, std::min(r_cap, g.e_slots * expect_r));
+    const int budget_two = h->tc_stage_kb >= 32 ? std::min(h->tc_stage_kb, 196) * 1024 : 96 * 1024;
+    const int budget_one = h->tc_stage_kb >= 32 ? std::min(h->tc_stage_kb, 196) * 1024 : 196 * 1024;
+    for (;;) {
+        g.b_off = g.e_slots * g.a_slot;
+        g.stage_bytes = (g.b_off + g.r_slots * b_slot + 1023) & ~1023;
+        const bool two = units > h->sm_count && 2 * g.stage_bytes + g.a_slot <= budget_two;
+        const int budget = two ? budget_two : budget_one;
+        g.stages = std::min(kMaxStages, (budget - g.a_slot) / g.stage_bytes);
+        if (g.stages >= 2 || g.r_slots <= 1) break;
+        --g.r_slots;                                   // shrink the chunk until two stages fit
+    }
+    g.stages = std::max(g.stages, 2);
+    if (g.stages >= kProducers) {
+        g.stages = g.stages / kProducers * kProducers;
+        g.producers = kProducers;
+    } else {
+        g.stages = g.stages / 2 * 2;
+        g.producers = 2;
+    }
     return g;
 }
 
@@ -960,7 +1021,7 @@ bsmm_status fb_dispatch(bsmm_ctx *h, const void *act, const void *w, void *out, 
             int Fslots, Fsrc, bse;
             fb_shape(h, BWD, Fslots, Fsrc, bse);
             const int W = std::min(1 << wl, Fslots);
-            geo = choose_stages(h, N, (int64_t)((Fslots + W - 1) / W) * n_tiles);
+            geo = choose_stages(h, N, (int64_t)((Fslots + W - 1) / W) * n_tiles, W);
             const uint64_t key = (uint64_t)BWD | ((uint64_t)wl << 1) | ((uint64_t)geo.e_slots << 8) |
                                  ((uint64_t)geo.r_slots << 16) | ((uint64_t)a_ops << 24);
             FbSched &c = st->fb[key];

@@ -79,6 +79,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     }
 }
 
+// Warp-wide bounded wait: lane 0 polls (sleeping sleep_ns between polls) while the other
+// lanes park at the warp barrier, so waiting warps do not flood the barrier unit.
+// Returns the same result in every lane.  Call with the whole warp converged.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, int32_t *status, uint32_t sleep_ns)
+{
+    uint32_t ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        ok = mbar_try_wait(bar, parity) ? 1u : 0u;
+        if (!ok) {
+            const uint64_t t0 = globaltimer();
+            for (;;) {
+                __nanosleep(sleep_ns);
+                if (mbar_try_wait(bar, parity)) {
+                    ok = 1;
+                    break;
+                }
+                if (globaltimer() - t0 > kWaitNs) {
+                    if (status) atomicExch(status, (int32_t)BSMM_ERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // ---- TMA -------------------------------------------------------------------------------
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m)
