@@ -171,6 +171,10 @@ def run_ours(args):
     m = bsmm.BlocksparseMatMul(L, block_size=bs, feature_axis=1)
     nnz = m.nnz
     passes = pass_list(nnz, bs, C, K, Ns)
+    if args.only:
+        passes = [p for p in passes if p[0] == args.only]
+        if not passes:
+            raise SystemExit("--only must name one of fprop_n1024 bprop_n1024 updat_n1024 fprop_n64 bprop_n64 updat_n64")
     step_flops = sum(p[2] for p in passes)
 
     # Rotating device sets: inputs (x, dy per N, w) and outputs (y, dx per N, dw per N).
@@ -282,7 +286,7 @@ def run_ours(args):
                 "frac": round(achieved / peak, 4), "traffic": traffic_for(name), "kernel": name,
                 "algorithmic_bytes": b, "flops": f, "peak_source": peak_src + " (burst)"}
 
-    e2e = run_e2e(m, inp, Ns, passes, dev, args) if rank == 0 else None
+    e2e = run_e2e(m, inp, Ns, passes, dev, args) if (rank == 0 and not args.only) else None
     cpu = (run_cpu_baseline(wl, inp, Ns, budget_s=args.cpu_budget)
            if (rank == 0 and ws == 1 and args.cpu_budget > 0) else None)
 
@@ -422,7 +426,10 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--cpu-budget", type=float, default=20.0,
+                    help="seconds of CPU time for the oracle baseline sample (0 skips it)")
+    ap.add_argument("--only", default="",
+                    help="time a single pass (e.g. fprop_n1024) instead of the whole step; for kernel profiling")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

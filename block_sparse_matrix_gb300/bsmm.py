@@ -57,6 +57,7 @@ def lib():
             "bsmm_updat_grouped": [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i, i, i, vp, i, vp],
             "bsmm_set_kernel": [vp, i],
             "bsmm_sync_status": [vp, vp],
+            "bsmm_selftest_wait_timeout": [vp, ctypes.c_uint64, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -148,6 +149,10 @@ def bsmm_updat_grouped(h, xs, dys, dw, N: int, accumulate: bool = False, stream=
 
 def bsmm_sync_status(h, stream=None):
     _check(lib().bsmm_sync_status(h, _stream(stream)), "bsmm_sync_status")
+
+
+def bsmm_selftest_wait_timeout(h, limit_ns: int, stream=None):
+    _check(lib().bsmm_selftest_wait_timeout(h, int(limit_ns), _stream(stream)), "bsmm_selftest_wait_timeout")
 
 
 # ---- README-style object -------------------------------------------------------------

@@ -276,4 +276,11 @@ const char *bsmm_status_string(bsmm_status s)
 
 int64_t bsmm_launch_count(void) { return g_bsmm_launches.load(); }
 
+bsmm_status bsmm_selftest_wait_timeout(bsmm_t h, uint64_t limit_ns, void *stream)
+{
+    if (!h || limit_ns == 0 || limit_ns > 10000000000ull) return BSMM_ERR_INVALID;
+    cudaSetDevice(h->device);
+    return launch_wait_selftest(h, limit_ns, (cudaStream_t)stream);
+}
+
 } // extern "C"

@@ -76,3 +76,4 @@ bsmm_status tc_bprop(bsmm_ctx *h, const void *dy, const void *w, void *dx, int N
 bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dtype t,
                      int accumulate, cudaStream_t s);
 void tc_release(bsmm_ctx *h);
+bsmm_status launch_wait_selftest(bsmm_ctx *h, uint64_t limit_ns, cudaStream_t s);

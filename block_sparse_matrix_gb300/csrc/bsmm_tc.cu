@@ -1050,7 +1050,26 @@ bsmm_status fb_dispatch(bsmm_ctx *h, const void *act, const void *w, void *out, 
     return BSMM_ERR_UNSUPPORTED;
 }
 
+// Self-test of the bounded waits: one warp waits on an mbarrier that nothing arrives on.
+__global__ void k_wait_selftest(int32_t *status, uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, status, limit_ns);
+}
+
 } // namespace
+
+bsmm_status launch_wait_selftest(bsmm_ctx *h, uint64_t limit_ns, cudaStream_t s)
+{
+    k_wait_selftest<<<1, 32, 0, s>>>(h->d_status, limit_ns);
+    g_bsmm_launches += 1;
+    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+}
 
 bool tc_supported(bsmm_ctx *h, bsmm_dtype t)
 {

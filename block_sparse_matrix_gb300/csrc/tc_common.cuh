@@ -64,15 +64,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.  On timeout
-// sets *status (if not null) and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *status)
+// Bounded wait for the phase with the given parity to complete.  After limit_ns of
+// %globaltimer time it sets *status (if not null) to BSMM_ERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *status,
+                                          uint64_t limit_ns = kWaitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 63u && globaltimer() - t0 > kWaitNs) {
+        if ((it & 63u) == 63u && globaltimer() - t0 > limit_ns) {
             if (status) atomicExch(status, (int32_t)BSMM_ERR_TIMEOUT);
             return false;
         }

@@ -155,6 +155,16 @@ const char *bsmm_status_string(bsmm_status s);
 /* Number of kernels this library has launched since load (all handles). */
 int64_t bsmm_launch_count(void);
 
+/*
+ * Failure-detection self-test (no counterpart in the README): enqueues a kernel whose
+ * single thread waits on an mbarrier that nothing ever arrives on, using the same bounded
+ * wait as the tensor-core kernels, with a limit of limit_ns nanoseconds (1 .. 1e10).  The
+ * wait gives up, records BSMM_ERR_TIMEOUT in the handle's sticky status, and the kernel
+ * returns normally: a following bsmm_sync_status() reports TIMEOUT and the CUDA context
+ * stays usable.  Errors: INVALID (null handle, limit out of range), CUDA.
+ */
+bsmm_status bsmm_selftest_wait_timeout(bsmm_t h, uint64_t limit_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -65,3 +65,8 @@ def test_null_handle_rejected():
     assert L.bsmm_updat_grouped(None, None, None, 1, 4, 0, None, 0, None) == bsmm.ERR_INVALID
     assert L.bsmm_destroy(None) == bsmm.OK
     assert L.bsmm_set_kernel(None, 0) == bsmm.ERR_INVALID
+
+
+def test_selftest_rejects_bad_arguments_on_host():
+    L = bsmm.lib()
+    assert L.bsmm_selftest_wait_timeout(None, 1000, None) == bsmm.ERR_INVALID

@@ -307,3 +307,19 @@ def test_window_sizes_bit_identical(monkeypatch, bs, fa, dtype):
         assert torch.equal(y, outs[0][0]) and torch.equal(dx, outs[0][1])
     assert rel_fro(cpu64(outs[0][0]), ref_y) <= TIGHT[dtype]
     assert rel_fro(cpu64(outs[0][1]), ref_dx) <= TIGHT[dtype]
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A device wait that nothing satisfies gives up after its limit, the status word
+    reports TIMEOUT, and the same handle keeps computing correct results afterwards."""
+    L = np.eye(4, dtype=np.uint8)
+    m = make(L, 32, 1)
+    bsmm.bsmm_selftest_wait_timeout(m.handle, 20_000_000)        # 20 ms
+    with pytest.raises(bsmm.BsmmError) as e:
+        m.sync_status()
+    assert e.value.code == bsmm.ERR_TIMEOUT
+    m.sync_status()                                              # the sticky word was cleared
+    w = m.identity_init(dtype=torch.bfloat16)
+    x = wk.normals((128, 128), 3, 1.0, "bf16").cuda()
+    assert torch.equal(m.fprop(x, w), x)
+    m.sync_status()
