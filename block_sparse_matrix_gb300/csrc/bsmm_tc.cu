@@ -29,6 +29,7 @@
 #include "tc_common.cuh"
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -88,6 +89,7 @@ struct UpSched {
 struct TcState {
     std::map<uint64_t, FbSched> fb;   // key: pass, window log2, chunk entries, chunk records
     UpSched up;
+    struct UpDenseSched *upd = nullptr;
     void *d_zero = nullptr;   // zero buffer: 8x8 zero tiles for absent sub-blocks of 16x16 coarse blocks
     std::mutex mu;
 };
@@ -317,6 +319,61 @@ bool build_up(bsmm_ctx *h, UpSched &us)
         int32_t *t = table.data() + (size_t)b * kTableWords;
         t[0] = i + 1;
         std::copy(units[u].begin(), units[u].end(), t + 4 + i * kUnitWords);
+    }
+    us.ctas = nunits ? ctas : 0;
+    if (!upload(&us.d_table, table)) return false;
+    us.built = true;
+    return true;
+}
+
+// Schedule of the dense-tile weight gradient (bs = 32): the 128 x 256 tiles of the dense
+// gradient x^T.dy (4 block rows x 8 block columns) that contain at least one block, dealt
+// round-robin to persistent CTAs.  Table word 0 = number of units; unit u at word
+// 4 + u * kDUnitWords: c0 (first block row), k0 (first block column), count, then count
+// words ((c_sub * 8 + k_sub) << 24) | block id.
+constexpr int kDUnitWords = 36;
+constexpr int kDUnitsPerCta = 48;
+constexpr int kDTableWords = 4 + kDUnitsPerCta * kDUnitWords;
+
+struct UpDenseSched {
+    int ctas = 0;
+    int32_t *d_table = nullptr;
+    bool built = false;
+};
+
+bool build_up_dense(bsmm_ctx *h, UpDenseSched &us)
+{
+    const int Rt = (h->R + 3) / 4, St = (h->S + 7) / 8;
+    std::vector<std::vector<int32_t>> units;
+    for (int tc = 0; tc < Rt; ++tc)
+        for (int tk = 0; tk < St; ++tk) {
+            std::vector<int32_t> u(kDUnitWords, 0);
+            int n = 0;
+            for (int cs = 0; cs < 4; ++cs) {
+                const int c = tc * 4 + cs;
+                if (c >= h->R) break;
+                const int32_t *b = h->h_row_ent.data() + h->h_row_ptr[c];
+                const int32_t *e = h->h_row_ent.data() + h->h_row_ptr[c + 1];
+                for (const int32_t *q = std::lower_bound(b, e, tk * 8); q != e && *q < tk * 8 + 8; ++q) {
+                    const int32_t id = h->h_row_ptr[c] + (int32_t)(q - b);
+                    u[3 + n++] = ((cs * 8 + (*q - tk * 8)) << 24) | id;
+                }
+            }
+            if (!n) continue;
+            u[0] = tc * 4;
+            u[1] = tk * 8;
+            u[2] = n;
+            units.push_back(u);
+        }
+    const int nunits = (int)units.size();
+    int ctas = std::max(1, std::min(nunits, std::max(1, h->sm_count)));
+    ctas = std::max(ctas, (nunits + kDUnitsPerCta - 1) / kDUnitsPerCta);
+    std::vector<int32_t> table((size_t)ctas * kDTableWords, 0);
+    for (int u = 0; u < nunits; ++u) {
+        const int b = u % ctas, i = u / ctas;
+        int32_t *t = table.data() + (size_t)b * kDTableWords;
+        t[0] = i + 1;
+        std::copy(units[u].begin(), units[u].end(), t + 4 + i * kDUnitWords);
     }
     us.ctas = nunits ? ctas : 0;
     if (!upload(&us.d_table, table)) return false;
@@ -865,6 +922,184 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
     if (warp == kProducers) tmem_dealloc(tmem, 64);
 }
 
+// Dense-tile weight gradient, bs = 32.  A unit is a 128 x 256 tile of x^T.dy: block rows
+// c0..c0+3 (M = 128) by block columns k0..k0+7 (N = 256), reduced over the minibatch in
+// stages of 64 rows (4 MMAs of 128 x 256 x 16).  All loads are 128-byte rows: with (N,C)
+// activations two 64-column boxes of x (MN-major A, two 64-row M atoms) and four of dy
+// (MN-major B, four 64-column N atoms); with (C,N) one 128-row box of x (K-major A) and one
+// 256-row box of dy (K-major B).  The epilogue warp for TMEM lane quarter q owns block row
+// c0+q and writes every present block of that row.
+struct UpDenseGeo {
+    static constexpr int TK = 64;
+    static constexpr int A_BYTES = 128 * TK * 2;                     // 16 KB
+    static constexpr int B_BYTES = 256 * TK * 2;                     // 32 KB
+    static constexpr int STAGES = 4;                                 // a multiple of kProducers
+    static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + kDTableWords * 4;
+};
+
+template <int FA, bool BF16>
+__global__ void __launch_bounds__(kUpThreads, 1)
+k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
+{
+    using G = UpDenseGeo;
+    static_assert(G::STAGES % kProducers == 0, "producer warp w must own stages w, w+4, ...");
+    // fa=1: A = x^T MN-major (M atoms of 64 at 8 KB), B = dy MN-major (N atoms of 64 at 8 KB);
+    // fa=0: both K-major, 128-byte rows.
+    constexpr uint32_t A_LBO = FA ? 8192 : 16, B_LBO = FA ? 8192 : 16;
+    constexpr uint32_t KSTEP = FA ? 16 * 128 : 32;
+    constexpr uint32_t IDESC = idesc_f16(128, 256, BF16, FA == 1, FA == 1);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + G::STAGES * G::A_BYTES;
+    int32_t *tab = reinterpret_cast<int32_t *>(sB + G::STAGES * G::B_BYTES);
+    __shared__ __align__(8) uint64_t full[G::STAGES], empty[G::STAGES], acc_full[2], acc_empty[2], tab_full;
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int aborted;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const int chunks = (p.N + G::TK - 1) / G::TK;
+    const int total = chunks * p.G;
+
+    if (threadIdx.x == 0) {
+        aborted = 0;
+        for (int i = 0; i < G::STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        mbar_init(&tab_full, 1);
+        fence_barrier_init();
+    }
+    if (warp == kProducers) tmem_alloc(&tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    const int32_t *gtab = p.table + (size_t)blockIdx.x * kDTableWords;
+    if (warp == 0 && lane == 0) {
+        const int nu = gtab[0];
+        const uint32_t bytes = (uint32_t)(4 + nu * kDUnitWords) * 4u;
+        mbar_arrive_expect_tx(&tab_full, bytes);
+        bulk_load(tab, gtab, bytes, &tab_full, policy_evict_first());
+    }
+    const bool tab_ok = mbar_wait_warp(&tab_full, 0, p.status, 64);
+    const int nunits = tab_ok ? tab[0] : 0;
+
+    if (warp < kProducers) {
+        const uint64_t pol = policy_evict_last();
+        const uint32_t bytes = G::A_BYTES + G::B_BYTES;
+        int it = 0, last = -1;
+        for (int u = 0; u < nunits && !aborted; ++u) {
+            const int32_t *ut = tab + 4 + u * kDUnitWords;
+            const int f_c = ut[0] * 32, f_k = ut[1] * 32;        // first feature of the tile
+            for (int c = 0; c < total; ++c, ++it) {
+                if (it % kProducers != warp) continue;
+                const int t = c / chunks, n0 = (c % chunks) * G::TK;
+                const int s = it % G::STAGES;
+                if (lane == 0) {
+                    if (it >= G::STAGES && !mbar_wait(&empty[s], ((it / G::STAGES) - 1) & 1, p.status)) aborted = 1;
+                    else mbar_arrive_expect_tx(&full[s], bytes);
+                }
+                __syncwarp();
+                if (aborted) break;
+                last = it;
+                uint8_t *a = sA + s * G::A_BYTES;
+                uint8_t *b = sB + s * G::B_BYTES;
+                if (FA) {
+                    if (lane < 2) tma_load_2d(a + lane * 8192, &maps.x[t], &full[s], f_c + lane * 64, n0, pol);
+                    else if (lane < 6)
+                        tma_load_2d(b + (lane - 2) * 8192, &maps.dy[t], &full[s], f_k + (lane - 2) * 64, n0, pol);
+                } else {
+                    if (lane == 0) tma_load_2d(a, &maps.x[t], &full[s], n0, f_c, pol);
+                    else if (lane == 1) tma_load_2d(b, &maps.dy[t], &full[s], n0, f_k, pol);
+                }
+            }
+        }
+        if (aborted && lane == 0 && last >= 0) mbar_wait(&full[last % G::STAGES], (last / G::STAGES) & 1, nullptr);
+        __syncwarp();
+    } else if (warp == kProducers) {
+        if (elect_one()) {
+            const uint64_t a_desc0 = sdesc(smem_u32(sA), A_LBO, 1024, SW_128);
+            const uint64_t b_desc0 = sdesc(smem_u32(sB), B_LBO, 1024, SW_128);
+            int it = 0;
+            for (int u = 0; u < nunits && !aborted; ++u) {
+                const int buf = u & 1;
+                if (u >= 2 && !mbar_wait(&acc_empty[buf], ((u >> 1) - 1) & 1, p.status)) {
+                    aborted = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + buf * 256;
+                for (int c = 0; c < total; ++c, ++it) {
+                    const int s = it % G::STAGES;
+                    if (!mbar_wait(&full[s], (it / G::STAGES) & 1, p.status)) {
+                        aborted = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = a_desc0 + ((s * G::A_BYTES) >> 4);
+                    const uint64_t bd = b_desc0 + ((s * G::B_BYTES) >> 4);
+#pragma unroll
+                    for (int ks = 0; ks < G::TK / 16; ++ks)
+                        mma_ss(d, ad + ((ks * KSTEP) >> 4), bd + ((ks * KSTEP) >> 4), IDESC,
+                               (c > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(&empty[s]);
+                }
+                mma_commit(&acc_full[buf]);
+            }
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;                  // TMEM lane quarter = block row c0 + q
+        for (int u = 0; u < nunits; ++u) {
+            const int buf = u & 1;
+            const bool ok = mbar_wait_warp(&acc_full[buf], (u >> 1) & 1, p.status, 128);
+            if (!ok) break;
+            tc_fence_after();
+            const int32_t *ut = tab + 4 + u * kDUnitWords;
+            const int cnt = ut[2];
+            for (int e = 0; e < cnt; ++e) {
+                const uint32_t wd = (uint32_t)ut[3 + e];
+                const int sub = (int)(wd >> 24), id = (int)(wd & 0xFFFFFFu);
+                if ((sub >> 3) != q) continue;
+                float v[32];
+#pragma unroll
+                for (int c0 = 0; c0 < 32; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + (sub & 7) * 32 + c0, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[c0 + j] = __uint_as_float(r[j]);
+                }
+                if (!aborted) {
+                    float *dst = p.dw + ((size_t)id * 32 + lane) * 32;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                        if (p.accumulate) {
+                            float4 a = *reinterpret_cast<float4 *>(dst + j);
+                            o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
+                        }
+                        *reinterpret_cast<float4 *>(dst + j) = o;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kProducers) tmem_dealloc(tmem, 512);
+}
+
 // ---------------------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------------------
@@ -1000,6 +1235,45 @@ FbStages choose_stages(const bsmm_ctx *h, int N, int64_t units, int W)
     return g;
 }
 
+template <int FA, bool BF16>
+bsmm_status launch_up_dense(bsmm_ctx *h, UpDenseSched &us, const GroupPtrs &g, float *dw, int N, bsmm_dtype t,
+                            int acc, cudaStream_t s)
+{
+    using G = UpDenseGeo;
+    const int C = h->R * 32, K = h->S * 32;
+    UpMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    for (int i = 0; i < g.G; ++i) {
+        bool ok;
+        if (FA) {
+            ok = make_map2d(&maps.x[i], g.x[i], t, C, N, 64, G::TK, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 make_map2d(&maps.dy[i], g.dy[i], t, K, N, 64, G::TK, CU_TENSOR_MAP_SWIZZLE_128B);
+        } else {
+            ok = make_map2d(&maps.x[i], g.x[i], t, N, C, G::TK, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 make_map2d(&maps.dy[i], g.dy[i], t, N, K, G::TK, 256, CU_TENSOR_MAP_SWIZZLE_128B);
+        }
+        if (!ok) return BSMM_ERR_CUDA;
+    }
+    UpParams p;
+    p.dw = dw;
+    p.table = us.d_table;
+    p.status = h->d_status;
+    p.N = N;
+    p.G = g.G;
+    p.accumulate = acc;
+    const int smem = G::SMEM + 1024;
+    auto kern = k_tc_updat_dense<FA, BF16>;
+    static std::atomic<int> attr_set{-1};
+    if (attr_set.load() != h->device) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return BSMM_ERR_CUDA;
+        attr_set.store(h->device);
+    }
+    kern<<<us.ctas, kUpThreads, smem, s>>>(maps, p);
+    g_bsmm_launches += 1;
+    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+}
+
 template <bool BWD>
 bsmm_status fb_dispatch(bsmm_ctx *h, const void *act, const void *w, void *out, int N, bsmm_dtype t, cudaStream_t s)
 {
@@ -1095,12 +1369,32 @@ bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dty
                      cudaStream_t s)
 {
     TcState *st = state(h);
+    const bool bf = t == BSMM_BF16;
+    // Dense 128 x 256 tiles when bs = 32, at least a quarter of the layout is present and
+    // the minibatch spans two or more 64-row stages (BSMM_TC_UPDAT=stack / dense overrides).
+    const double density = (double)h->nnz / ((double)h->R * h->S);
+    bool dense = h->bs == 32 && density >= 0.25 && N * g.G > 64 && h->nnz < (1 << 24);
+    if (const char *e = getenv("BSMM_TC_UPDAT")) {
+        if (!strcmp(e, "stack")) dense = false;
+        if (!strcmp(e, "dense")) dense = h->bs == 32 && h->nnz < (1 << 24);
+    }
+    if (dense) {
+        {
+            std::lock_guard<std::mutex> lk(st->mu);
+            if (!st->upd) st->upd = new UpDenseSched();
+            if (!st->upd->built && !build_up_dense(h, *st->upd)) return BSMM_ERR_OOM;
+        }
+        if (st->upd->ctas == 0) return BSMM_OK;
+        if (h->fa) return bf ? launch_up_dense<1, true>(h, *st->upd, g, dw, N, t, accumulate, s)
+                             : launch_up_dense<1, false>(h, *st->upd, g, dw, N, t, accumulate, s);
+        return bf ? launch_up_dense<0, true>(h, *st->upd, g, dw, N, t, accumulate, s)
+                  : launch_up_dense<0, false>(h, *st->upd, g, dw, N, t, accumulate, s);
+    }
     {
         std::lock_guard<std::mutex> lk(st->mu);
         if (!st->up.built && !build_up(h, st->up)) return BSMM_ERR_OOM;
     }
     if (st->up.ctas == 0) return BSMM_OK;
-    const bool bf = t == BSMM_BF16;
 #define UP_CASE(BS_, FA_)                                                                         \
     if (h->bs == BS_ && h->fa == FA_)                                                             \
         return bf ? launch_up<BS_, FA_, true>(h, st->up, g, dw, N, t, accumulate, s)             \
@@ -1128,6 +1422,10 @@ void tc_release(bsmm_ctx *h)
         cudaFree(f.d_win_mask);
     }
     cudaFree(st->up.d_table);
+    if (st->upd) {
+        cudaFree(st->upd->d_table);
+        delete st->upd;
+    }
     cudaFree(st->d_zero);
     delete st;
     h->tc = nullptr;

@@ -323,3 +323,29 @@ def test_bounded_wait_times_out_and_context_survives():
     x = wk.normals((128, 128), 3, 1.0, "bf16").cuda()
     assert torch.equal(m.fprop(x, w), x)
     m.sync_status()
+
+
+@pytest.mark.parametrize("variant", ["stack", "dense"])
+@pytest.mark.parametrize("fa", [0, 1])
+@pytest.mark.parametrize("p,G", [(0.5, 1), (0.2, 3), (0.9, 8)])
+def test_updat_variants_bs32(monkeypatch, variant, fa, p, G):
+    """Both tensor-core weight-gradient schemes (blocks of a column stacked along M, or dense
+    128x256 tiles of x^T.dy with the present blocks extracted) against the oracle, on
+    ragged layouts (R, S not multiples of the tile) and a ragged minibatch."""
+    monkeypatch.setenv("BSMM_TC_UPDAT", variant)
+    bs, R, S, N = 32, 10, 13, 136
+    L = rand_layout(R, S, p, 17 + G)
+    m = make(L, bs, fa, "auto")
+    xs = [wk.normals(wk.act_shape(R * bs, N, fa), 500 + t, 1.0, "bf16") for t in range(G)]
+    dys = [wk.normals(wk.act_shape(S * bs, N, fa), 600 + t, 1.0, "bf16") for t in range(G)]
+    ref = o.updat_grouped(L, bs, xs, dys, fa)
+    dw = m.updat_grouped([a.cuda() for a in xs], [a.cuda() for a in dys])
+    m.sync_status()
+    assert rel_fro(cpu64(dw), ref) <= TOL_DW["bf16"]
+    m.updat_grouped([a.cuda() for a in xs], [a.cuda() for a in dys], dw=dw, accumulate=True)
+    m.sync_status()
+    assert rel_fro(cpu64(dw), 2 * ref) <= TOL_DW["bf16"]
+    if G == 1:
+        dw1 = m.updat(xs[0].cuda(), dys[0].cuda())
+        m.sync_status()
+        assert rel_fro(cpu64(dw1), o.updat(L, bs, xs[0], dys[0], fa)) <= TOL_DW["bf16"]
