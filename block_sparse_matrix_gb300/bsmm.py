@@ -58,6 +58,7 @@ def lib():
             "bsmm_set_kernel": [vp, i],
             "bsmm_sync_status": [vp, vp],
             "bsmm_selftest_wait_timeout": [vp, ctypes.c_uint64, vp],
+            "bsmm_updat_noalloc": [vp, vp, vp, vp, i, i, i, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -145,6 +146,13 @@ def bsmm_updat_grouped(h, xs, dys, dw, N: int, accumulate: bool = False, stream=
     dt = _DT[xs[0].dtype] if G else F32
     _check(lib().bsmm_updat_grouped(h, xa, da, G, N, dt, _ptr(dw), int(accumulate), _stream(stream)),
            "bsmm_updat_grouped")
+
+
+def bsmm_updat_noalloc(h, x, dy, dw, N: int, accumulate: bool = False, stream=None):
+    """Weight gradient that allocates no device memory (see include/bsmm.h): for callers
+    whose allocator or memory budget forbids cudaMalloc.  dw must be float32."""
+    _check(lib().bsmm_updat_noalloc(h, _ptr(x), _ptr(dy), _ptr(dw), N, _DT[x.dtype], int(accumulate),
+                                    _stream(stream)), "bsmm_updat_noalloc")
 
 
 def bsmm_sync_status(h, stream=None):

@@ -1430,3 +1430,143 @@ void tc_release(bsmm_ctx *h)
     delete st;
     h->tc = nullptr;
 }
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free weight gradient
+// ---------------------------------------------------------------------------------------
+// Some callers cannot call cudaMalloc: code that runs under a framework's memory budget or
+// caching allocator (where a raw driver allocation would bypass it, fragment it or fail at
+// the memory limit), and latency-critical loops where an allocation's cost or failure is
+// not acceptable.  bsmm_updat_noalloc serves them: it runs the stacked weight-gradient
+// kernel with its unit table in the fixed device array below instead of a table the
+// handle would allocate.  The array is a module global: every GPU that loads this library
+// holds its 4 MB until the process exits.
+
+namespace {
+
+constexpr int kNoAllocTableWords = 1 << 20;          // 4 MB: at most this many table words
+__device__ __align__(256) int32_t g_noalloc_table[kNoAllocTableWords];
+
+int32_t g_noalloc_host[kNoAllocTableWords];          // host staging copy (static, not allocated)
+std::mutex g_noalloc_mu;
+int32_t *g_noalloc_dev_ptr[64] = {nullptr};          // device address of the array, per device
+
+// Builds the stacked-updat unit tables into g_noalloc_host (same layout as build_up).
+// Returns the number of CTAs, 0 for an empty layout, or -1 if the tables do not fit.
+int noalloc_build(const bsmm_ctx *h)
+{
+    const bool coarse = h->bs == 8;
+    const int f = coarse ? 2 : 1;
+    const int Rc = (h->R + f - 1) / f, Sc = (h->S + f - 1) / f;
+    const int MS = coarse ? 8 : 128 / h->bs;
+    BidLookup bid{h};
+    // count units first
+    int64_t nunits = 0;
+    for (int kc = 0; kc < Sc; ++kc) {
+        int n = 0;
+        for (int cc = 0; cc < Rc; ++cc) {
+            bool any = false;
+            for (int cs = 0; cs < f; ++cs)
+                for (int ks = 0; ks < f; ++ks) any |= bid(cc * f + cs, kc * f + ks) >= 0;
+            n += any;
+        }
+        nunits += (n + MS - 1) / MS;
+    }
+    if (nunits == 0) return 0;
+    int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(nunits, 2 * std::max(1, h->sm_count)));
+    ctas = std::max<int64_t>(ctas, (nunits + kUnitsPerCta - 1) / kUnitsPerCta);
+    if (ctas * kTableWords > kNoAllocTableWords) return -1;
+    std::fill(g_noalloc_host, g_noalloc_host + ctas * kTableWords, 0);
+    int64_t u = 0;
+    for (int kc = 0; kc < Sc; ++kc) {
+        int32_t *cur = nullptr;
+        int m = 0;
+        for (int cc = 0; cc < Rc; ++cc) {
+            int32_t ids[4];
+            bool any = false;
+            for (int cs = 0; cs < f; ++cs)
+                for (int ks = 0; ks < f; ++ks) {
+                    ids[cs * 2 + ks] = bid(cc * f + cs, kc * f + ks);
+                    any |= ids[cs * 2 + ks] >= 0;
+                }
+            if (!any) continue;
+            if (!cur || m == MS) {                    // start a new unit in CTA u % ctas
+                int32_t *t = g_noalloc_host + (u % ctas) * kTableWords;
+                const int i = (int)(u / ctas);
+                t[0] = i + 1;
+                cur = t + 4 + i * kUnitWords;
+                cur[0] = kc;
+                m = 0;
+                ++u;
+            }
+            int32_t *r = cur + 2 + 5 * m;
+            r[0] = cc;
+            for (int q = 0; q < 4; ++q) r[1 + q] = ids[q];
+            cur[1] = ++m;
+        }
+    }
+    return (int)ctas;
+}
+
+} // namespace
+
+extern "C" bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *dy, float *dw, int N, bsmm_dtype t,
+                                          int accumulate, void *stream)
+{
+    if (!h || N < 0) return BSMM_ERR_INVALID;
+    if (t != BSMM_F16 && t != BSMM_BF16) return BSMM_ERR_UNSUPPORTED;
+    if (h->fa == 0 && ((int64_t)N * 2) % 16 != 0) return BSMM_ERR_ALIGN;
+    if (h->nnz == 0) return BSMM_OK;
+    if (!x || !dy || !dw) return BSMM_ERR_INVALID;
+    if (((uintptr_t)x | (uintptr_t)dy | (uintptr_t)dw) & 15u) return BSMM_ERR_ALIGN;
+    if (h->device < 0 || h->device >= 64) return BSMM_ERR_UNSUPPORTED;
+    if (cudaSetDevice(h->device) != cudaSuccess) return BSMM_ERR_CUDA;
+    if (!tc_supported(h, t)) return BSMM_ERR_UNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_dev_ptr[h->device]) {
+        // One-time set-up on this device: the array's device address (a host-side symbol
+        // is not a device pointer).
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_table) != cudaSuccess || !ptr) return BSMM_ERR_CUDA;
+        g_noalloc_dev_ptr[h->device] = static_cast<int32_t *>(ptr);
+    }
+    int32_t *table = g_noalloc_dev_ptr[h->device];
+    if (N == 0) {
+        if (accumulate) return BSMM_OK;
+        return cudaMemsetAsync(dw, 0, (size_t)h->nnz * h->bs * h->bs * sizeof(float), s) == cudaSuccess
+                   ? BSMM_OK
+                   : BSMM_ERR_CUDA;
+    }
+    const int ctas = noalloc_build(h);
+    if (ctas < 0) return BSMM_ERR_UNSUPPORTED;       // layout needs more than the fixed 4 MB table
+    if (ctas == 0) return BSMM_OK;
+    // Pageable copy: returns once the host buffer has been staged, ordered before the kernel.
+    if (cudaMemcpyAsync(table, g_noalloc_host, (size_t)ctas * kTableWords * sizeof(int32_t), cudaMemcpyHostToDevice,
+                        s) != cudaSuccess)
+        return BSMM_ERR_CUDA;
+    UpSched us;
+    us.ctas = ctas;
+    us.d_table = table;
+    us.built = true;
+    GroupPtrs g{};
+    g.x[0] = x;
+    g.dy[0] = dy;
+    g.G = 1;
+    const bool bf = t == BSMM_BF16;
+    const int acc = accumulate ? 1 : 0;
+    bsmm_status st = BSMM_ERR_UNSUPPORTED;
+#define NA_CASE(BS_, FA_)                                                                      \
+    if (h->bs == BS_ && h->fa == FA_)                                                          \
+        st = bf ? launch_up<BS_, FA_, true>(h, us, g, dw, N, t, acc, s)                        \
+                : launch_up<BS_, FA_, false>(h, us, g, dw, N, t, acc, s);
+    NA_CASE(32, 1)
+    NA_CASE(32, 0)
+    NA_CASE(16, 1)
+    NA_CASE(16, 0)
+    NA_CASE(8, 1)
+    NA_CASE(8, 0)
+#undef NA_CASE
+    us.d_table = nullptr;                            // the array is not the handle's to free
+    return st;
+}

@@ -142,6 +142,31 @@ bsmm_status bsmm_updat(bsmm_t h, const void *x, const void *dy, void *dw, int N,
 bsmm_status bsmm_updat_grouped(bsmm_t h, const void *const *xs, const void *const *dys, int G,
                                int N, bsmm_dtype t, float *dw, int accumulate, void *stream);
 
+/*
+ * Allocation-free weight gradient.  The paper has no counterpart: this entry point exists
+ * for callers that must not allocate device memory -- code running under a framework's
+ * memory budget or caching allocator, where a raw cudaMalloc would bypass, fragment or
+ * exhaust it, and latency-critical loops that cannot afford an allocation or its failure.
+ * bsmm_updat allocates its work tables on first use; this call never allocates: it uses a
+ * fixed 4 MB device array that the library holds on every GPU that loads it, until the
+ * process exits.
+ *
+ * Computes the same as bsmm_updat with dw_t = BSMM_F32 for 16-bit x and dy (t = BSMM_F16
+ * or BSMM_BF16), using the stacked-block tensor-core kernel.  x, dy, dw are DEVICE
+ * pointers as in bsmm_updat; accumulate = 0 sets dw, 1 adds to it.
+ * - The first call on a device looks up the array's device address; make that first call
+ *   before any stream capture.
+ * - The array is shared by every call and keeps the last call's contents.  Each call
+ *   rewrites the part it uses (copied from the host, ordered on `stream` before the
+ *   kernel), so calls on one stream are safe in sequence, but calls that overlap on the
+ *   GPU (other streams, other threads) race on the array and must not be issued.
+ * - Errors: INVALID (null handle or pointers, N < 0), ALIGN, UNSUPPORTED (fp32 inputs, or a
+ *   layout whose work tables need more than the 4 MB array: about 23,000 stacks of
+ *   128/bs blocks, e.g. ~95,000 blocks at bs 32), CUDA.
+ */
+bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *dy, float *dw, int N, bsmm_dtype t,
+                               int accumulate, void *stream);
+
 /* Kernel family for later calls on this handle (testing / comparison). */
 bsmm_status bsmm_set_kernel(bsmm_t h, bsmm_kernel which);
 
