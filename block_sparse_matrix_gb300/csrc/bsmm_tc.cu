@@ -90,6 +90,7 @@ struct TcState {
     std::map<uint64_t, FbSched> fb;   // key: pass, window log2, chunk entries, chunk records
     UpSched up;
     struct UpDenseSched *upd = nullptr;
+    struct FbDenseSched *fbd[2] = {nullptr, nullptr};   // dense-tile fprop / bprop
     void *d_zero = nullptr;   // zero buffer: 8x8 zero tiles for absent sub-blocks of 16x16 coarse blocks
     std::mutex mu;
 };
@@ -378,6 +379,58 @@ bool build_up_dense(bsmm_ctx *h, UpDenseSched &us)
     us.ctas = nunits ? ctas : 0;
     if (!upload(&us.d_table, table)) return false;
     us.built = true;
+    return true;
+}
+
+// Schedule of the dense-tile fprop/bprop (bs = 32): for each group of 4 output blocks
+// (fprop: block columns, bprop: block rows), the pairs of adjacent source blocks with at
+// least one block among the group's outputs.  Per group a word stream:
+//   entry: ((pair << 8) | mask), then 8 words id + 1 (0 = absent) in (sub, out) order,
+//          mask bit sub*4 + out set when block (source 2*pair+sub, output out) is present
+//   0xFFFFFFFF ends the stream; streams are padded to 4 words.
+constexpr int kFbdSchedWords = 3072;
+
+struct FbDenseSched {
+    int ngroups = 0;
+    uint32_t *d_stream = nullptr;
+    int32_t *d_off = nullptr, *d_len = nullptr;
+    bool built = false, too_big = false;
+};
+
+bool build_fb_dense(bsmm_ctx *h, FbDenseSched &fs, bool bwd)
+{
+    const int Fout = bwd ? h->R : h->S, Fsrc = bwd ? h->S : h->R;
+    const int ng = (Fout + 3) / 4;
+    BidLookup bid{h};
+    std::vector<uint32_t> stream;
+    std::vector<int32_t> off(ng), len(ng);
+    for (int gi = 0; gi < ng; ++gi) {
+        off[gi] = (int32_t)stream.size();
+        for (int pr = 0; pr * 2 < Fsrc; ++pr) {
+            uint32_t mask = 0, ids[8];
+            for (int sub = 0; sub < 2; ++sub)
+                for (int o = 0; o < 4; ++o) {
+                    const int src = pr * 2 + sub, out = gi * 4 + o;
+                    int32_t b = -1;
+                    if (src < Fsrc && out < Fout) b = bwd ? bid(out, src) : bid(src, out);
+                    ids[sub * 4 + o] = (uint32_t)(b + 1);
+                    if (b >= 0) mask |= 1u << (sub * 4 + o);
+                }
+            if (!mask) continue;
+            stream.push_back(((uint32_t)pr << 8) | mask);
+            stream.insert(stream.end(), ids, ids + 8);
+        }
+        stream.push_back(0xFFFFFFFFu);
+        while (stream.size() % 4) stream.push_back(0);
+        len[gi] = (int32_t)(stream.size() - off[gi]);
+        if (len[gi] > kFbdSchedWords) {
+            fs.too_big = true;
+            return true;
+        }
+    }
+    fs.ngroups = ng;
+    if (!upload(&fs.d_stream, stream) || !upload(&fs.d_off, off) || !upload(&fs.d_len, len)) return false;
+    fs.built = true;
     return true;
 }
 
@@ -1100,6 +1153,199 @@ k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
     if (warp == kProducers) tmem_dealloc(tmem, 512);
 }
 
+// Dense-tile fprop / bprop, bs = 32.  A CTA computes D[128 output features][256 minibatch
+// rows] for a group of 4 output blocks: D += A[128 x 32] . B[32 x 256] for each present
+// source block, A being the group's 4 weight blocks of that source (absent ones are zero
+// tiles) and B the activation panel.  Sources are loaded in adjacent pairs so activation
+// rows are 128 bytes.  Every MMA is M128 x N256 x K16.
+//   fprop: A[(out, j)][i] = w(src, out)[i][j]  -> MN-major, 4 SW64 blocks 2 KB apart
+//   bprop: A[(out, i)][j] = w(out, src)[i][j]  -> K-major, 128 rows of 64 bytes
+//   (N,C) activations: B rows = minibatch rows of 128 bytes (K-major, SW128)
+//   (C,N) activations: B = four 64-column MN-major SW128 atoms, 8 KB apart
+struct FbdParams {
+    void *out;
+    const uint32_t *stream;
+    const int32_t *off, *len;
+    int32_t *status;
+    int N, Fout, n_tiles;
+};
+
+template <int FA, bool BWD, bool BF16>
+__global__ void __launch_bounds__(kFbThreads, 1)
+k_tc_fbd(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
+         const __grid_constant__ CUtensorMap tm_zero, const FbdParams p)
+{
+    constexpr int STAGES = 4;                                    // = kProducers: warp w owns stage w
+    static_assert(STAGES % kProducers == 0, "producer warp w must own stages w, w+4, ...");
+    constexpr int A_BYTES = 16384, B_BYTES = 32768, STAGE = A_BYTES + B_BYTES;
+    constexpr uint32_t A_LBO = BWD ? 16 : 2048, A_SBO = 512, A_KSTEP = BWD ? 32 : 1024;
+    constexpr uint32_t B_LBO = FA ? 16 : 8192, B_KSTEP = FA ? 32 : 2048, B_SUB = FA ? 64 : 4096;
+    constexpr uint32_t IDESC = idesc_f16(128, 256, BF16, !BWD, FA == 0);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t *sched = reinterpret_cast<const uint32_t *>(smem + STAGES * STAGE);
+    __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full, sched_full;
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int aborted;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const int grp = blockIdx.x / p.n_tiles;
+    const int n0 = (blockIdx.x % p.n_tiles) * 256;
+    const int len = p.len[grp];
+
+    if (threadIdx.x == 0) {
+        aborted = 0;
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(&acc_full, 1);
+        mbar_init(&sched_full, 1);
+        fence_barrier_init();
+    }
+    if (warp == kProducers) tmem_alloc(&tmem_base, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    if (warp < kProducers) {
+        const uint64_t pol_act = policy_evict_last();
+        const uint64_t pol_w = policy_evict_first();
+        if (warp == 0 && lane == 0) {
+            mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
+            bulk_load((void *)sched, p.stream + p.off[grp], (uint32_t)len * 4u, &sched_full, pol_act);
+            prefetch_tmap(&tm_act);
+            prefetch_tmap(&tm_w);
+        }
+        if (!mbar_wait_warp(&sched_full, 0, p.status, 64)) aborted = 1;
+        __syncwarp();
+        int last = -1;
+        for (int chunk = 0, pos = 0; !aborted; ++chunk, pos += 9) {
+            const uint32_t hdr = sched[pos];
+            if (hdr == 0xFFFFFFFFu) break;
+            if (chunk % kProducers != warp) continue;
+            const int st = chunk % STAGES;
+            if (lane == 0) {
+                if (chunk >= STAGES && !mbar_wait(&empty[st], ((chunk / STAGES) - 1) & 1, p.status)) aborted = 1;
+                else mbar_arrive_expect_tx(&full[st], (uint32_t)STAGE);
+            }
+            __syncwarp();
+            if (aborted) break;
+            last = chunk;
+            const int pr = (int)(hdr >> 8);
+            uint8_t *a = smem + st * STAGE;
+            uint8_t *b = a + A_BYTES;
+            if (FA) {
+                if (lane == 0) tma_load_2d(b, &tm_act, &full[st], pr * 64, n0, pol_act);
+            } else {
+                if (lane < 4) tma_load_2d(b + lane * 8192, &tm_act, &full[st], n0 + 64 * lane, pr * 64, pol_act);
+            }
+            if (lane >= 8 && lane < 16) {
+                const int sl = lane - 8;                        // sub * 4 + out
+                const int id = (int)sched[pos + 1 + sl] - 1;
+                uint8_t *d = a + (sl >> 2) * 8192 + (sl & 3) * 2048;
+                if (id >= 0) {
+                    tma_load_2d(d, &tm_w, &full[st], 0, id * 32, pol_w);
+                } else {
+                    const int zr = (int)((blockIdx.x * 13u + (unsigned)chunk * 8u + (unsigned)sl) % 128u) * 32;
+                    tma_load_2d(d, &tm_zero, &full[st], 0, zr, pol_w);
+                }
+            }
+        }
+        if (aborted && lane == 0 && last >= 0) mbar_wait(&full[last % STAGES], (last / STAGES) & 1, nullptr);
+        __syncwarp();
+    } else {
+        if (elect_one()) {
+            const uint32_t s_base = smem_u32(smem);
+            const uint64_t a_desc0 = sdesc(s_base, A_LBO, A_SBO, SW_64);
+            const uint64_t b_desc0 = sdesc(s_base + A_BYTES, B_LBO, 1024, SW_128);
+            uint32_t acc = 0;
+            if (!mbar_wait(&sched_full, 0, p.status)) aborted = 1;
+            for (int chunk = 0, pos = 0; !aborted; ++chunk, pos += 9) {
+                const uint32_t hdr = sched[pos];
+                if (hdr == 0xFFFFFFFFu) break;
+                const int st = chunk % STAGES;
+                if (!mbar_wait(&full[st], (chunk / STAGES) & 1, p.status)) {
+                    aborted = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t so = st * STAGE;
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub) {
+                    if (!((hdr >> (sub * 4)) & 0xFu)) continue;     // no block of this source in the group
+                    const uint64_t ad = a_desc0 + ((so + sub * 8192) >> 4);
+                    const uint64_t bd = b_desc0 + ((so + sub * B_SUB) >> 4);
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        mma_ss(tmem, ad + ((ks * A_KSTEP) >> 4), bd + ((ks * B_KSTEP) >> 4), IDESC, acc);
+                        acc = 1;
+                    }
+                }
+                mma_commit(&empty[st]);
+            }
+            mma_commit(&acc_full);
+        }
+        __syncwarp();
+    }
+    if (warp < kProducers) {
+        // epilogue: warp q holds output features 32q..32q+31 of the group, lane = feature
+        const int q = warp & 3;
+        const int f = grp * 128 + q * 32 + lane;
+        const bool ok = mbar_wait_warp(&acc_full, 0, p.status, 256);
+        tc_fence_after();
+        const bool any = len > 4;                     // at least one entry (else the stream is the end marker)
+        uint16_t *out = static_cast<uint16_t *>(p.out);
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+            if (n0 + c0 >= p.N) break;
+            float v[32];
+            if (ok && any) {
+#pragma unroll
+                for (int h2 = 0; h2 < 32; h2 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0 + h2, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[h2 + j] = __uint_as_float(r[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            if (f >= p.Fout) continue;
+            const int nb = n0 + c0;
+            if (FA) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (nb + j < p.N) out[(size_t)(nb + j) * p.Fout + f] = cvt1<BF16>(v[j]);
+            } else {
+                uint16_t *dst = out + (size_t)f * p.N + nb;
+                if (nb + 32 <= p.N) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 pk;
+                        pk.x = pack2<BF16>(v[j], v[j + 1]);
+                        pk.y = pack2<BF16>(v[j + 2], v[j + 3]);
+                        pk.z = pack2<BF16>(v[j + 4], v[j + 5]);
+                        pk.w = pack2<BF16>(v[j + 6], v[j + 7]);
+                        *reinterpret_cast<uint4 *>(dst + j) = pk;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (nb + j < p.N) dst[j] = cvt1<BF16>(v[j]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kProducers) tmem_dealloc(tmem, 256);
+}
+
 // ---------------------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------------------
@@ -1274,6 +1520,76 @@ bsmm_status launch_up_dense(bsmm_ctx *h, UpDenseSched &us, const GroupPtrs &g, f
     return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
+template <int FA, bool BWD, bool BF16>
+bsmm_status launch_fbd(bsmm_ctx *h, FbDenseSched &fs, const void *act, const void *w, void *out, int N,
+                       bsmm_dtype t, cudaStream_t s)
+{
+    TcState *st = state(h);
+    const int C = h->R * 32, K = h->S * 32;
+    const int Fin = BWD ? K : C, Fout = BWD ? C : K;
+    CUtensorMap m_act, m_w, m_zero;
+    bool ok;
+    if (FA) ok = make_map2d(&m_act, act, t, Fin, N, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B);
+    else ok = make_map2d(&m_act, act, t, N, Fin, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map2d(&m_w, w, t, 32, (uint64_t)h->nnz * 32, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok = ok && make_map2d(&m_zero, st->d_zero, t, 32, kZeroBytes / 64, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!ok) return BSMM_ERR_CUDA;
+    FbdParams p;
+    p.out = out;
+    p.stream = fs.d_stream;
+    p.off = fs.d_off;
+    p.len = fs.d_len;
+    p.status = h->d_status;
+    p.N = N;
+    p.Fout = Fout;
+    p.n_tiles = (N + 255) / 256;
+    const int smem = 4 * (16384 + 32768) + kFbdSchedWords * 4 + 1024;
+    auto kern = k_tc_fbd<FA, BWD, BF16>;
+    static std::atomic<int> attr_set{-1};
+    if (attr_set.load() != h->device) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return BSMM_ERR_CUDA;
+        attr_set.store(h->device);
+    }
+    kern<<<fs.ngroups * p.n_tiles, kFbThreads, smem, s>>>(m_act, m_w, m_zero, p);
+    g_bsmm_launches += 1;
+    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+}
+
+// Dense tiles for bs = 32 layouts with at least a quarter of the blocks present and a
+// minibatch of more than 128 rows (BSMM_TC_FB=dense / window overrides).  Returns
+// BSMM_ERR_UNSUPPORTED when the window kernel should run instead.
+template <bool BWD>
+bsmm_status fbd_try(bsmm_ctx *h, const void *act, const void *w, void *out, int N, bsmm_dtype t, cudaStream_t s)
+{
+    if (h->bs != 32 || h->nnz == 0) return BSMM_ERR_UNSUPPORTED;
+    const double density = (double)h->nnz / ((double)h->R * h->S);
+    bool dense = density >= 0.25 && N > 128;
+    if (const char *e = getenv("BSMM_TC_FB")) {
+        if (!strcmp(e, "window")) dense = false;
+        if (!strcmp(e, "dense")) dense = true;
+    }
+    if (!dense) return BSMM_ERR_UNSUPPORTED;
+    TcState *st = state(h);
+    FbDenseSched *fs;
+    {
+        std::lock_guard<std::mutex> lk(st->mu);
+        if (!st->d_zero) {
+            if (cudaMalloc(&st->d_zero, kZeroBytes) != cudaSuccess) return BSMM_ERR_OOM;
+            if (cudaMemset(st->d_zero, 0, kZeroBytes) != cudaSuccess) return BSMM_ERR_CUDA;
+        }
+        if (!st->fbd[BWD]) st->fbd[BWD] = new FbDenseSched();
+        fs = st->fbd[BWD];
+        if (!fs->built && !fs->too_big && !build_fb_dense(h, *fs, BWD)) return BSMM_ERR_OOM;
+    }
+    if (!fs->built) return BSMM_ERR_UNSUPPORTED;
+    const bool bf = t == BSMM_BF16;
+    if (h->fa) return bf ? launch_fbd<1, BWD, true>(h, *fs, act, w, out, N, t, s)
+                         : launch_fbd<1, BWD, false>(h, *fs, act, w, out, N, t, s);
+    return bf ? launch_fbd<0, BWD, true>(h, *fs, act, w, out, N, t, s)
+              : launch_fbd<0, BWD, false>(h, *fs, act, w, out, N, t, s);
+}
+
 template <bool BWD>
 bsmm_status fb_dispatch(bsmm_ctx *h, const void *act, const void *w, void *out, int N, bsmm_dtype t, cudaStream_t s)
 {
@@ -1357,11 +1673,15 @@ bool tc_supported(bsmm_ctx *h, bsmm_dtype t)
 
 bsmm_status tc_fprop(bsmm_ctx *h, const void *x, const void *w, void *y, int N, bsmm_dtype t, cudaStream_t s)
 {
+    const bsmm_status st = fbd_try<false>(h, x, w, y, N, t, s);
+    if (st != BSMM_ERR_UNSUPPORTED) return st;
     return fb_dispatch<false>(h, x, w, y, N, t, s);
 }
 
 bsmm_status tc_bprop(bsmm_ctx *h, const void *dy, const void *w, void *dx, int N, bsmm_dtype t, cudaStream_t s)
 {
+    const bsmm_status st = fbd_try<true>(h, dy, w, dx, N, t, s);
+    if (st != BSMM_ERR_UNSUPPORTED) return st;
     return fb_dispatch<true>(h, dy, w, dx, N, t, s);
 }
 
@@ -1426,6 +1746,13 @@ void tc_release(bsmm_ctx *h)
         cudaFree(st->upd->d_table);
         delete st->upd;
     }
+    for (auto *f : st->fbd)
+        if (f) {
+            cudaFree(f->d_stream);
+            cudaFree(f->d_off);
+            cudaFree(f->d_len);
+            delete f;
+        }
     cudaFree(st->d_zero);
     delete st;
     h->tc = nullptr;

@@ -349,3 +349,35 @@ def test_updat_variants_bs32(monkeypatch, variant, fa, p, G):
         dw1 = m.updat(xs[0].cuda(), dys[0].cuda())
         m.sync_status()
         assert rel_fro(cpu64(dw1), o.updat(L, bs, xs[0], dys[0], fa)) <= TOL_DW["bf16"]
+
+
+@pytest.mark.parametrize("fa,dtype", [(1, "bf16"), (0, "f16")])
+@pytest.mark.parametrize("R,S,p,N", [(10, 13, 0.5, 392), (7, 9, 0.9, 264), (12, 6, 0.3, 136)])
+def test_fprop_bprop_variants_bs32(monkeypatch, fa, dtype, R, S, p, N):
+    """Both tensor-core fprop/bprop schemes (windows of output blocks over 128-row tiles,
+    or dense 4-block x 256-row tiles with absent blocks as zero tiles) against the oracle,
+    on layouts whose block counts are not multiples of the tile and a ragged minibatch."""
+    bs = 32
+    L = rand_layout(R, S, p, R * 31 + S)
+    L[:, 2] = 0                                           # an empty output block column
+    L[1, :] = 0                                           # an empty input block row
+    nnz = int(L.sum())
+    x = wk.normals(wk.act_shape(R * bs, N, fa), 700 + R, 1.0, dtype)
+    dy = wk.normals(wk.act_shape(S * bs, N, fa), 800 + S, 1.0, dtype)
+    w = wk.normals((nnz, bs, bs), 900 + R + S, float(1 / np.sqrt(R * bs * p)), dtype)
+    ref_y, ref_dx = o.fprop(L, bs, x, w, fa), o.bprop(L, bs, dy, w, fa)
+    outs = {}
+    for variant in ("window", "dense"):
+        monkeypatch.setenv("BSMM_TC_FB", variant)
+        m = make(L, bs, fa, "auto")
+        y = torch.full(m.o_shape(N), float("nan"), dtype=DT[dtype], device="cuda")
+        dx = torch.full(m.i_shape(N), float("nan"), dtype=DT[dtype], device="cuda")
+        m.fprop(x.cuda(), w.cuda(), y)
+        m.bprop(dy.cuda(), w.cuda(), dx)
+        m.sync_status()
+        assert rel_fro(cpu64(y), ref_y) <= TIGHT[dtype]
+        assert rel_fro(cpu64(dx), ref_dx) <= TIGHT[dtype]
+        outs[variant] = (cpu64(y), cpu64(dx))
+    # both schemes accumulate in fp32 and round once: they agree to a few output ulps
+    for a, b in zip(outs["window"], outs["dense"]):
+        assert rel_fro(a, b) <= TIGHT[dtype]
