@@ -1173,7 +1173,7 @@ struct FbdParams {
 template <int FA, bool BWD, bool BF16>
 __global__ void __launch_bounds__(kFbThreads, 1)
 k_tc_fbd(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
-         const __grid_constant__ CUtensorMap tm_zero, const FbdParams p)
+         const __grid_constant__ CUtensorMap tm_zero, const __grid_constant__ CUtensorMap tm_out, const FbdParams p)
 {
     constexpr int STAGES = 4;                                    // = kProducers: warp w owns stage w
     static_assert(STAGES % kProducers == 0, "producer warp w must own stages w, w+4, ...");
@@ -1299,8 +1299,11 @@ k_tc_fbd(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUt
         tc_fence_after();
         const bool any = len > 4;                     // at least one entry (else the stream is the end marker)
         uint16_t *out = static_cast<uint16_t *>(p.out);
+        // (N,C) outputs: the bf16 tile is staged as [256 minibatch rows][128 features] in the
+        // idle stage memory and written by one TMA store; (C,N) outputs are row-contiguous.
+        uint16_t *tile = reinterpret_cast<uint16_t *>(smem);
         for (int c0 = 0; c0 < 256; c0 += 32) {
-            if (n0 + c0 >= p.N) break;
+            if (!FA && n0 + c0 >= p.N) break;
             float v[32];
             if (ok && any) {
 #pragma unroll
@@ -1315,35 +1318,259 @@ k_tc_fbd(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUt
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;
             }
-            if (f >= p.Fout) continue;
-            const int nb = n0 + c0;
             if (FA) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (nb + j < p.N) out[(size_t)(nb + j) * p.Fout + f] = cvt1<BF16>(v[j]);
-            } else {
-                uint16_t *dst = out + (size_t)f * p.N + nb;
-                if (nb + 32 <= p.N) {
+                for (int j = 0; j < 32; ++j) tile[(c0 + j) * 128 + q * 32 + lane] = cvt1<BF16>(v[j]);
+                continue;
+            }
+            if (f >= p.Fout) continue;
+            const int nb = n0 + c0;
+            uint16_t *dst = out + (size_t)f * p.N + nb;
+            if (nb + 32 <= p.N) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 pk;
-                        pk.x = pack2<BF16>(v[j], v[j + 1]);
-                        pk.y = pack2<BF16>(v[j + 2], v[j + 3]);
-                        pk.z = pack2<BF16>(v[j + 4], v[j + 5]);
-                        pk.w = pack2<BF16>(v[j + 6], v[j + 7]);
-                        *reinterpret_cast<uint4 *>(dst + j) = pk;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (nb + j < p.N) dst[j] = cvt1<BF16>(v[j]);
+                for (int j = 0; j < 32; j += 8) {
+                    uint4 pk;
+                    pk.x = pack2<BF16>(v[j], v[j + 1]);
+                    pk.y = pack2<BF16>(v[j + 2], v[j + 3]);
+                    pk.z = pack2<BF16>(v[j + 4], v[j + 5]);
+                    pk.w = pack2<BF16>(v[j + 6], v[j + 7]);
+                    *reinterpret_cast<uint4 *>(dst + j) = pk;
                 }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (nb + j < p.N) dst[j] = cvt1<BF16>(v[j]);
+            }
+        }
+        if (FA) {
+            fence_proxy_async_smem();
+            named_sync(1, 32 * kProducers);
+            if (warp == 0 && lane == 0) {
+                tma_store_2d(&tm_out, tile, grp * 128, n0);
+                bulk_commit();
+                bulk_wait_read();
             }
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == kProducers) tmem_dealloc(tmem, 256);
+}
+
+// Dense-tile fprop / bprop for a minibatch of at most 64 rows, bs = 32.  Same tiles and
+// operands as k_tc_fbd with N = 64, but a 64-row minibatch gives too few tiles to fill the
+// GPU, so a cluster of kSplit CTAs shares one tile: CTA r multiplies the r-th quarter of the
+// tile's source pairs, the other CTAs write their fp32 partial tiles into the first CTA's
+// shared memory (distributed shared memory), and the first CTA sums them, rounds once and
+// stores.  No atomics and no global scratch.
+constexpr int kSplit = 4;
+
+template <int FA, bool BWD, bool BF16>
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kFbThreads, 1)
+k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
+               const __grid_constant__ CUtensorMap tm_zero, const __grid_constant__ CUtensorMap tm_out,
+               const FbdParams p)
+{
+    constexpr int STAGES = 4;                                    // = kProducers: warp w owns stage w
+    static_assert(STAGES % kProducers == 0, "producer warp w must own stages w, w+4, ...");
+    constexpr int A_BYTES = 16384, B_BYTES = 8192, STAGE = A_BYTES + B_BYTES;
+    constexpr int RED_BYTES = (kSplit - 1) * 128 * 64 * 4;     // partial tiles of the other CTAs
+    constexpr uint32_t A_LBO = BWD ? 16 : 2048, A_SBO = 512, A_KSTEP = BWD ? 32 : 1024;
+    constexpr uint32_t B_LBO = FA ? 16 : 8192, B_KSTEP = FA ? 32 : 2048, B_SUB = FA ? 64 : 4096;
+    constexpr uint32_t IDESC = idesc_f16(128, 64, BF16, !BWD, FA == 0);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *red = reinterpret_cast<float *>(smem + STAGES * STAGE);
+    const uint32_t *sched = reinterpret_cast<const uint32_t *>(smem + STAGES * STAGE + RED_BYTES);
+    __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full, sched_full;
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int aborted;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int grp = blockIdx.x / kSplit;
+    const int len = p.len[grp];
+
+    if (threadIdx.x == 0) {
+        aborted = 0;
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(&acc_full, 1);
+        mbar_init(&sched_full, 1);
+        fence_barrier_init();
+    }
+    if (warp == kProducers) tmem_alloc(&tmem_base, 64);
+    tc_fence_before();
+    cluster_sync();                                  // every CTA of the cluster is running
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    // this CTA's share of the tile's entries (the stream ends with 0xFFFFFFFF)
+    int lo = 0, hi = 0;
+    if (warp == 0 && lane == 0) {
+        mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
+        bulk_load((void *)sched, p.stream + p.off[grp], (uint32_t)len * 4u, &sched_full, policy_evict_last());
+        prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_w);
+    }
+    if (!mbar_wait(&sched_full, 0, p.status)) aborted = 1;
+    {
+        int n = 0;
+        while (sched[n * 9] != 0xFFFFFFFFu) ++n;
+        lo = (int)(rank * n / kSplit);
+        hi = (int)((rank + 1) * n / kSplit);
+    }
+
+    if (warp < kProducers) {
+        const uint64_t pol_act = policy_evict_last();
+        const uint64_t pol_w = policy_evict_first();
+        int last = -1;
+        for (int e = lo; e < hi && !aborted; ++e) {
+            const int chunk = e - lo, pos = e * 9;
+            if (chunk % kProducers != warp) continue;
+            const uint32_t hdr = sched[pos];
+            const int st = chunk % STAGES;
+            if (lane == 0) {
+                if (chunk >= STAGES && !mbar_wait(&empty[st], ((chunk / STAGES) - 1) & 1, p.status)) aborted = 1;
+                else mbar_arrive_expect_tx(&full[st], (uint32_t)STAGE);
+            }
+            __syncwarp();
+            if (aborted) break;
+            last = chunk;
+            const int pr = (int)(hdr >> 8);
+            uint8_t *a = smem + st * STAGE;
+            uint8_t *b = a + A_BYTES;
+            if (FA) {
+                if (lane == 0) tma_load_2d(b, &tm_act, &full[st], pr * 64, 0, pol_act);
+            } else {
+                if (lane == 0) tma_load_2d(b, &tm_act, &full[st], 0, pr * 64, pol_act);
+            }
+            if (lane >= 8 && lane < 16) {
+                const int sl = lane - 8;                        // sub * 4 + out
+                const int id = (int)sched[pos + 1 + sl] - 1;
+                uint8_t *d = a + (sl >> 2) * 8192 + (sl & 3) * 2048;
+                if (id >= 0) {
+                    tma_load_2d(d, &tm_w, &full[st], 0, id * 32, pol_w);
+                } else {
+                    const int zr = (int)((blockIdx.x * 13u + (unsigned)chunk * 8u + (unsigned)sl) % 128u) * 32;
+                    tma_load_2d(d, &tm_zero, &full[st], 0, zr, pol_w);
+                }
+            }
+        }
+        if (aborted && lane == 0 && last >= 0) mbar_wait(&full[last % STAGES], (last / STAGES) & 1, nullptr);
+        __syncwarp();
+    } else {
+        if (elect_one()) {
+            const uint32_t s_base = smem_u32(smem);
+            const uint64_t a_desc0 = sdesc(s_base, A_LBO, A_SBO, SW_64);
+            const uint64_t b_desc0 = sdesc(s_base + A_BYTES, B_LBO, 1024, SW_128);
+            uint32_t acc = 0;
+            for (int e = lo; e < hi && !aborted; ++e) {
+                const int chunk = e - lo;
+                const uint32_t hdr = sched[e * 9];
+                const int st = chunk % STAGES;
+                if (!mbar_wait(&full[st], (chunk / STAGES) & 1, p.status)) {
+                    aborted = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t so = st * STAGE;
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub) {
+                    if (!((hdr >> (sub * 4)) & 0xFu)) continue;
+                    const uint64_t ad = a_desc0 + ((so + sub * 8192) >> 4);
+                    const uint64_t bd = b_desc0 + ((so + sub * B_SUB) >> 4);
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        mma_ss(tmem, ad + ((ks * A_KSTEP) >> 4), bd + ((ks * B_KSTEP) >> 4), IDESC, acc);
+                        acc = 1;
+                    }
+                }
+                mma_commit(&empty[st]);
+            }
+            mma_commit(&acc_full);
+        }
+        __syncwarp();
+    }
+    // partial tile: warp q holds output features 32q..32q+31, lane = feature, 64 minibatch columns
+    float v[64];
+    const int q = warp & 3;
+    if (warp < kProducers) {
+        const bool ok = mbar_wait_warp(&acc_full, 0, p.status, 128);
+        tc_fence_after();
+        if (ok && hi > lo) {
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[c0 + j] = __uint_as_float(r[j]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) v[j] = 0.f;
+        }
+        if (rank != 0) {
+            const uint32_t dst = map_to_rank(smem_u32(red + ((rank - 1) * 128 + q * 32 + lane) * 64), 0);
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) st_cluster_v4(dst + j * 4, v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+    }
+    cluster_sync();                                  // partial tiles have landed in CTA 0
+    if (rank == 0 && warp < kProducers) {
+        const int f = grp * 128 + q * 32 + lane;
+#pragma unroll
+        for (int sidx = 0; sidx < kSplit - 1; ++sidx) {
+            const float *src = red + (sidx * 128 + q * 32 + lane) * 64;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(src + j);
+                v[j] += t4.x;
+                v[j + 1] += t4.y;
+                v[j + 2] += t4.z;
+                v[j + 3] += t4.w;
+            }
+        }
+        uint16_t *out = static_cast<uint16_t *>(p.out);
+        if (FA) {
+            // stage [64 minibatch rows][128 features] in the idle stage memory, one TMA store
+            uint16_t *tile = reinterpret_cast<uint16_t *>(smem);
+#pragma unroll
+            for (int j = 0; j < 64; ++j) tile[j * 128 + q * 32 + lane] = cvt1<BF16>(v[j]);
+            fence_proxy_async_smem();
+            named_sync(1, 32 * kProducers);
+            if (warp == 0 && lane == 0) {
+                tma_store_2d(&tm_out, tile, grp * 128, 0);
+                bulk_commit();
+                bulk_wait_read();
+            }
+        } else if (f < p.Fout) {
+            uint16_t *dst = out + (size_t)f * p.N;
+            if (p.N == 64) {
+#pragma unroll
+                for (int j = 0; j < 64; j += 8) {
+                    uint4 pk;
+                    pk.x = pack2<BF16>(v[j], v[j + 1]);
+                    pk.y = pack2<BF16>(v[j + 2], v[j + 3]);
+                    pk.z = pack2<BF16>(v[j + 4], v[j + 5]);
+                    pk.w = pack2<BF16>(v[j + 6], v[j + 7]);
+                    *reinterpret_cast<uint4 *>(dst + j) = pk;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (j < p.N) dst[j] = cvt1<BF16>(v[j]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kProducers) tmem_dealloc(tmem, 64);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -1533,6 +1760,9 @@ bsmm_status launch_fbd(bsmm_ctx *h, FbDenseSched &fs, const void *act, const voi
     else ok = make_map2d(&m_act, act, t, N, Fin, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && make_map2d(&m_w, w, t, 32, (uint64_t)h->nnz * 32, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     ok = ok && make_map2d(&m_zero, st->d_zero, t, 32, kZeroBytes / 64, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    CUtensorMap m_out;
+    if (FA) ok = ok && make_map2d(&m_out, out, t, Fout, N, 128, 256, CU_TENSOR_MAP_SWIZZLE_NONE);
+    else m_out = m_act;                                  // unused for (C,N) outputs
     if (!ok) return BSMM_ERR_CUDA;
     FbdParams p;
     p.out = out;
@@ -1551,7 +1781,45 @@ bsmm_status launch_fbd(bsmm_ctx *h, FbDenseSched &fs, const void *act, const voi
             return BSMM_ERR_CUDA;
         attr_set.store(h->device);
     }
-    kern<<<fs.ngroups * p.n_tiles, kFbThreads, smem, s>>>(m_act, m_w, m_zero, p);
+    kern<<<fs.ngroups * p.n_tiles, kFbThreads, smem, s>>>(m_act, m_w, m_zero, m_out, p);
+    g_bsmm_launches += 1;
+    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+}
+
+template <int FA, bool BWD, bool BF16>
+bsmm_status launch_fbd_split(bsmm_ctx *h, FbDenseSched &fs, const void *act, const void *w, void *out, int N,
+                             bsmm_dtype t, cudaStream_t s)
+{
+    TcState *st = state(h);
+    const int C = h->R * 32, K = h->S * 32;
+    const int Fin = BWD ? K : C, Fout = BWD ? C : K;
+    CUtensorMap m_act, m_w, m_zero, m_out;
+    bool ok;
+    if (FA) ok = make_map2d(&m_act, act, t, Fin, N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    else ok = make_map2d(&m_act, act, t, N, Fin, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map2d(&m_w, w, t, 32, (uint64_t)h->nnz * 32, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok = ok && make_map2d(&m_zero, st->d_zero, t, 32, kZeroBytes / 64, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (FA) ok = ok && make_map2d(&m_out, out, t, Fout, N, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+    else m_out = m_act;                                  // unused for (C,N) outputs
+    if (!ok) return BSMM_ERR_CUDA;
+    FbdParams p;
+    p.out = out;
+    p.stream = fs.d_stream;
+    p.off = fs.d_off;
+    p.len = fs.d_len;
+    p.status = h->d_status;
+    p.N = N;
+    p.Fout = Fout;
+    p.n_tiles = 1;
+    const int smem = 4 * (16384 + 8192) + (kSplit - 1) * 128 * 64 * 4 + kFbdSchedWords * 4 + 1024;
+    auto kern = k_tc_fbd_split<FA, BWD, BF16>;
+    static std::atomic<int> attr_set{-1};
+    if (attr_set.load() != h->device) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return BSMM_ERR_CUDA;
+        attr_set.store(h->device);
+    }
+    kern<<<fs.ngroups * kSplit, kFbThreads, smem, s>>>(m_act, m_w, m_zero, m_out, p);
     g_bsmm_launches += 1;
     return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
@@ -1564,7 +1832,7 @@ bsmm_status fbd_try(bsmm_ctx *h, const void *act, const void *w, void *out, int 
 {
     if (h->bs != 32 || h->nnz == 0) return BSMM_ERR_UNSUPPORTED;
     const double density = (double)h->nnz / ((double)h->R * h->S);
-    bool dense = density >= 0.25 && N > 128;
+    bool dense = density >= 0.25 && (N > 128 || N <= 64);
     if (const char *e = getenv("BSMM_TC_FB")) {
         if (!strcmp(e, "window")) dense = false;
         if (!strcmp(e, "dense")) dense = true;
@@ -1584,6 +1852,13 @@ bsmm_status fbd_try(bsmm_ctx *h, const void *act, const void *w, void *out, int 
     }
     if (!fs->built) return BSMM_ERR_UNSUPPORTED;
     const bool bf = t == BSMM_BF16;
+    if (N <= 64) {
+        // minibatch of one 64-row tile: clusters of kSplit CTAs share each tile
+        if (h->fa) return bf ? launch_fbd_split<1, BWD, true>(h, *fs, act, w, out, N, t, s)
+                             : launch_fbd_split<1, BWD, false>(h, *fs, act, w, out, N, t, s);
+        return bf ? launch_fbd_split<0, BWD, true>(h, *fs, act, w, out, N, t, s)
+                  : launch_fbd_split<0, BWD, false>(h, *fs, act, w, out, N, t, s);
+    }
     if (h->fa) return bf ? launch_fbd<1, BWD, true>(h, *fs, act, w, out, N, t, s)
                          : launch_fbd<1, BWD, false>(h, *fs, act, w, out, N, t, s);
     return bf ? launch_fbd<0, BWD, true>(h, *fs, act, w, out, N, t, s)

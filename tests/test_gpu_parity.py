@@ -352,11 +352,14 @@ def test_updat_variants_bs32(monkeypatch, variant, fa, p, G):
 
 
 @pytest.mark.parametrize("fa,dtype", [(1, "bf16"), (0, "f16")])
-@pytest.mark.parametrize("R,S,p,N", [(10, 13, 0.5, 392), (7, 9, 0.9, 264), (12, 6, 0.3, 136)])
+@pytest.mark.parametrize("R,S,p,N", [(10, 13, 0.5, 392), (7, 9, 0.9, 264), (12, 6, 0.3, 136),
+                                     (10, 13, 0.5, 64), (9, 7, 0.8, 40)])
 def test_fprop_bprop_variants_bs32(monkeypatch, fa, dtype, R, S, p, N):
     """Both tensor-core fprop/bprop schemes (windows of output blocks over 128-row tiles,
-    or dense 4-block x 256-row tiles with absent blocks as zero tiles) against the oracle,
-    on layouts whose block counts are not multiples of the tile and a ragged minibatch."""
+    or dense 4-block x 256-row tiles with absent blocks as zero tiles; for a minibatch of
+    at most 64 rows the dense tiles are split over a cluster of 4 CTAs and summed in
+    distributed shared memory) against the oracle, on layouts whose block counts are not
+    multiples of the tile and a ragged minibatch."""
     bs = 32
     L = rand_layout(R, S, p, R * 31 + S)
     L[:, 2] = 0                                           # an empty output block column
