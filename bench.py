@@ -227,9 +227,30 @@ def run_ours(args):
     sleep_cycles = int(host_step_s * 1.3 * chunk * 2.1e9) + 100000   # cycles at <= 2.1 GHz
 
     K_steps = args.steps
-    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
-    ev_pass = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in passes]
-               for _ in range(K_steps)]
+
+    def timed(per_pass):
+        # Steps are queued in chunks behind a device sleep so the host never starves the GPU.
+        # The step events bracket whole steps only, so consecutive kernels of a step may overlap
+        # (programmatic dependent launch); the per-pass run brackets every kernel with events,
+        # which gives each kernel's own duration.
+        ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(K_steps)]
+        ev_pass = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in passes]
+                   for _ in range(K_steps)] if per_pass else None
+        for c0 in range(0, K_steps, chunk):
+            torch.cuda._sleep(sleep_cycles)
+            for i in range(c0, min(K_steps, c0 + chunk)):
+                d = sets[i % NSETS]
+                ev_step[i][0].record(stream)
+                for j, p in enumerate(passes):
+                    if per_pass:
+                        ev_pass[i][j][0].record(stream)
+                    launch_pass(p[0], d)
+                    if per_pass:
+                        ev_pass[i][j][1].record(stream)
+                ev_step[i][1].record(stream)
+        return ev_step, ev_pass
+
     sampler = ClockSampler(local)
     if ws > 1:
         torch.distributed.barrier()
@@ -237,20 +258,13 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.3)
     wall0 = time.perf_counter()
-    for c0 in range(0, K_steps, chunk):
-        torch.cuda._sleep(sleep_cycles)
-        for i in range(c0, min(K_steps, c0 + chunk)):
-            d = sets[i % NSETS]
-            ev_step[i][0].record(stream)
-            for j, p in enumerate(passes):
-                ev_pass[i][j][0].record(stream)
-                launch_pass(p[0], d)
-                ev_pass[i][j][1].record(stream)
-            ev_step[i][1].record(stream)
+    ev_step, _ = timed(False)
     torch.cuda.synchronize()
     wall1 = time.perf_counter()
     if ws > 1:
         torch.distributed.barrier()
+    _, ev_pass = timed(True)
+    torch.cuda.synchronize()
     clocks = sampler.stop()
     m.sync_status()
 

@@ -583,18 +583,23 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    // Every CTA of this grid holds its tensor memory before a dependent kernel may start, so a
+    // dependent CTA that waits for it in tcgen05.alloc waits only on CTAs that will finish.
+    pdl_launch_dependents();
+    // The window schedule belongs to the handle: fetch it before waiting for the previous kernel.
+    if (warp == 0 && lane == 0) {
+        const int len = p.win_len[win];
+        mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
+        if (len > 0) bulk_load((void *)sched, p.stream + p.win_off[win], (uint32_t)len * 4u, &sched_full, policy_evict_last());
+        prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_w);
+    }
+    pdl_wait();
 
     if (warp < kProducers) {
         // ---------------- TMA producers: warp w < P issues chunks w, w+P, ...; one load per lane ----
         const uint64_t pol_act = policy_evict_last();
         const uint64_t pol_w = policy_evict_first();
-        if (warp == 0 && lane == 0) {
-            const int len = p.win_len[win];
-            mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
-            if (len > 0) bulk_load((void *)sched, p.stream + p.win_off[win], (uint32_t)len * 4u, &sched_full, pol_act);
-            prefetch_tmap(&tm_act);
-            prefetch_tmap(&tm_w);
-        }
         if (!mbar_wait_warp(&sched_full, 0, p.status, 64)) aborted = 1;
         __syncwarp();
         int chunk = 0, last = -1;
@@ -836,6 +841,9 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    // Every CTA of this grid holds its tensor memory before a dependent kernel may start, so a
+    // dependent CTA that waits for it in tcgen05.alloc waits only on CTAs that will finish.
+    pdl_launch_dependents();
     const int32_t *gtab = p.table + (size_t)blockIdx.x * kTableWords;
     if (warp == 0 && lane == 0) {
         const int nu = gtab[0];
@@ -843,6 +851,7 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
         mbar_arrive_expect_tx(&tab_full, bytes);
         bulk_load(tab, gtab, bytes, &tab_full, policy_evict_first());
     }
+    pdl_wait();
     const bool tab_ok = mbar_wait_warp(&tab_full, 0, p.status, 64);
     const int nunits = tab_ok ? tab[0] : 0;
 
@@ -1034,6 +1043,9 @@ k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    // Every CTA of this grid holds its tensor memory before a dependent kernel may start, so a
+    // dependent CTA that waits for it in tcgen05.alloc waits only on CTAs that will finish.
+    pdl_launch_dependents();
     const int32_t *gtab = p.table + (size_t)blockIdx.x * kDTableWords;
     if (warp == 0 && lane == 0) {
         const int nu = gtab[0];
@@ -1041,6 +1053,7 @@ k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
         mbar_arrive_expect_tx(&tab_full, bytes);
         bulk_load(tab, gtab, bytes, &tab_full, policy_evict_first());
     }
+    pdl_wait();
     const bool tab_ok = mbar_wait_warp(&tab_full, 0, p.status, 64);
     const int nunits = tab_ok ? tab[0] : 0;
 
@@ -1210,16 +1223,21 @@ k_tc_fbd(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    // Every CTA of this grid holds its tensor memory before a dependent kernel may start, so a
+    // dependent CTA that waits for it in tcgen05.alloc waits only on CTAs that will finish.
+    pdl_launch_dependents();
+    // The tile schedule belongs to the handle: fetch it before waiting for the previous kernel.
+    if (warp == 0 && lane == 0) {
+        mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
+        bulk_load((void *)sched, p.stream + p.off[grp], (uint32_t)len * 4u, &sched_full, policy_evict_last());
+        prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_w);
+    }
+    pdl_wait();
 
     if (warp < kProducers) {
         const uint64_t pol_act = policy_evict_last();
         const uint64_t pol_w = policy_evict_first();
-        if (warp == 0 && lane == 0) {
-            mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
-            bulk_load((void *)sched, p.stream + p.off[grp], (uint32_t)len * 4u, &sched_full, pol_act);
-            prefetch_tmap(&tm_act);
-            prefetch_tmap(&tm_w);
-        }
         if (!mbar_wait_warp(&sched_full, 0, p.status, 64)) aborted = 1;
         __syncwarp();
         int last = -1;
@@ -1408,6 +1426,9 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     cluster_sync();                                  // every CTA of the cluster is running
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    // Every CTA of this grid holds its tensor memory before a dependent kernel may start, so a
+    // dependent CTA that waits for it in tcgen05.alloc waits only on CTAs that will finish.
+    pdl_launch_dependents();
 
     // this CTA's share of the tile's entries (the stream ends with 0xFFFFFFFF)
     int lo = 0, hi = 0;
@@ -1417,6 +1438,7 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         prefetch_tmap(&tm_act);
         prefetch_tmap(&tm_w);
     }
+    pdl_wait();
     if (!mbar_wait(&sched_full, 0, p.status)) aborted = 1;
     {
         int n = 0;
@@ -1577,6 +1599,26 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
 // Host launchers
 // ---------------------------------------------------------------------------------------
 
+// Launches with programmatic stream serialization when `pdl` is set: the kernel may start
+// while the previous kernel on the stream finishes; it fetches handle-owned schedules, then
+// waits in pdl_wait() before it touches any caller buffer.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int BS, int FA, bool BWD, bool BF16>
 bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const FbStages &geo, const void *act, const void *w, void *out,
                       int N, bsmm_dtype t, cudaStream_t s)
@@ -1618,14 +1660,14 @@ bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const FbStages &geo, const void 
         attr_set.store(h->device);
     }
     dim3 grid(fs.nwin * p.n_tiles);
-    kern<<<grid, kFbThreads, smem, s>>>(m_act, m_w, m_zero, p);
+    const cudaError_t le = launch_pdl(kern, grid, dim3(kFbThreads), smem, s, true, m_act, m_w, m_zero, p);
     g_bsmm_launches += 1;
-    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+    return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
 template <int BS, int FA, bool BF16>
 bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, float *dw, int N, bsmm_dtype t, int acc,
-                      cudaStream_t s)
+                      cudaStream_t s, bool pdl = true)
 {
     constexpr int BSE = BS == 8 ? 16 : BS;
     using G = UpGeo<BSE, FA>;
@@ -1658,9 +1700,9 @@ bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, float *dw, i
             return BSMM_ERR_CUDA;
         attr_set.store(h->device);
     }
-    kern<<<us.ctas, kUpThreads, smem, s>>>(maps, p);
+    const cudaError_t le = launch_pdl(kern, dim3(us.ctas), dim3(kUpThreads), smem, s, pdl, maps, p);
     g_bsmm_launches += 1;
-    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+    return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
 // Stage geometry for a call.  P producer warps share the chunks (chunk c -> warp c mod P)
@@ -1742,9 +1784,9 @@ bsmm_status launch_up_dense(bsmm_ctx *h, UpDenseSched &us, const GroupPtrs &g, f
             return BSMM_ERR_CUDA;
         attr_set.store(h->device);
     }
-    kern<<<us.ctas, kUpThreads, smem, s>>>(maps, p);
+    const cudaError_t le = launch_pdl(kern, dim3(us.ctas), dim3(kUpThreads), smem, s, true, maps, p);
     g_bsmm_launches += 1;
-    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+    return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
 template <int FA, bool BWD, bool BF16>
@@ -1781,9 +1823,10 @@ bsmm_status launch_fbd(bsmm_ctx *h, FbDenseSched &fs, const void *act, const voi
             return BSMM_ERR_CUDA;
         attr_set.store(h->device);
     }
-    kern<<<fs.ngroups * p.n_tiles, kFbThreads, smem, s>>>(m_act, m_w, m_zero, m_out, p);
+    const cudaError_t le =
+        launch_pdl(kern, dim3(fs.ngroups * p.n_tiles), dim3(kFbThreads), smem, s, true, m_act, m_w, m_zero, m_out, p);
     g_bsmm_launches += 1;
-    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+    return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
 template <int FA, bool BWD, bool BF16>
@@ -1819,9 +1862,10 @@ bsmm_status launch_fbd_split(bsmm_ctx *h, FbDenseSched &fs, const void *act, con
             return BSMM_ERR_CUDA;
         attr_set.store(h->device);
     }
-    kern<<<fs.ngroups * kSplit, kFbThreads, smem, s>>>(m_act, m_w, m_zero, m_out, p);
+    const cudaError_t le =
+        launch_pdl(kern, dim3(fs.ngroups * kSplit), dim3(kFbThreads), smem, s, true, m_act, m_w, m_zero, m_out, p);
     g_bsmm_launches += 1;
-    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+    return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
 // Dense tiles for bs = 32 layouts with at least a quarter of the blocks present and a

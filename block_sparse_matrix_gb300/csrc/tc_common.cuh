@@ -297,6 +297,18 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ---- programmatic dependent launch -------------------------------------------------------
+
+// Lets the next kernel on the stream start its launch (it still waits in pdl_wait()).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the previous kernel on the stream has completed and its writes are visible.
+// A no-op when the kernel was launched without programmatic serialization.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- clusters (distributed shared memory) -------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
