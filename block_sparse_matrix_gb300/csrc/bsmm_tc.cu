@@ -1378,29 +1378,31 @@ k_tc_fbd(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUt
 // Dense-tile fprop / bprop for a minibatch of at most 64 rows, bs = 32.  Same tiles and
 // operands as k_tc_fbd with N = 64, but a 64-row minibatch gives too few tiles to fill the
 // GPU, so a cluster of kSplit CTAs shares one tile: CTA r multiplies the r-th quarter of the
-// tile's source pairs, the other CTAs write their fp32 partial tiles into the first CTA's
-// shared memory (distributed shared memory), and the first CTA sums them, rounds once and
-// stores.  No atomics and no global scratch.
+// tile's source pairs.  The partial tiles are then summed across the cluster in distributed
+// shared memory, each CTA owning 32 of the tile's 128 output features: it receives the other
+// three CTAs' fp32 partials of its features into its (then idle) stage memory, adds its own,
+// rounds once and stores.  No atomics and no global scratch; with the reduction buffer inside
+// the stage memory, 8 stages of 24 KB keep the weight stream from HBM in flight.
 constexpr int kSplit = 4;
 
 template <int FA, bool BWD, bool BF16>
 __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kFbThreads, 1)
 k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
-               const __grid_constant__ CUtensorMap tm_zero, const __grid_constant__ CUtensorMap tm_out,
-               const FbdParams p)
+               const __grid_constant__ CUtensorMap tm_zero, const FbdParams p)
 {
-    constexpr int STAGES = 4;                                    // = kProducers: warp w owns stage w
+    constexpr int STAGES = 8;                                    // warp w owns stages w and w + 4
     static_assert(STAGES % kProducers == 0, "producer warp w must own stages w, w+4, ...");
+    static_assert(kSplit == kProducers, "CTA r of the cluster owns the features of epilogue warp r");
     constexpr int A_BYTES = 16384, B_BYTES = 8192, STAGE = A_BYTES + B_BYTES;
-    constexpr int RED_BYTES = (kSplit - 1) * 128 * 64 * 4;     // partial tiles of the other CTAs
     constexpr uint32_t A_LBO = BWD ? 16 : 2048, A_SBO = 512, A_KSTEP = BWD ? 32 : 1024;
     constexpr uint32_t B_LBO = FA ? 16 : 8192, B_KSTEP = FA ? 32 : 2048, B_SUB = FA ? 64 : 4096;
     constexpr uint32_t IDESC = idesc_f16(128, 64, BF16, !BWD, FA == 0);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *red = reinterpret_cast<float *>(smem + STAGES * STAGE);
-    const uint32_t *sched = reinterpret_cast<const uint32_t *>(smem + STAGES * STAGE + RED_BYTES);
+    // after the main loop: red[slot][j / 4][lane][4], the partials of the three other CTAs
+    float *red = reinterpret_cast<float *>(smem);
+    const uint32_t *sched = reinterpret_cast<const uint32_t *>(smem + STAGES * STAGE);
     __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full, sched_full;
     __shared__ uint32_t tmem_base;
     __shared__ volatile int aborted;
@@ -1450,7 +1452,7 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     if (warp < kProducers) {
         const uint64_t pol_act = policy_evict_last();
         const uint64_t pol_w = policy_evict_first();
-        int last = -1;
+        int last = -1, prev = -1;
         for (int e = lo; e < hi && !aborted; ++e) {
             const int chunk = e - lo, pos = e * 9;
             if (chunk % kProducers != warp) continue;
@@ -1462,6 +1464,7 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
             }
             __syncwarp();
             if (aborted) break;
+            prev = last;
             last = chunk;
             const int pr = (int)(hdr >> 8);
             uint8_t *a = smem + st * STAGE;
@@ -1483,7 +1486,11 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
                 }
             }
         }
-        if (aborted && lane == 0 && last >= 0) mbar_wait(&full[last % STAGES], (last / STAGES) & 1, nullptr);
+        if (aborted && lane == 0) {
+            // let this warp's copies in flight land before the stage memory is reused
+            if (last >= 0) mbar_wait(&full[last % STAGES], (last / STAGES) & 1, nullptr);
+            if (prev >= 0) mbar_wait(&full[prev % STAGES], (prev / STAGES) & 1, nullptr);
+        }
         __syncwarp();
     } else {
         if (elect_one()) {
@@ -1518,7 +1525,8 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
         __syncwarp();
     }
-    // partial tile: warp q holds output features 32q..32q+31, lane = feature, 64 minibatch columns
+    // partial tile: warp q holds output features 32q..32q+31 (lane = feature) for the 64
+    // minibatch columns; CTA q of the cluster owns those features
     float v[64];
     const int q = warp & 3;
     if (warp < kProducers) {
@@ -1537,43 +1545,37 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
 #pragma unroll
             for (int j = 0; j < 64; ++j) v[j] = 0.f;
         }
-        if (rank != 0) {
-            const uint32_t dst = map_to_rank(smem_u32(red + ((rank - 1) * 128 + q * 32 + lane) * 64), 0);
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) st_cluster_v4(dst + j * 4, v[j], v[j + 1], v[j + 2], v[j + 3]);
-        }
     }
-    cluster_sync();                                  // partial tiles have landed in CTA 0
-    if (rank == 0 && warp < kProducers) {
-        const int f = grp * 128 + q * 32 + lane;
+    cluster_sync();                                  // every CTA's MMAs are done: stage memory is free
+    if (warp < kProducers && q != (int)rank) {
+        const int slot = (int)rank < q ? (int)rank : (int)rank - 1;
+        const uint32_t dst = map_to_rank(smem_u32(red + (slot * 16 * 32 + lane) * 4), (uint32_t)q);
 #pragma unroll
-        for (int sidx = 0; sidx < kSplit - 1; ++sidx) {
-            const float *src = red + (sidx * 128 + q * 32 + lane) * 64;
+        for (int j = 0; j < 64; j += 4) st_cluster_v4(dst + (j / 4) * 32 * 16, v[j], v[j + 1], v[j + 2], v[j + 3]);
+    }
+    cluster_sync();                                  // the partials of this CTA's features have landed
+    if (warp == (int)rank) {
+#pragma unroll
+        for (int slot = 0; slot < kSplit - 1; ++slot) {
 #pragma unroll
             for (int j = 0; j < 64; j += 4) {
-                const float4 t4 = *reinterpret_cast<const float4 *>(src + j);
+                const float4 t4 = *reinterpret_cast<const float4 *>(red + ((slot * 16 + j / 4) * 32 + lane) * 4);
                 v[j] += t4.x;
                 v[j + 1] += t4.y;
                 v[j + 2] += t4.z;
                 v[j + 3] += t4.w;
             }
         }
+        const int f = grp * 128 + q * 32 + lane;
         uint16_t *out = static_cast<uint16_t *>(p.out);
-        if (FA) {
-            // stage [64 minibatch rows][128 features] in the idle stage memory, one TMA store
-            uint16_t *tile = reinterpret_cast<uint16_t *>(smem);
+        if (f < p.Fout) {
+            if (FA) {
+                // (N, F) rows: the warp writes 64 contiguous bytes of each minibatch row
 #pragma unroll
-            for (int j = 0; j < 64; ++j) tile[j * 128 + q * 32 + lane] = cvt1<BF16>(v[j]);
-            fence_proxy_async_smem();
-            named_sync(1, 32 * kProducers);
-            if (warp == 0 && lane == 0) {
-                tma_store_2d(&tm_out, tile, grp * 128, 0);
-                bulk_commit();
-                bulk_wait_read();
-            }
-        } else if (f < p.Fout) {
-            uint16_t *dst = out + (size_t)f * p.N;
-            if (p.N == 64) {
+                for (int j = 0; j < 64; ++j)
+                    if (j < p.N) out[(size_t)j * p.Fout + f] = cvt1<BF16>(v[j]);
+            } else if (p.N == 64) {
+                uint16_t *dst = out + (size_t)f * p.N;
 #pragma unroll
                 for (int j = 0; j < 64; j += 8) {
                     uint4 pk;
@@ -1584,6 +1586,7 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
                     *reinterpret_cast<uint4 *>(dst + j) = pk;
                 }
             } else {
+                uint16_t *dst = out + (size_t)f * p.N;
 #pragma unroll
                 for (int j = 0; j < 64; ++j)
                     if (j < p.N) dst[j] = cvt1<BF16>(v[j]);
@@ -1836,14 +1839,12 @@ bsmm_status launch_fbd_split(bsmm_ctx *h, FbDenseSched &fs, const void *act, con
     TcState *st = state(h);
     const int C = h->R * 32, K = h->S * 32;
     const int Fin = BWD ? K : C, Fout = BWD ? C : K;
-    CUtensorMap m_act, m_w, m_zero, m_out;
+    CUtensorMap m_act, m_w, m_zero;
     bool ok;
     if (FA) ok = make_map2d(&m_act, act, t, Fin, N, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     else ok = make_map2d(&m_act, act, t, N, Fin, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && make_map2d(&m_w, w, t, 32, (uint64_t)h->nnz * 32, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     ok = ok && make_map2d(&m_zero, st->d_zero, t, 32, kZeroBytes / 64, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (FA) ok = ok && make_map2d(&m_out, out, t, Fout, N, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
-    else m_out = m_act;                                  // unused for (C,N) outputs
     if (!ok) return BSMM_ERR_CUDA;
     FbdParams p;
     p.out = out;
@@ -1854,7 +1855,7 @@ bsmm_status launch_fbd_split(bsmm_ctx *h, FbDenseSched &fs, const void *act, con
     p.N = N;
     p.Fout = Fout;
     p.n_tiles = 1;
-    const int smem = 4 * (16384 + 8192) + (kSplit - 1) * 128 * 64 * 4 + kFbdSchedWords * 4 + 1024;
+    const int smem = 8 * (16384 + 8192) + kFbdSchedWords * 4 + 1024;
     auto kern = k_tc_fbd_split<FA, BWD, BF16>;
     static std::atomic<int> attr_set{-1};
     if (attr_set.load() != h->device) {
@@ -1863,7 +1864,7 @@ bsmm_status launch_fbd_split(bsmm_ctx *h, FbDenseSched &fs, const void *act, con
         attr_set.store(h->device);
     }
     const cudaError_t le =
-        launch_pdl(kern, dim3(fs.ngroups * kSplit), dim3(kFbThreads), smem, s, true, m_act, m_w, m_zero, m_out, p);
+        launch_pdl(kern, dim3(fs.ngroups * kSplit), dim3(kFbThreads), smem, s, true, m_act, m_w, m_zero, p);
     g_bsmm_launches += 1;
     return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
