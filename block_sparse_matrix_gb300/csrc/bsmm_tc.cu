@@ -784,7 +784,10 @@ template <int BSE, int FA> struct UpGeo {
     static constexpr int B_BYTES = TK * BSE * 2;
     static constexpr int PANEL = TK * BSE * 2;                      // one stacked panel
     static constexpr int STAGES = 4;                                 // a multiple of kProducers
-    static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + kTableWords * 4;
+    static constexpr int TAB_OFF = STAGES * (A_BYTES + B_BYTES);
+    static constexpr int OUT_OFF = (TAB_OFF + kTableWords * 4 + 127) / 128 * 128;
+    static constexpr int OUT_BYTES = 4 * 32 * 32 * 4;              // per epilogue warp: 32 rows of up to 32 fp32
+    static constexpr int SMEM = OUT_OFF + OUT_BYTES;
     // fa=1: A MN-major (rows n, BSE features contiguous); fa=0: A K-major (rows = features, n contiguous).
     static constexpr uint32_t A_SWZ = FA ? (BSE == 32 ? SW_64 : SW_32) : SW_128;
     static constexpr uint32_t A_LBO = FA ? PANEL : 16;
@@ -813,7 +816,8 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + G::STAGES * G::A_BYTES;
-    int32_t *tab = reinterpret_cast<int32_t *>(sB + G::STAGES * G::B_BYTES);
+    int32_t *tab = reinterpret_cast<int32_t *>(smem + G::TAB_OFF);
+    float *sout = reinterpret_cast<float *>(smem + G::OUT_OFF);
     __shared__ __align__(8) uint64_t full[G::STAGES], empty[G::STAGES], acc_full[2], acc_empty[2], tab_full;
     __shared__ uint32_t tmem_base;
     __shared__ volatile int aborted;
@@ -945,20 +949,39 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
             const int32_t *ut = tab + 4 + u * kUnitWords;
-            if (slot < ut[1] && !aborted) {
-                const int32_t *rec = ut + 2 + 5 * slot;
-                if (!COARSE) {
-                    float *dst = p.dw + ((size_t)rec[1] * BS + i) * BS;
+            if (!COARSE) {
+                // The warp's 32 rows are 32 / BSE whole blocks, [row][BS] fp32 like the blocks in
+                // dw.  Pass them through shared memory so that each store instruction writes 512
+                // contiguous bytes of one block; 16-byte chunk c of row r sits at chunk
+                // c ^ (r mod BS/4), which keeps both the row writes and the reads conflict-free.
+                constexpr int CH = BS / 4;                      // 16-byte chunks per row
+                float *stg = sout + q * 32 * 32;
 #pragma unroll
-                    for (int j = 0; j < BS; j += 4) {
-                        float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                for (int c = 0; c < CH; ++c)
+                    *reinterpret_cast<float4 *>(stg + lane * BS + ((c ^ (lane & (CH - 1))) * 4)) =
+                        make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
+                __syncwarp();
+                constexpr int BLK = BSE * BS;                   // floats per block
+#pragma unroll
+                for (int k4 = 0; k4 < BS / 4; ++k4) {
+                    const int o = k4 * 128 + lane * 4;          // float offset in the warp's rows
+                    const int sl = q * (32 / BSE) + o / BLK;
+                    const int r = o / BS, c = (o % BS) / 4;
+                    const float4 val = *reinterpret_cast<const float4 *>(stg + r * BS + ((c ^ (r & (CH - 1))) * 4));
+                    if (sl < ut[1] && !aborted) {
+                        float *dst = p.dw + (size_t)ut[2 + 5 * sl + 1] * (BS * BS) + (o % BLK);
+                        float4 r4 = val;
                         if (p.accumulate) {
-                            float4 a = *reinterpret_cast<float4 *>(dst + j);
-                            o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
+                            const float4 a = *reinterpret_cast<const float4 *>(dst);
+                            r4.x += a.x; r4.y += a.y; r4.z += a.z; r4.w += a.w;
                         }
-                        *reinterpret_cast<float4 *>(dst + j) = o;
+                        *reinterpret_cast<float4 *>(dst) = r4;
                     }
-                } else {
+                }
+                __syncwarp();                                   // reads done before the next unit's writes
+            } else if (slot < ut[1] && !aborted) {
+                const int32_t *rec = ut + 2 + 5 * slot;
+                {
                     const int cs = i / 8, i8 = i % 8;
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
