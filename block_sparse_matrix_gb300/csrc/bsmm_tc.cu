@@ -1019,7 +1019,9 @@ struct UpDenseGeo {
     static constexpr int A_BYTES = 128 * TK * 2;                     // 16 KB
     static constexpr int B_BYTES = 256 * TK * 2;                     // 32 KB
     static constexpr int STAGES = 4;                                 // a multiple of kProducers
-    static constexpr int SMEM = STAGES * (A_BYTES + B_BYTES) + kDTableWords * 4;
+    static constexpr int TAB_OFF = STAGES * (A_BYTES + B_BYTES);
+    static constexpr int OUT_OFF = (TAB_OFF + kDTableWords * 4 + 127) / 128 * 128;
+    static constexpr int SMEM = OUT_OFF + 4 * 32 * 32 * 4;           // + a 32 x 32 fp32 block per epilogue warp
 };
 
 template <int FA, bool BF16>
@@ -1038,7 +1040,8 @@ k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + G::STAGES * G::A_BYTES;
-    int32_t *tab = reinterpret_cast<int32_t *>(sB + G::STAGES * G::B_BYTES);
+    int32_t *tab = reinterpret_cast<int32_t *>(smem + G::TAB_OFF);
+    float *sout = reinterpret_cast<float *>(smem + G::OUT_OFF);
     __shared__ __align__(8) uint64_t full[G::STAGES], empty[G::STAGES], acc_full[2], acc_empty[2], tab_full;
     __shared__ uint32_t tmem_base;
     __shared__ volatile int aborted;
@@ -1166,18 +1169,28 @@ k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) v[c0 + j] = __uint_as_float(r[j]);
                 }
-                if (!aborted) {
-                    float *dst = p.dw + ((size_t)id * 32 + lane) * 32;
+                // through shared memory so that each store writes 512 contiguous bytes of the block;
+                // 16-byte chunk c of row r sits at chunk c ^ (r mod 8) (conflict-free both ways)
+                float *stg = sout + q * 32 * 32;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4 *>(stg + lane * 32 + ((c ^ (lane & 7)) * 4)) =
+                        make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
+                __syncwarp();
+                if (!aborted) {
+                    float *blk = p.dw + (size_t)id * 1024;
+#pragma unroll
+                    for (int k4 = 0; k4 < 8; ++k4) {
+                        const int o = k4 * 128 + lane * 4, r = o / 32, c = (o % 32) / 4;
+                        float4 r4 = *reinterpret_cast<const float4 *>(stg + r * 32 + ((c ^ (r & 7)) * 4));
                         if (p.accumulate) {
-                            float4 a = *reinterpret_cast<float4 *>(dst + j);
-                            o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
+                            const float4 a = *reinterpret_cast<const float4 *>(blk + o);
+                            r4.x += a.x; r4.y += a.y; r4.z += a.z; r4.w += a.w;
                         }
-                        *reinterpret_cast<float4 *>(dst + j) = o;
+                        *reinterpret_cast<float4 *>(blk + o) = r4;
                     }
                 }
+                __syncwarp();                                   // reads done before the next block's writes
             }
             tc_fence_before();
             __syncwarp();
