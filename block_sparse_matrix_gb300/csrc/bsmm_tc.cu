@@ -90,7 +90,7 @@ struct TcState {
     std::map<uint64_t, FbSched> fb;   // key: pass, window log2, chunk entries, chunk records
     UpSched up;
     struct UpDenseSched *upd = nullptr;
-    struct FbDenseSched *fbd[2] = {nullptr, nullptr};   // dense-tile fprop / bprop
+    struct FbDenseSched *fbd[4] = {};   // dense-tile fprop / bprop; + 2: CTA-pair schedules
     void *d_zero = nullptr;   // zero buffer: 8x8 zero tiles for absent sub-blocks of 16x16 coarse blocks
     std::mutex mu;
 };
@@ -424,6 +424,48 @@ bool build_fb_dense(bsmm_ctx *h, FbDenseSched &fs, bool bwd)
         while (stream.size() % 4) stream.push_back(0);
         len[gi] = (int32_t)(stream.size() - off[gi]);
         if (len[gi] > kFbdSchedWords) {
+            fs.too_big = true;
+            return true;
+        }
+    }
+    fs.ngroups = ng;
+    if (!upload(&fs.d_stream, stream) || !upload(&fs.d_off, off) || !upload(&fs.d_len, len)) return false;
+    fs.built = true;
+    return true;
+}
+
+// Schedule of the CTA-pair dense fprop/bprop (bs = 32): as build_fb_dense, for groups of 8
+// output blocks.  Entry: ((pair << 16) | mask), mask bit sub * 8 + out, then 16 words id + 1
+// in (sub, out) order; outputs 0-3 belong to the pair's even CTA, 4-7 to the odd one.
+constexpr int kFbpSchedWords = 3072;
+
+bool build_fb_dense_pair(bsmm_ctx *h, FbDenseSched &fs, bool bwd)
+{
+    const int Fout = bwd ? h->R : h->S, Fsrc = bwd ? h->S : h->R;
+    const int ng = (Fout + 7) / 8;
+    BidLookup bid{h};
+    std::vector<uint32_t> stream;
+    std::vector<int32_t> off(ng), len(ng);
+    for (int gi = 0; gi < ng; ++gi) {
+        off[gi] = (int32_t)stream.size();
+        for (int pr = 0; pr * 2 < Fsrc; ++pr) {
+            uint32_t mask = 0, ids[16];
+            for (int sub = 0; sub < 2; ++sub)
+                for (int o = 0; o < 8; ++o) {
+                    const int src = pr * 2 + sub, out = gi * 8 + o;
+                    int32_t b = -1;
+                    if (src < Fsrc && out < Fout) b = bwd ? bid(out, src) : bid(src, out);
+                    ids[sub * 8 + o] = (uint32_t)(b + 1);
+                    if (b >= 0) mask |= 1u << (sub * 8 + o);
+                }
+            if (!mask) continue;
+            stream.push_back(((uint32_t)pr << 16) | mask);
+            stream.insert(stream.end(), ids, ids + 16);
+        }
+        stream.push_back(0xFFFFFFFFu);
+        while (stream.size() % 4) stream.push_back(0);
+        len[gi] = (int32_t)(stream.size() - off[gi]);
+        if (len[gi] > kFbpSchedWords) {
             fs.too_big = true;
             return true;
         }
@@ -1411,6 +1453,224 @@ k_tc_fbd(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUt
     if (warp == kProducers) tmem_dealloc(tmem, 256);
 }
 
+// Dense-tile fprop / bprop on CTA pairs with two-SM MMAs, bs = 32.  A pair computes
+// D[256 output features][256 minibatch rows] for a group of 8 output blocks.  M = 256 is split
+// over the two CTAs' tensor memory (the even CTA holds the group's outputs 0-3, the odd one
+// 4-7); each CTA loads only its own 4 weight blocks per source (its half of A) and 128 of the
+// 256 activation rows (its half of B), and the even CTA issues M256 x N256 x K16 MMAs that
+// read both CTAs' shared memory.  Per pair of sources a CTA thus streams 32 KB instead of the
+// 48 KB of k_tc_fbd for the same MMA work per SM, which is what the L2 -> SM rate limits.
+//   Loads of both CTAs complete on the even CTA's `full` barrier (which expects both halves);
+//   the even CTA's commits release the stage in both CTAs and finally signal both
+//   accumulators.  Operand layouts per CTA are those of k_tc_fbd with 128 activation rows.
+template <int FA, bool BWD, bool BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFbThreads, 1)
+k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
+              const __grid_constant__ CUtensorMap tm_zero, const __grid_constant__ CUtensorMap tm_out,
+              const FbdParams p)
+{
+    constexpr int PROD = 3;                                      // producer warps; warp w owns stages w, w + 3
+    constexpr int STAGES = 6;
+    static_assert(STAGES % PROD == 0, "producer warp w must own stages w, w+PROD, ...");
+    constexpr int A_BYTES = 16384, B_BYTES = 16384, STAGE = A_BYTES + B_BYTES;
+    constexpr uint32_t A_LBO = BWD ? 16 : 2048, A_SBO = 512, A_KSTEP = BWD ? 32 : 1024;
+    constexpr uint32_t B_LBO = FA ? 16 : 8192, B_KSTEP = FA ? 32 : 2048, B_SUB = FA ? 64 : 4096;
+    constexpr uint32_t IDESC = idesc_f16(256, 256, BF16, !BWD, FA == 0);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t *sched = reinterpret_cast<const uint32_t *>(smem + STAGES * STAGE);
+    __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full, sched_full;
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int aborted;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int tile = blockIdx.x >> 1;
+    const int grp = tile / p.n_tiles;                            // group of 8 output blocks
+    const int n0 = (tile % p.n_tiles) * 256;
+    const int len = p.len[grp];
+
+    if (threadIdx.x == 0) {
+        aborted = 0;
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);                              // the even CTA's producer, + both halves' bytes
+            mbar_init(&empty[i], 1);                             // one commit of the even CTA's MMA warp
+        }
+        mbar_init(&acc_full, 1);
+        mbar_init(&sched_full, 1);
+        fence_barrier_init();
+    }
+    if (warp == kProducers) tmem_alloc_pair(&tmem_base, 256);
+    tc_fence_before();
+    cluster_sync();                                  // both CTAs' barriers and tensor memory exist
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    // Every CTA of this grid holds its tensor memory before a dependent kernel may start, so a
+    // dependent CTA that waits for it in tcgen05.alloc waits only on CTAs that will finish.
+    pdl_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
+        bulk_load((void *)sched, p.stream + p.off[grp], (uint32_t)len * 4u, &sched_full, policy_evict_last());
+        prefetch_tmap(&tm_act);
+        prefetch_tmap(&tm_w);
+    }
+    pdl_wait();
+    const uint32_t full0 = map_to_rank(smem_u32(&full[0]), 0);   // the even CTA's full[0]
+
+    if (warp < PROD) {
+        const uint64_t pol_act = policy_evict_last();
+        const uint64_t pol_w = policy_evict_first();
+        if (!mbar_wait_warp(&sched_full, 0, p.status, 64)) aborted = 1;
+        __syncwarp();
+        int last = -1;
+        for (int chunk = 0, pos = 0; !aborted; ++chunk, pos += 17) {
+            const uint32_t hdr = sched[pos];
+            if (hdr == 0xFFFFFFFFu) break;
+            if (chunk % PROD != warp) continue;
+            const int st = chunk % STAGES;
+            if (lane == 0) {
+                if (chunk >= STAGES && !mbar_wait(&empty[st], ((chunk / STAGES) - 1) & 1, p.status)) aborted = 1;
+                else if (rank == 0) mbar_arrive_expect_tx(&full[st], 2u * STAGE);
+            }
+            __syncwarp();
+            if (aborted) break;
+            last = chunk;
+            const int pr = (int)(hdr >> 16);
+            uint8_t *a = smem + st * STAGE;
+            uint8_t *b = a + A_BYTES;
+            const uint32_t fb = full0 + (uint32_t)st * 8u;
+            if (FA) {
+                if (lane == 0) tma_load_2d_pair(b, &tm_act, fb, pr * 64, n0 + 128 * (int)rank, pol_act);
+            } else {
+                if (lane < 2)
+                    tma_load_2d_pair(b + lane * 8192, &tm_act, fb, n0 + 128 * (int)rank + 64 * lane, pr * 64, pol_act);
+            }
+            if (lane >= 8 && lane < 16) {
+                const int sl = lane - 8, sub = sl >> 2, o = sl & 3;
+                const int id = (int)sched[pos + 1 + sub * 8 + (int)rank * 4 + o] - 1;
+                uint8_t *d = a + sub * 8192 + o * 2048;
+                if (id >= 0) {
+                    tma_load_2d_pair(d, &tm_w, fb, 0, id * 32, pol_w);
+                } else {
+                    const int zr = (int)((blockIdx.x * 13u + (unsigned)chunk * 8u + (unsigned)sl) % 128u) * 32;
+                    tma_load_2d_pair(d, &tm_zero, fb, 0, zr, pol_w);
+                }
+            }
+        }
+        // The last release of this warp's stages comes from the even CTA's MMA warp: waiting for
+        // it means no commit of the peer is still on its way to this CTA when it exits.
+        if (!aborted && lane == 0 && last >= 0) {
+            mbar_wait(&empty[last % STAGES], (last / STAGES) & 1, p.status);
+            if (last >= PROD) mbar_wait(&empty[(last - PROD) % STAGES], ((last - PROD) / STAGES) & 1, p.status);
+        }
+        __syncwarp();
+    } else if (warp == kProducers) {
+        if (rank == 0 && elect_one()) {
+            const uint32_t s_base = smem_u32(smem);
+            const uint64_t a_desc0 = sdesc(s_base, A_LBO, A_SBO, SW_64);
+            const uint64_t b_desc0 = sdesc(s_base + A_BYTES, B_LBO, 1024, SW_128);
+            uint32_t acc = 0;
+            if (!mbar_wait(&sched_full, 0, p.status)) aborted = 1;
+            for (int chunk = 0, pos = 0; !aborted; ++chunk, pos += 17) {
+                const uint32_t hdr = sched[pos];
+                if (hdr == 0xFFFFFFFFu) break;
+                const int st = chunk % STAGES;
+                if (!mbar_wait(&full[st], (chunk / STAGES) & 1, p.status)) {
+                    aborted = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t so = st * STAGE;
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub) {
+                    if (!((hdr >> (sub * 8)) & 0xFFu)) continue;  // no block of this source in the group
+                    const uint64_t ad = a_desc0 + ((so + sub * 8192) >> 4);
+                    const uint64_t bd = b_desc0 + ((so + sub * B_SUB) >> 4);
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        mma_pair_ss(tmem, ad + ((ks * A_KSTEP) >> 4), bd + ((ks * B_KSTEP) >> 4), IDESC, acc);
+                        acc = 1;
+                    }
+                }
+                mma_pair_commit_mc(&empty[st], 3);        // releases the stage in both CTAs
+            }
+            mma_pair_commit_mc(&acc_full, 3);
+        }
+        __syncwarp();
+    }
+    if (warp < kProducers) {
+        // epilogue: warp q holds output features 32q..32q+31 of this CTA's half, lane = feature
+        const int q = warp & 3;
+        const int fbase = grp * 256 + (int)rank * 128;
+        const int f = fbase + q * 32 + lane;
+        const bool ok = mbar_wait_warp(&acc_full, 0, p.status, 256);
+        tc_fence_after();
+        const bool any = len > 4;                     // at least one entry (else the stream is the end marker)
+        uint16_t *out = static_cast<uint16_t *>(p.out);
+        uint16_t *tile_s = reinterpret_cast<uint16_t *>(smem);
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+            if (!FA && n0 + c0 >= p.N) break;
+            float v[32];
+            if (ok && any) {
+#pragma unroll
+                for (int h2 = 0; h2 < 32; h2 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0 + h2, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[h2 + j] = __uint_as_float(r[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            if (FA) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) tile_s[(c0 + j) * 128 + q * 32 + lane] = cvt1<BF16>(v[j]);
+                continue;
+            }
+            if (f >= p.Fout) continue;
+            const int nb = n0 + c0;
+            uint16_t *dst = out + (size_t)f * p.N + nb;
+            if (nb + 32 <= p.N) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                    uint4 pk;
+                    pk.x = pack2<BF16>(v[j], v[j + 1]);
+                    pk.y = pack2<BF16>(v[j + 2], v[j + 3]);
+                    pk.z = pack2<BF16>(v[j + 4], v[j + 5]);
+                    pk.w = pack2<BF16>(v[j + 6], v[j + 7]);
+                    *reinterpret_cast<uint4 *>(dst + j) = pk;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (nb + j < p.N) dst[j] = cvt1<BF16>(v[j]);
+            }
+        }
+        if (FA) {
+            fence_proxy_async_smem();
+            named_sync(1, 32 * kProducers);
+            if (warp == 0 && lane == 0) {
+                tma_store_2d(&tm_out, tile_s, fbase, n0);
+                bulk_commit();
+                bulk_wait_read();
+            }
+        }
+    }
+    if (aborted) {
+        // copies of the pair may still be landing in this CTA: give them time (bounded)
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 20000u) __nanosleep(1000);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                                  // both CTAs are done with the pair's tensor memory
+    if (warp == kProducers) tmem_dealloc_pair(tmem, 256);
+}
+
 // Dense-tile fprop / bprop for a minibatch of at most 64 rows, bs = 32.  Same tiles and
 // operands as k_tc_fbd with N = 64, but a 64-row minibatch gives too few tiles to fill the
 // GPU, so a cluster of kSplit CTAs shares one tile: CTA r multiplies the r-th quarter of the
@@ -1869,6 +2129,46 @@ bsmm_status launch_fbd(bsmm_ctx *h, FbDenseSched &fs, const void *act, const voi
 }
 
 template <int FA, bool BWD, bool BF16>
+bsmm_status launch_fbd_pair(bsmm_ctx *h, FbDenseSched &fs, const void *act, const void *w, void *out, int N,
+                            bsmm_dtype t, cudaStream_t s)
+{
+    TcState *st = state(h);
+    const int C = h->R * 32, K = h->S * 32;
+    const int Fin = BWD ? K : C, Fout = BWD ? C : K;
+    CUtensorMap m_act, m_w, m_zero, m_out;
+    bool ok;
+    // this CTA's half panel: 128 minibatch rows x 64 features, or 64 features x 64 minibatch columns
+    if (FA) ok = make_map2d(&m_act, act, t, Fin, N, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    else ok = make_map2d(&m_act, act, t, N, Fin, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map2d(&m_w, w, t, 32, (uint64_t)h->nnz * 32, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok = ok && make_map2d(&m_zero, st->d_zero, t, 32, kZeroBytes / 64, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (FA) ok = ok && make_map2d(&m_out, out, t, Fout, N, 128, 256, CU_TENSOR_MAP_SWIZZLE_NONE);
+    else m_out = m_act;                                  // unused for (C,N) outputs
+    if (!ok) return BSMM_ERR_CUDA;
+    FbdParams p = {};
+    p.out = out;
+    p.stream = fs.d_stream;
+    p.off = fs.d_off;
+    p.len = fs.d_len;
+    p.status = h->d_status;
+    p.N = N;
+    p.Fout = Fout;
+    p.n_tiles = (N + 255) / 256;
+    const int smem = 6 * (16384 + 16384) + kFbpSchedWords * 4 + 1024;
+    auto kern = k_tc_fbd_pair<FA, BWD, BF16>;
+    static std::atomic<int> attr_set{-1};
+    if (attr_set.load() != h->device) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return BSMM_ERR_CUDA;
+        attr_set.store(h->device);
+    }
+    const cudaError_t le = launch_pdl(kern, dim3(fs.ngroups * p.n_tiles * 2), dim3(kFbThreads), smem, s, true, m_act,
+                                      m_w, m_zero, m_out, p);
+    g_bsmm_launches += 1;
+    return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+}
+
+template <int FA, bool BWD, bool BF16>
 bsmm_status launch_fbd_split(bsmm_ctx *h, FbDenseSched &fs, const void *act, const void *w, void *out, int N,
                              bsmm_dtype t, cudaStream_t s)
 {
@@ -1914,9 +2214,11 @@ bsmm_status fbd_try(bsmm_ctx *h, const void *act, const void *w, void *out, int 
     if (h->bs != 32 || h->nnz == 0) return BSMM_ERR_UNSUPPORTED;
     const double density = (double)h->nnz / ((double)h->R * h->S);
     bool dense = density >= 0.25 && (N > 128 || N <= 64);
+    bool pair = N > 64;                              // CTA-pair kernel unless one 64-row tile
     if (const char *e = getenv("BSMM_TC_FB")) {
         if (!strcmp(e, "window")) dense = false;
         if (!strcmp(e, "dense")) dense = true;
+        if (!strcmp(e, "dense1")) dense = true, pair = false;
     }
     if (!dense) return BSMM_ERR_UNSUPPORTED;
     TcState *st = state(h);
@@ -1927,9 +2229,16 @@ bsmm_status fbd_try(bsmm_ctx *h, const void *act, const void *w, void *out, int 
             if (cudaMalloc(&st->d_zero, kZeroBytes) != cudaSuccess) return BSMM_ERR_OOM;
             if (cudaMemset(st->d_zero, 0, kZeroBytes) != cudaSuccess) return BSMM_ERR_CUDA;
         }
+        if (pair) {
+            if (!st->fbd[2 + BWD]) st->fbd[2 + BWD] = new FbDenseSched();
+            FbDenseSched *fp = st->fbd[2 + BWD];
+            if (!fp->built && !fp->too_big && !build_fb_dense_pair(h, *fp, BWD)) return BSMM_ERR_OOM;
+            if (!fp->built) pair = false;                // schedule too long: single-CTA tiles
+        }
         if (!st->fbd[BWD]) st->fbd[BWD] = new FbDenseSched();
         fs = st->fbd[BWD];
-        if (!fs->built && !fs->too_big && !build_fb_dense(h, *fs, BWD)) return BSMM_ERR_OOM;
+        if (!pair && !fs->built && !fs->too_big && !build_fb_dense(h, *fs, BWD)) return BSMM_ERR_OOM;
+        if (pair) fs = st->fbd[2 + BWD];
     }
     if (!fs->built) return BSMM_ERR_UNSUPPORTED;
     const bool bf = t == BSMM_BF16;
@@ -1939,6 +2248,12 @@ bsmm_status fbd_try(bsmm_ctx *h, const void *act, const void *w, void *out, int 
                              : launch_fbd_split<1, BWD, false>(h, *fs, act, w, out, N, t, s);
         return bf ? launch_fbd_split<0, BWD, true>(h, *fs, act, w, out, N, t, s)
                   : launch_fbd_split<0, BWD, false>(h, *fs, act, w, out, N, t, s);
+    }
+    if (pair) {
+        if (h->fa) return bf ? launch_fbd_pair<1, BWD, true>(h, *fs, act, w, out, N, t, s)
+                             : launch_fbd_pair<1, BWD, false>(h, *fs, act, w, out, N, t, s);
+        return bf ? launch_fbd_pair<0, BWD, true>(h, *fs, act, w, out, N, t, s)
+                  : launch_fbd_pair<0, BWD, false>(h, *fs, act, w, out, N, t, s);
     }
     if (h->fa) return bf ? launch_fbd<1, BWD, true>(h, *fs, act, w, out, N, t, s)
                          : launch_fbd<1, BWD, false>(h, *fs, act, w, out, N, t, s);

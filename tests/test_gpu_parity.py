@@ -353,13 +353,14 @@ def test_updat_variants_bs32(monkeypatch, variant, fa, p, G):
 
 @pytest.mark.parametrize("fa,dtype", [(1, "bf16"), (0, "f16")])
 @pytest.mark.parametrize("R,S,p,N", [(10, 13, 0.5, 392), (7, 9, 0.9, 264), (12, 6, 0.3, 136),
-                                     (10, 13, 0.5, 64), (9, 7, 0.8, 40)])
+                                     (20, 37, 0.5, 520), (10, 13, 0.5, 64), (9, 7, 0.8, 40)])
 def test_fprop_bprop_variants_bs32(monkeypatch, fa, dtype, R, S, p, N):
-    """Both tensor-core fprop/bprop schemes (windows of output blocks over 128-row tiles,
-    or dense 4-block x 256-row tiles with absent blocks as zero tiles; for a minibatch of
-    at most 64 rows the dense tiles are split over a cluster of 4 CTAs and summed in
-    distributed shared memory) against the oracle, on layouts whose block counts are not
-    multiples of the tile and a ragged minibatch."""
+    """The tensor-core fprop/bprop schemes against the oracle: windows of output blocks over
+    128-row tiles; dense tiles of 4 output blocks x 256 rows with absent blocks as zero tiles
+    on one CTA ("dense1"); dense tiles of 8 output blocks x 256 rows on a CTA pair with
+    two-SM MMAs ("dense"; for a minibatch of at most 64 rows the dense tile is instead split
+    over a cluster of 4 CTAs and summed in distributed shared memory).  Layouts whose block
+    counts are not multiples of the tile, and ragged minibatches."""
     bs = 32
     L = rand_layout(R, S, p, R * 31 + S)
     L[:, 2] = 0                                           # an empty output block column
@@ -370,7 +371,7 @@ def test_fprop_bprop_variants_bs32(monkeypatch, fa, dtype, R, S, p, N):
     w = wk.normals((nnz, bs, bs), 900 + R + S, float(1 / np.sqrt(R * bs * p)), dtype)
     ref_y, ref_dx = o.fprop(L, bs, x, w, fa), o.bprop(L, bs, dy, w, fa)
     outs = {}
-    for variant in ("window", "dense"):
+    for variant in ("window", "dense1", "dense"):
         monkeypatch.setenv("BSMM_TC_FB", variant)
         m = make(L, bs, fa, "auto")
         y = torch.full(m.o_shape(N), float("nan"), dtype=DT[dtype], device="cuda")
@@ -384,3 +385,6 @@ def test_fprop_bprop_variants_bs32(monkeypatch, fa, dtype, R, S, p, N):
     # both schemes accumulate in fp32 and round once: they agree to a few output ulps
     for a, b in zip(outs["window"], outs["dense"]):
         assert rel_fro(a, b) <= TIGHT[dtype]
+    # one-CTA and CTA-pair dense tiles add the same products in the same order
+    for a, b in zip(outs["dense1"], outs["dense"]):
+        assert np.array_equal(a, b)
