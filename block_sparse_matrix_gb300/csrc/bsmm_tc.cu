@@ -90,6 +90,7 @@ struct TcState {
     std::map<uint64_t, FbSched> fb;   // key: pass, window log2, chunk entries, chunk records
     UpSched up;
     struct UpDenseSched *upd = nullptr;
+    struct UpPairSched *upp = nullptr;
     struct FbDenseSched *fbd[4] = {};   // dense-tile fprop / bprop; + 2: CTA-pair schedules
     void *d_zero = nullptr;   // zero buffer: 8x8 zero tiles for absent sub-blocks of 16x16 coarse blocks
     std::mutex mu;
@@ -377,6 +378,93 @@ bool build_up_dense(bsmm_ctx *h, UpDenseSched &us)
         std::copy(units[u].begin(), units[u].end(), t + 4 + i * kDUnitWords);
     }
     us.ctas = nunits ? ctas : 0;
+    if (!upload(&us.d_table, table)) return false;
+    us.built = true;
+    return true;
+}
+
+// Schedule of the CTA-pair weight gradient (bs = 32): units are 256 x 256 tiles of x^T.dy
+// (8 block rows x 8 block columns) with at least one block, dealt round-robin to the pairs.
+// When the last round would leave most pairs idle (at most half of them busy), its tiles are
+// split into two 256 x 128 units (nk = 4) so the tail is spread over twice as many pairs.
+// Per pair: word 0 = number of units; unit u at 4 + u * kPUnitWords: c0, k0, nk, count, then
+// count words ((c_sub * 8 + k_sub) << 24) | block id.
+constexpr int kPUnitWords = 68;
+constexpr int kPUnitsPerPair = 48;
+constexpr int kPTableWords = 4 + kPUnitsPerPair * kPUnitWords;
+
+struct UpPairSched {
+    int ctas = 0;
+    int32_t *d_table = nullptr;
+    bool built = false, too_big = false;
+};
+
+bool build_up_pair(bsmm_ctx *h, UpPairSched &us)
+{
+    const int Rt = (h->R + 7) / 8, St = (h->S + 7) / 8;
+    std::vector<std::vector<int32_t>> tiles;
+    for (int tc = 0; tc < Rt; ++tc)
+        for (int tk = 0; tk < St; ++tk) {
+            std::vector<int32_t> u(kPUnitWords, 0);
+            int n = 0;
+            for (int cs = 0; cs < 8; ++cs) {
+                const int c = tc * 8 + cs;
+                if (c >= h->R) break;
+                const int32_t *b = h->h_row_ent.data() + h->h_row_ptr[c];
+                const int32_t *e = h->h_row_ent.data() + h->h_row_ptr[c + 1];
+                for (const int32_t *q = std::lower_bound(b, e, tk * 8); q != e && *q < tk * 8 + 8; ++q) {
+                    const int32_t id = h->h_row_ptr[c] + (int32_t)(q - b);
+                    u[4 + n++] = ((cs * 8 + (*q - tk * 8)) << 24) | id;
+                }
+            }
+            if (!n) continue;
+            u[0] = tc * 8;
+            u[1] = tk * 8;
+            u[2] = 8;
+            u[3] = n;
+            tiles.push_back(u);
+        }
+    const int P = std::max(1, h->sm_count / 2);
+    const int T = (int)tiles.size();
+    const int full_rounds = T / P, rem = T - full_rounds * P;
+    std::vector<std::vector<int32_t>> units(tiles.begin(), tiles.begin() + (size_t)full_rounds * P);
+    for (int i = full_rounds * P; i < T; ++i) {
+        const std::vector<int32_t> &t = tiles[i];
+        if (full_rounds > 0 && 2 * rem <= P) {
+            for (int half = 0; half < 2; ++half) {                 // block columns k0 + 4 half .. + 3
+                std::vector<int32_t> u(kPUnitWords, 0);
+                int n = 0;
+                for (int e = 0; e < t[3]; ++e) {
+                    const int ks = (t[4 + e] >> 24) & 7;
+                    if ((ks >> 2) != half) continue;
+                    const int cs = t[4 + e] >> 27;
+                    u[4 + n++] = ((cs * 8 + (ks & 3)) << 24) | (t[4 + e] & 0xFFFFFF);
+                }
+                if (!n) continue;
+                u[0] = t[0];
+                u[1] = t[1] + 4 * half;
+                u[2] = 4;
+                u[3] = n;
+                units.push_back(u);
+            }
+        } else {
+            units.push_back(t);
+        }
+    }
+    const int nunits = (int)units.size();
+    const int pairs = std::max(1, std::min(nunits, P));
+    if ((nunits + pairs - 1) / pairs > kPUnitsPerPair) {
+        us.too_big = true;
+        return true;
+    }
+    std::vector<int32_t> table((size_t)pairs * kPTableWords, 0);
+    for (int u = 0; u < nunits; ++u) {
+        const int b = u % pairs, i = u / pairs;
+        int32_t *t = table.data() + (size_t)b * kPTableWords;
+        t[0] = i + 1;
+        std::copy(units[u].begin(), units[u].end(), t + 4 + i * kPUnitWords);
+    }
+    us.ctas = nunits ? 2 * pairs : 0;
     if (!upload(&us.d_table, table)) return false;
     us.built = true;
     return true;
@@ -1244,6 +1332,230 @@ k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
     if (warp == kProducers) tmem_dealloc(tmem, 512);
 }
 
+// Weight gradient on CTA pairs with two-SM MMAs, bs = 32.  A unit is a 256 x (32 nk) tile of
+// x^T.dy (nk = 8, or 4 for split tail units): block rows c0..c0+7 by block columns
+// k0..k0+nk-1, reduced over the minibatch in stages of 64 rows.  The even CTA holds tile rows
+// 0-127 (block rows c0..c0+3) in its tensor memory, the odd CTA rows 128-255; each CTA loads
+// its 128-feature slice of x (its half of A) and 128 dy features (its half of B, of which the
+// MMA uses nk * 16), and the even CTA issues M256 x N x K16 MMAs over both CTAs' shared memory:
+// 32 KB per CTA per stage for the MMA work that k_tc_updat_dense feeds with 48 KB.
+// Accumulators are double-buffered (2 x 256 columns per CTA); the epilogue warps of both CTAs
+// release a buffer to the even CTA's MMA warp, and epilogue warp q writes the present blocks
+// of block row c0 + 4 rank + q with coalesced stores.
+struct UpPairGeo {
+    static constexpr int TK = 64;
+    static constexpr int A_BYTES = 128 * TK * 2;                     // 16 KB
+    static constexpr int B_BYTES = 128 * TK * 2;                     // 16 KB
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int PROD = 3;                                   // producer warps; warp w owns stages w, w + 3
+    static constexpr int STAGES = 6;
+    static constexpr int TAB_OFF = STAGES * STAGE;
+    static constexpr int OUT_OFF = (TAB_OFF + kPTableWords * 4 + 127) / 128 * 128;
+    static constexpr int SMEM = OUT_OFF + 4 * 32 * 32 * 4;           // + a 32 x 32 fp32 block per epilogue warp
+};
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+template <int FA, bool BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kUpThreads, 1)
+k_tc_updat_pair(const __grid_constant__ UpMaps maps, const UpParams p)
+{
+    using G = UpPairGeo;
+    static_assert(G::STAGES % G::PROD == 0, "producer warp w must own stages w, w+PROD, ...");
+    // fa=1: A = x^T MN-major (M atoms of 64 at 8 KB), B = dy MN-major (N atoms of 64 at 8 KB);
+    // fa=0: both K-major, 128-byte rows.
+    constexpr uint32_t A_LBO = FA ? 8192 : 16, B_LBO = FA ? 8192 : 16;
+    constexpr uint32_t KSTEP = FA ? 16 * 128 : 32;
+    constexpr uint32_t IDESC8 = idesc_f16(256, 256, BF16, FA == 1, FA == 1);
+    constexpr uint32_t IDESC4 = idesc_f16(256, 128, BF16, FA == 1, FA == 1);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int32_t *tab = reinterpret_cast<int32_t *>(smem + G::TAB_OFF);
+    float *sout = reinterpret_cast<float *>(smem + G::OUT_OFF);
+    __shared__ __align__(8) uint64_t full[G::STAGES], empty[G::STAGES], acc_full[2], acc_empty[2], tab_full;
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int aborted;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1;
+    const int chunks = (p.N + G::TK - 1) / G::TK;
+    const int total = chunks * p.G;
+
+    if (threadIdx.x == 0) {
+        aborted = 0;
+        for (int i = 0; i < G::STAGES; ++i) {
+            mbar_init(&full[i], 1);                              // the even CTA's producer, + both halves' bytes
+            mbar_init(&empty[i], 1);                             // one commit of the even CTA's MMA warp
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 8);                         // 4 epilogue warps in each CTA
+        }
+        mbar_init(&tab_full, 1);
+        fence_barrier_init();
+    }
+    if (warp == kProducers) tmem_alloc_pair(&tmem_base, 512);
+    tc_fence_before();
+    cluster_sync();                                  // both CTAs' barriers and tensor memory exist
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    // Every CTA of this grid holds its tensor memory before a dependent kernel may start, so a
+    // dependent CTA that waits for it in tcgen05.alloc waits only on CTAs that will finish.
+    pdl_launch_dependents();
+    const int32_t *gtab = p.table + (size_t)pair * kPTableWords;
+    if (warp == 0 && lane == 0) {
+        const int nu = gtab[0];
+        const uint32_t bytes = (uint32_t)(4 + nu * kPUnitWords) * 4u;
+        mbar_arrive_expect_tx(&tab_full, bytes);
+        bulk_load(tab, gtab, bytes, &tab_full, policy_evict_first());
+    }
+    pdl_wait();
+    const bool tab_ok = mbar_wait_warp(&tab_full, 0, p.status, 64);
+    const int nunits = tab_ok ? tab[0] : 0;
+    const uint32_t full0 = map_to_rank(smem_u32(&full[0]), 0);       // the even CTA's barriers
+    const uint32_t acc_empty0 = map_to_rank(smem_u32(&acc_empty[0]), 0);
+
+    if (warp < G::PROD) {
+        const uint64_t pol = policy_evict_last();
+        int it = 0, last = -1;
+        for (int u = 0; u < nunits && !aborted; ++u) {
+            const int32_t *ut = tab + 4 + u * kPUnitWords;
+            const int nk = ut[2];
+            const int f_c = ut[0] * 32 + (int)rank * 128;         // this CTA's 128 tile rows
+            const int f_k = ut[1] * 32 + (int)rank * nk * 16;     // this CTA's half of the tile columns
+            for (int c = 0; c < total; ++c, ++it) {
+                if (it % G::PROD != warp) continue;
+                const int t = c / chunks, n0 = (c % chunks) * G::TK;
+                const int s = it % G::STAGES;
+                if (lane == 0) {
+                    if (it >= G::STAGES && !mbar_wait(&empty[s], ((it / G::STAGES) - 1) & 1, p.status)) aborted = 1;
+                    else if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * G::STAGE);
+                }
+                __syncwarp();
+                if (aborted) break;
+                last = it;
+                uint8_t *a = smem + s * G::STAGE;
+                uint8_t *b = a + G::A_BYTES;
+                const uint32_t fb = full0 + (uint32_t)s * 8u;
+                if (FA) {
+                    if (lane < 2) tma_load_2d_pair(a + lane * 8192, &maps.x[t], fb, f_c + lane * 64, n0, pol);
+                    else if (lane < 4)
+                        tma_load_2d_pair(b + (lane - 2) * 8192, &maps.dy[t], fb, f_k + (lane - 2) * 64, n0, pol);
+                } else {
+                    if (lane == 0) tma_load_2d_pair(a, &maps.x[t], fb, n0, f_c, pol);
+                    else if (lane == 1) tma_load_2d_pair(b, &maps.dy[t], fb, n0, f_k, pol);
+                }
+            }
+        }
+        // The last release of this warp's stages comes from the even CTA's MMA warp: waiting for
+        // it means no commit of the peer is still on its way to this CTA when it exits.
+        if (!aborted && lane == 0 && last >= 0) {
+            mbar_wait(&empty[last % G::STAGES], (last / G::STAGES) & 1, p.status);
+            if (last >= G::PROD)
+                mbar_wait(&empty[(last - G::PROD) % G::STAGES], ((last - G::PROD) / G::STAGES) & 1, p.status);
+        }
+        __syncwarp();
+    } else if (warp == kProducers) {
+        if (rank == 0 && elect_one()) {
+            const uint64_t a_desc0 = sdesc(smem_u32(smem), A_LBO, 1024, SW_128);
+            const uint64_t b_desc0 = sdesc(smem_u32(smem) + G::A_BYTES, B_LBO, 1024, SW_128);
+            int it = 0;
+            for (int u = 0; u < nunits && !aborted; ++u) {
+                const int buf = u & 1;
+                const uint32_t idesc = tab[4 + u * kPUnitWords + 2] == 8 ? IDESC8 : IDESC4;
+                if (u >= 2 && !mbar_wait(&acc_empty[buf], ((u >> 1) - 1) & 1, p.status)) {
+                    aborted = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + buf * 256;
+                for (int c = 0; c < total; ++c, ++it) {
+                    const int s = it % G::STAGES;
+                    if (!mbar_wait(&full[s], (it / G::STAGES) & 1, p.status)) {
+                        aborted = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = a_desc0 + ((s * G::STAGE) >> 4);
+                    const uint64_t bd = b_desc0 + ((s * G::STAGE) >> 4);
+#pragma unroll
+                    for (int ks = 0; ks < G::TK / 16; ++ks)
+                        mma_pair_ss(d, ad + ((ks * KSTEP) >> 4), bd + ((ks * KSTEP) >> 4), idesc,
+                                    (c > 0 || ks > 0) ? 1u : 0u);
+                    mma_pair_commit_mc(&empty[s], 3);             // releases the stage in both CTAs
+                }
+                mma_pair_commit_mc(&acc_full[buf], 3);
+            }
+        }
+        __syncwarp();
+    } else if (warp > kProducers) {
+        const int q = warp & 3;                  // TMEM lane quarter = block row c0 + 4 rank + q
+        const int row = (int)rank * 4 + q;
+        for (int u = 0; u < nunits; ++u) {
+            const int buf = u & 1;
+            const bool ok = mbar_wait_warp(&acc_full[buf], (u >> 1) & 1, p.status, 128);
+            if (!ok) break;
+            tc_fence_after();
+            const int32_t *ut = tab + 4 + u * kPUnitWords;
+            const int cnt = ut[3];
+            for (int e = 0; e < cnt; ++e) {
+                const uint32_t wd = (uint32_t)ut[4 + e];
+                const int sub = (int)(wd >> 24), id = (int)(wd & 0xFFFFFFu);
+                if ((sub >> 3) != row) continue;
+                float v[32];
+#pragma unroll
+                for (int c0 = 0; c0 < 32; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + (sub & 7) * 32 + c0, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[c0 + j] = __uint_as_float(r[j]);
+                }
+                // through shared memory so that each store writes 512 contiguous bytes of the block;
+                // 16-byte chunk c of row r sits at chunk c ^ (r mod 8) (conflict-free both ways)
+                float *stg = sout + q * 32 * 32;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4 *>(stg + lane * 32 + ((c ^ (lane & 7)) * 4)) =
+                        make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
+                __syncwarp();
+                if (!aborted) {
+                    float *blk = p.dw + (size_t)id * 1024;
+#pragma unroll
+                    for (int k4 = 0; k4 < 8; ++k4) {
+                        const int o = k4 * 128 + lane * 4, r = o / 32, c = (o % 32) / 4;
+                        float4 r4 = *reinterpret_cast<const float4 *>(stg + r * 32 + ((c ^ (r & 7)) * 4));
+                        if (p.accumulate) {
+                            const float4 a = *reinterpret_cast<const float4 *>(blk + o);
+                            r4.x += a.x; r4.y += a.y; r4.z += a.z; r4.w += a.w;
+                        }
+                        *reinterpret_cast<float4 *>(blk + o) = r4;
+                    }
+                }
+                __syncwarp();                                   // reads done before the next block's writes
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty0 + (uint32_t)buf * 8u);
+        }
+    }
+    if (aborted) {
+        // copies of the pair may still be landing in this CTA: give them time (bounded)
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 20000u) __nanosleep(1000);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                                  // both CTAs are done with the pair's tensor memory
+    if (warp == kProducers) tmem_dealloc_pair(tmem, 512);
+}
+
 // Dense-tile fprop / bprop, bs = 32.  A CTA computes D[128 output features][256 minibatch
 // rows] for a group of 4 output blocks: D += A[128 x 32] . B[32 x 256] for each present
 // source block, A being the group's 4 weight blocks of that source (absent ones are zero
@@ -2088,6 +2400,45 @@ bsmm_status launch_up_dense(bsmm_ctx *h, UpDenseSched &us, const GroupPtrs &g, f
     return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
+template <int FA, bool BF16>
+bsmm_status launch_up_pair(bsmm_ctx *h, UpPairSched &us, const GroupPtrs &g, float *dw, int N, bsmm_dtype t,
+                           int acc, cudaStream_t s)
+{
+    using G = UpPairGeo;
+    const int C = h->R * 32, K = h->S * 32;
+    UpMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    for (int i = 0; i < g.G; ++i) {
+        bool ok;
+        if (FA) {
+            ok = make_map2d(&maps.x[i], g.x[i], t, C, N, 64, G::TK, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 make_map2d(&maps.dy[i], g.dy[i], t, K, N, 64, G::TK, CU_TENSOR_MAP_SWIZZLE_128B);
+        } else {
+            ok = make_map2d(&maps.x[i], g.x[i], t, N, C, G::TK, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 make_map2d(&maps.dy[i], g.dy[i], t, N, K, G::TK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        }
+        if (!ok) return BSMM_ERR_CUDA;
+    }
+    UpParams p;
+    p.dw = dw;
+    p.table = us.d_table;
+    p.status = h->d_status;
+    p.N = N;
+    p.G = g.G;
+    p.accumulate = acc;
+    const int smem = G::SMEM + 1024;
+    auto kern = k_tc_updat_pair<FA, BF16>;
+    static std::atomic<int> attr_set{-1};
+    if (attr_set.load() != h->device) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return BSMM_ERR_CUDA;
+        attr_set.store(h->device);
+    }
+    const cudaError_t le = launch_pdl(kern, dim3(us.ctas), dim3(kUpThreads), smem, s, true, maps, p);
+    g_bsmm_launches += 1;
+    return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+}
+
 template <int FA, bool BWD, bool BF16>
 bsmm_status launch_fbd(bsmm_ctx *h, FbDenseSched &fs, const void *act, const void *w, void *out, int N,
                        bsmm_dtype t, cudaStream_t s)
@@ -2365,9 +2716,25 @@ bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dty
     // the minibatch spans two or more 64-row stages (BSMM_TC_UPDAT=stack / dense overrides).
     const double density = (double)h->nnz / ((double)h->R * h->S);
     bool dense = h->bs == 32 && density >= 0.25 && N * g.G > 64 && h->nnz < (1 << 24);
+    bool pair = true;                                // CTA-pair tiles unless the table does not fit
     if (const char *e = getenv("BSMM_TC_UPDAT")) {
         if (!strcmp(e, "stack")) dense = false;
         if (!strcmp(e, "dense")) dense = h->bs == 32 && h->nnz < (1 << 24);
+        if (!strcmp(e, "dense1")) dense = h->bs == 32 && h->nnz < (1 << 24), pair = false;
+    }
+    if (dense && pair) {
+        {
+            std::lock_guard<std::mutex> lk(st->mu);
+            if (!st->upp) st->upp = new UpPairSched();
+            if (!st->upp->built && !st->upp->too_big && !build_up_pair(h, *st->upp)) return BSMM_ERR_OOM;
+        }
+        if (st->upp->built) {
+            if (st->upp->ctas == 0) return BSMM_OK;
+            if (h->fa) return bf ? launch_up_pair<1, true>(h, *st->upp, g, dw, N, t, accumulate, s)
+                                 : launch_up_pair<1, false>(h, *st->upp, g, dw, N, t, accumulate, s);
+            return bf ? launch_up_pair<0, true>(h, *st->upp, g, dw, N, t, accumulate, s)
+                      : launch_up_pair<0, false>(h, *st->upp, g, dw, N, t, accumulate, s);
+        }
     }
     if (dense) {
         {
@@ -2416,6 +2783,10 @@ void tc_release(bsmm_ctx *h)
     if (st->upd) {
         cudaFree(st->upd->d_table);
         delete st->upd;
+    }
+    if (st->upp) {
+        cudaFree(st->upp->d_table);
+        delete st->upp;
     }
     for (auto *f : st->fbd)
         if (f) {

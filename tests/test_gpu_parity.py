@@ -325,13 +325,14 @@ def test_bounded_wait_times_out_and_context_survives():
     m.sync_status()
 
 
-@pytest.mark.parametrize("variant", ["stack", "dense"])
+@pytest.mark.parametrize("variant", ["stack", "dense1", "dense"])
 @pytest.mark.parametrize("fa", [0, 1])
 @pytest.mark.parametrize("p,G", [(0.5, 1), (0.2, 3), (0.9, 8)])
 def test_updat_variants_bs32(monkeypatch, variant, fa, p, G):
-    """Both tensor-core weight-gradient schemes (blocks of a column stacked along M, or dense
-    128x256 tiles of x^T.dy with the present blocks extracted) against the oracle, on
-    ragged layouts (R, S not multiples of the tile) and a ragged minibatch."""
+    """The tensor-core weight-gradient schemes against the oracle: blocks of a column stacked
+    along M ("stack"), dense 128x256 tiles of x^T.dy on one CTA ("dense1"), dense 256x256
+    tiles on a CTA pair with two-SM MMAs ("dense"), the present blocks extracted; ragged
+    layouts (R, S not multiples of the tile) and a ragged minibatch."""
     monkeypatch.setenv("BSMM_TC_UPDAT", variant)
     bs, R, S, N = 32, 10, 13, 136
     L = rand_layout(R, S, p, 17 + G)
@@ -349,6 +350,25 @@ def test_updat_variants_bs32(monkeypatch, variant, fa, p, G):
         dw1 = m.updat(xs[0].cuda(), dys[0].cuda())
         m.sync_status()
         assert rel_fro(cpu64(dw1), o.updat(L, bs, xs[0], dys[0], fa)) <= TOL_DW["bf16"]
+
+
+@pytest.mark.parametrize("fa", [0, 1])
+def test_updat_pair_tail_split(monkeypatch, fa):
+    """A layout with more 256x256 tiles than CTA pairs, so the last round of tiles is split
+    into 256x128 units: the CTA-pair kernel equals the one-CTA dense kernel bit for bit (same
+    products, same order) and the oracle within tolerance."""
+    bs, R, S, N = 32, 72, 72, 136
+    L = rand_layout(R, S, 0.5, 31 + fa)
+    x = wk.normals(wk.act_shape(R * bs, N, fa), 900 + fa, 1.0, "bf16")
+    dy = wk.normals(wk.act_shape(S * bs, N, fa), 910 + fa, 1.0, "bf16")
+    outs = {}
+    for variant in ("dense1", "dense"):
+        monkeypatch.setenv("BSMM_TC_UPDAT", variant)
+        m = make(L, bs, fa, "auto")
+        outs[variant] = cpu64(m.updat(x.cuda(), dy.cuda()))
+        m.sync_status()
+    assert np.array_equal(outs["dense1"], outs["dense"])
+    assert rel_fro(outs["dense"], o.updat(L, bs, x, dy, fa)) <= TOL_DW["bf16"]
 
 
 @pytest.mark.parametrize("fa,dtype", [(1, "bf16"), (0, "f16")])
