@@ -10,9 +10,12 @@ device time of the step.
 Timing: W warm-up steps, then exactly K timed steps.  Four input/output sets
 (each ~83 MB, together > 2x the 129 MB L2) rotate between steps, so every step
 reads cold inputs.  Steps are enqueued in chunks behind a short device sleep so
-that the host never starves the GPU inside a chunk; CUDA events on the
-launching stream bracket every step and every pass, and the reported device
-time is the sum of the per-step event intervals.
+that the host never starves the GPU inside a chunk.  CUDA events on the
+launching stream bracket every step; the reported device time is the sum of
+the per-step event intervals (consecutive kernels of a step overlap their
+prologues under programmatic dependent launch).  A second pass over the same K
+steps brackets every kernel with events, which gives each kernel's own duration
+for the per-pass table and the roofline object.
 
 --impl reference times the float64 CPU oracle (the only other implementation
 of the method here) on a bounded sample of the same workload.
