@@ -753,31 +753,45 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
             last = chunk;
             uint8_t *stage = smem + st * g.stage_bytes;
             const int na = ne * a_ops;
-            if (lane < na) {
-                const int e = lane / a_ops, hf = lane % a_ops;
-                const int src = (int)(sched[pos + 1 + e] >> 8);
-                uint8_t *dst = stage + e * g.a_slot;
-                if (FA) tma_load_2d(dst, &tm_act, &full[st], src * 64, n0, pol_act);
-                else tma_load_2d(dst + hf * BSE * 128, &tm_act, &full[st], n0 + 64 * hf, src * BSE, pol_act);
-            } else if (lane < na + nr * B_OPS) {
-                const int q = lane - na, r = q / B_OPS, sub = q % B_OPS;
-                const uint32_t *rec = sched + pos + 1 + ne + r * RW;
-                uint8_t *dst = stage + g.b_off + r * G::B_SLOT;
-                if (!COARSE) {
-                    tma_load_2d(dst, &tm_w, &full[st], 0, ((int)(rec[0] >> 7) - 1) * BS, pol_w);
+            // One TMA instruction for the whole chunk (each issue costs a fixed few hundred ns
+            // whatever the number of lanes): lanes < na load activation panels, the next
+            // nr * B_OPS lanes weight blocks (or, for bs=8, 8x8 sub-blocks and zero tiles).
+            if (lane < na + nr * B_OPS) {
+                const bool isa = lane < na;
+                const CUtensorMap *mp;
+                uint8_t *dst;
+                int cx, cy;
+                uint64_t pol;
+                if (isa) {
+                    const int e = lane / a_ops, hf = lane % a_ops;
+                    const int src = (int)(sched[pos + 1 + e] >> 8);
+                    mp = &tm_act;
+                    dst = stage + e * g.a_slot + (FA ? 0 : hf * BSE * 128);
+                    cx = FA ? src * 64 : n0 + 64 * hf;
+                    cy = FA ? n0 : src * BSE;
+                    pol = pol_act;
                 } else {
-                    // sub-block (cs, ks) -> core matrix at (N-group)*256 + (K-group)*128
-                    const int cs = sub >> 1, ks = sub & 1;
-                    const int ng = BWD ? cs : ks, kg = BWD ? ks : cs;
-                    const int id = (int)(sub == 0 ? (rec[0] >> 7) : rec[sub]) - 1;
-                    if (id >= 0) {
-                        tma_load_2d(dst + ng * 256 + kg * 128, &tm_w, &full[st], 0, id * 8, pol_w);
+                    const int q = lane - na, r = q / B_OPS, sub = q % B_OPS;
+                    const uint32_t *rec = sched + pos + 1 + ne + r * RW;
+                    dst = stage + g.b_off + r * G::B_SLOT;
+                    pol = pol_w;
+                    cx = 0;
+                    if (!COARSE) {
+                        mp = &tm_w;
+                        cy = ((int)(rec[0] >> 7) - 1) * BS;
                     } else {
+                        // sub-block (cs, ks) -> core matrix at (N-group)*256 + (K-group)*128;
                         // zero tiles are spread over the zero buffer so they hit many L2 lines
+                        const int cs = sub >> 1, ks = sub & 1;
+                        const int ng = BWD ? cs : ks, kg = BWD ? ks : cs;
+                        const int id = (int)(sub == 0 ? (rec[0] >> 7) : rec[sub]) - 1;
                         const int zr = (int)((blockIdx.x * 61u + (unsigned)chunk * 32u + (unsigned)lane) % kZeroTiles) * 8;
-                        tma_load_2d(dst + ng * 256 + kg * 128, &tm_zero, &full[st], 0, zr, pol_w);
+                        mp = id >= 0 ? &tm_w : &tm_zero;
+                        dst += ng * 256 + kg * 128;
+                        cy = id >= 0 ? id * 8 : zr;
                     }
                 }
+                tma_load_2d(dst, mp, &full[st], cx, cy, pol);
             }
             pos += 1 + ne + nr * RW;
         }
@@ -1010,14 +1024,13 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
                 __syncwarp();
                 if (aborted) break;
                 last = it;
-                if (lane < nrec) {
-                    uint8_t *a = sA + s * G::A_BYTES + lane * G::PANEL;
-                    if (FA) tma_load_2d(a, &maps.x[t], &full[s], cc * BSE, n0, pol);
-                    else tma_load_2d(a, &maps.x[t], &full[s], n0, cc * BSE, pol);
-                } else if (lane == nrec) {
-                    uint8_t *b = sB + s * G::B_BYTES;
-                    if (FA) tma_load_2d(b, &maps.dy[t], &full[s], kc * BSE, n0, pol);
-                    else tma_load_2d(b, &maps.dy[t], &full[s], n0, kc * BSE, pol);
+                // one TMA instruction: lanes < nrec the stacked x panels, lane nrec the dy panel
+                if (lane <= nrec) {
+                    const bool isx = lane < nrec;
+                    const CUtensorMap *mp = isx ? &maps.x[t] : &maps.dy[t];
+                    uint8_t *dst = isx ? sA + s * G::A_BYTES + lane * G::PANEL : sB + s * G::B_BYTES;
+                    const int f = (isx ? cc : kc) * BSE;
+                    tma_load_2d(dst, mp, &full[s], FA ? f : n0, FA ? n0 : f, pol);
                 }
             }
         }
@@ -1233,13 +1246,15 @@ k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
                 last = it;
                 uint8_t *a = sA + s * G::A_BYTES;
                 uint8_t *b = sB + s * G::B_BYTES;
-                if (FA) {
-                    if (lane < 2) tma_load_2d(a + lane * 8192, &maps.x[t], &full[s], f_c + lane * 64, n0, pol);
-                    else if (lane < 6)
-                        tma_load_2d(b + (lane - 2) * 8192, &maps.dy[t], &full[s], f_k + (lane - 2) * 64, n0, pol);
-                } else {
-                    if (lane == 0) tma_load_2d(a, &maps.x[t], &full[s], n0, f_c, pol);
-                    else if (lane == 1) tma_load_2d(b, &maps.dy[t], &full[s], n0, f_k, pol);
+                // one TMA instruction: the NA x boxes, then the NB dy boxes
+                constexpr int NA = FA ? 2 : 1, NB = FA ? 4 : 1;
+                if (lane < NA + NB) {
+                    const bool isx = lane < NA;
+                    const int j = isx ? lane : lane - NA;
+                    const CUtensorMap *mp = isx ? &maps.x[t] : &maps.dy[t];
+                    uint8_t *dst = (isx ? a : b) + j * 8192;
+                    const int f = (isx ? f_c : f_k) + j * 64;
+                    tma_load_2d(dst, mp, &full[s], FA ? f : n0, FA ? n0 : f, pol);
                 }
             }
         }
@@ -1443,13 +1458,15 @@ k_tc_updat_pair(const __grid_constant__ UpMaps maps, const UpParams p)
                 uint8_t *a = smem + s * G::STAGE;
                 uint8_t *b = a + G::A_BYTES;
                 const uint32_t fb = full0 + (uint32_t)s * 8u;
-                if (FA) {
-                    if (lane < 2) tma_load_2d_pair(a + lane * 8192, &maps.x[t], fb, f_c + lane * 64, n0, pol);
-                    else if (lane < 4)
-                        tma_load_2d_pair(b + (lane - 2) * 8192, &maps.dy[t], fb, f_k + (lane - 2) * 64, n0, pol);
-                } else {
-                    if (lane == 0) tma_load_2d_pair(a, &maps.x[t], fb, n0, f_c, pol);
-                    else if (lane == 1) tma_load_2d_pair(b, &maps.dy[t], fb, n0, f_k, pol);
+                // one TMA instruction: the NB x boxes, then the NB dy boxes
+                constexpr int NB = FA ? 2 : 1;
+                if (lane < 2 * NB) {
+                    const bool isx = lane < NB;
+                    const int j = isx ? lane : lane - NB;
+                    const CUtensorMap *mp = isx ? &maps.x[t] : &maps.dy[t];
+                    uint8_t *dst = (isx ? a : b) + j * 8192;
+                    const int f = (isx ? f_c : f_k) + j * 64;
+                    tma_load_2d_pair(dst, mp, fb, FA ? f : n0, FA ? n0 : f, pol);
                 }
             }
         }
@@ -1646,21 +1663,19 @@ k_tc_fbd(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUt
             const int pr = (int)(hdr >> 8);
             uint8_t *a = smem + st * STAGE;
             uint8_t *b = a + A_BYTES;
-            if (FA) {
-                if (lane == 0) tma_load_2d(b, &tm_act, &full[st], pr * 64, n0, pol_act);
-            } else {
-                if (lane < 4) tma_load_2d(b + lane * 8192, &tm_act, &full[st], n0 + 64 * lane, pr * 64, pol_act);
-            }
-            if (lane >= 8 && lane < 16) {
-                const int sl = lane - 8;                        // sub * 4 + out
-                const int id = (int)sched[pos + 1 + sl] - 1;
-                uint8_t *d = a + (sl >> 2) * 8192 + (sl & 3) * 2048;
-                if (id >= 0) {
-                    tma_load_2d(d, &tm_w, &full[st], 0, id * 32, pol_w);
-                } else {
-                    const int zr = (int)((blockIdx.x * 13u + (unsigned)chunk * 8u + (unsigned)sl) % 128u) * 32;
-                    tma_load_2d(d, &tm_zero, &full[st], 0, zr, pol_w);
-                }
+            // one TMA instruction: lanes < NX the activation boxes, the next 8 lanes the weight
+            // slots (sub * 4 + out), an absent block reading a zero tile
+            constexpr int NX = FA ? 1 : 4;
+            if (lane < NX + 8) {
+                const bool isx = lane < NX;
+                const int sl = lane - NX;
+                const int id = isx ? 0 : (int)sched[pos + 1 + sl] - 1;
+                const int zr = (int)((blockIdx.x * 13u + (unsigned)chunk * 8u + (unsigned)sl) % 128u) * 32;
+                const CUtensorMap *mp = isx ? &tm_act : (id >= 0 ? &tm_w : &tm_zero);
+                uint8_t *dst = isx ? b + lane * 8192 : a + (sl >> 2) * 8192 + (sl & 3) * 2048;
+                const int cx = isx ? (FA ? pr * 64 : n0 + 64 * lane) : 0;
+                const int cy = isx ? (FA ? n0 : pr * 64) : (id >= 0 ? id * 32 : zr);
+                tma_load_2d(dst, mp, &full[st], cx, cy, isx ? pol_act : pol_w);
             }
         }
         if (aborted && lane == 0 && last >= 0) mbar_wait(&full[last % STAGES], (last / STAGES) & 1, nullptr);
@@ -1853,22 +1868,19 @@ k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant_
             uint8_t *a = smem + st * STAGE;
             uint8_t *b = a + A_BYTES;
             const uint32_t fb = full0 + (uint32_t)st * 8u;
-            if (FA) {
-                if (lane == 0) tma_load_2d_pair(b, &tm_act, fb, pr * 64, n0 + 128 * (int)rank, pol_act);
-            } else {
-                if (lane < 2)
-                    tma_load_2d_pair(b + lane * 8192, &tm_act, fb, n0 + 128 * (int)rank + 64 * lane, pr * 64, pol_act);
-            }
-            if (lane >= 8 && lane < 16) {
-                const int sl = lane - 8, sub = sl >> 2, o = sl & 3;
-                const int id = (int)sched[pos + 1 + sub * 8 + (int)rank * 4 + o] - 1;
-                uint8_t *d = a + sub * 8192 + o * 2048;
-                if (id >= 0) {
-                    tma_load_2d_pair(d, &tm_w, fb, 0, id * 32, pol_w);
-                } else {
-                    const int zr = (int)((blockIdx.x * 13u + (unsigned)chunk * 8u + (unsigned)sl) % 128u) * 32;
-                    tma_load_2d_pair(d, &tm_zero, fb, 0, zr, pol_w);
-                }
+            // one TMA instruction: lanes < NX this CTA's activation boxes, the next 8 lanes its
+            // weight slots (sub * 4 + out), an absent block reading a zero tile
+            constexpr int NX = FA ? 1 : 2;
+            if (lane < NX + 8) {
+                const bool isx = lane < NX;
+                const int sl = lane - NX, sub = sl >> 2, o = sl & 3;
+                const int id = isx ? 0 : (int)sched[pos + 1 + sub * 8 + (int)rank * 4 + o] - 1;
+                const int zr = (int)((blockIdx.x * 13u + (unsigned)chunk * 8u + (unsigned)sl) % 128u) * 32;
+                const CUtensorMap *mp = isx ? &tm_act : (id >= 0 ? &tm_w : &tm_zero);
+                uint8_t *dst = isx ? b + lane * 8192 : a + sub * 8192 + o * 2048;
+                const int cx = isx ? (FA ? pr * 64 : n0 + 128 * (int)rank + 64 * lane) : 0;
+                const int cy = isx ? (FA ? n0 + 128 * (int)rank : pr * 64) : (id >= 0 ? id * 32 : zr);
+                tma_load_2d_pair(dst, mp, fb, cx, cy, isx ? pol_act : pol_w);
             }
         }
         // The last release of this warp's stages comes from the even CTA's MMA warp: waiting for
@@ -2051,8 +2063,7 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
     pdl_wait();
     if (!mbar_wait(&sched_full, 0, p.status)) aborted = 1;
     {
-        int n = 0;
-        while (sched[n * 9] != 0xFFFFFFFFu) ++n;
+        const int n = (len - 1) / 9;                 // 9-word entries, the end marker, < 4 words of padding
         lo = (int)(rank * n / kSplit);
         hi = (int)((rank + 1) * n / kSplit);
     }
@@ -2077,21 +2088,18 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
             const int pr = (int)(hdr >> 8);
             uint8_t *a = smem + st * STAGE;
             uint8_t *b = a + A_BYTES;
-            if (FA) {
-                if (lane == 0) tma_load_2d(b, &tm_act, &full[st], pr * 64, 0, pol_act);
-            } else {
-                if (lane == 0) tma_load_2d(b, &tm_act, &full[st], 0, pr * 64, pol_act);
-            }
-            if (lane >= 8 && lane < 16) {
-                const int sl = lane - 8;                        // sub * 4 + out
-                const int id = (int)sched[pos + 1 + sl] - 1;
-                uint8_t *d = a + (sl >> 2) * 8192 + (sl & 3) * 2048;
-                if (id >= 0) {
-                    tma_load_2d(d, &tm_w, &full[st], 0, id * 32, pol_w);
-                } else {
-                    const int zr = (int)((blockIdx.x * 13u + (unsigned)chunk * 8u + (unsigned)sl) % 128u) * 32;
-                    tma_load_2d(d, &tm_zero, &full[st], 0, zr, pol_w);
-                }
+            // one TMA instruction: lane 0 the activation panel, lanes 1..8 the weight slots
+            // (sub * 4 + out), an absent block reading a zero tile
+            if (lane < 9) {
+                const bool isx = lane == 0;
+                const int sl = lane - 1;
+                const int id = isx ? 0 : (int)sched[pos + 1 + sl] - 1;
+                const int zr = (int)((blockIdx.x * 13u + (unsigned)chunk * 8u + (unsigned)sl) % 128u) * 32;
+                const CUtensorMap *mp = isx ? &tm_act : (id >= 0 ? &tm_w : &tm_zero);
+                uint8_t *dst = isx ? b : a + (sl >> 2) * 8192 + (sl & 3) * 2048;
+                const int cx = isx ? (FA ? pr * 64 : 0) : 0;
+                const int cy = isx ? (FA ? 0 : pr * 64) : (id >= 0 ? id * 32 : zr);
+                tma_load_2d(dst, mp, &full[st], cx, cy, isx ? pol_act : pol_w);
             }
         }
         if (aborted && lane == 0) {
