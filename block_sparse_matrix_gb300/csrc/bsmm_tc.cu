@@ -2000,8 +2000,8 @@ k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant_
 // GPU, so a cluster of kSplit CTAs shares one tile: CTA r multiplies the r-th quarter of the
 // tile's source pairs.  The partial tiles are then summed across the cluster in distributed
 // shared memory, each CTA owning 32 of the tile's 128 output features: it receives the other
-// three CTAs' fp32 partials of its features into its (then idle) stage memory, adds its own,
-// rounds once and stores.  No atomics and no global scratch; with the reduction buffer inside
+// three CTAs' fp32 partials of its features into its (then idle) stage memory, next to its
+// own, and its four warps add them for 16 minibatch columns each, round once and store.  No atomics and no global scratch; with the reduction buffer inside
 // the stage memory, 8 stages of 24 KB keep the weight stream from HBM in flight.
 constexpr int kSplit = 4;
 
@@ -2020,7 +2020,8 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    // after the main loop: red[slot][j / 4][lane][4], the partials of the three other CTAs
+    // after the main loop: red[slot][j / 4][lane][4], the partials of this CTA's 32 features
+    // from the three other CTAs (slots 0-2) and its own (slot 3)
     float *red = reinterpret_cast<float *>(smem);
     const uint32_t *sched = reinterpret_cast<const uint32_t *>(smem + STAGES * STAGE);
     __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full, sched_full;
@@ -2163,49 +2164,61 @@ k_tc_fbd_split(const __grid_constant__ CUtensorMap tm_act, const __grid_constant
         }
     }
     cluster_sync();                                  // every CTA's MMAs are done: stage memory is free
-    if (warp < kProducers && q != (int)rank) {
-        const int slot = (int)rank < q ? (int)rank : (int)rank - 1;
+    if (warp < kProducers) {
+        // warp q sends its partial to CTA q (slot = the sender's rank among the other three);
+        // the owner's own partial goes to slot 3 of its own buffer
+        const int slot = q == (int)rank ? 3 : ((int)rank < q ? (int)rank : (int)rank - 1);
         const uint32_t dst = map_to_rank(smem_u32(red + (slot * 16 * 32 + lane) * 4), (uint32_t)q);
 #pragma unroll
         for (int j = 0; j < 64; j += 4) st_cluster_v4(dst + (j / 4) * 32 * 16, v[j], v[j + 1], v[j + 2], v[j + 3]);
     }
-    cluster_sync();                                  // the partials of this CTA's features have landed
-    if (warp == (int)rank) {
+    cluster_sync();                                  // all four partials of this CTA's features have landed
+    if (warp < kProducers) {
+        // warp w sums minibatch columns 16w .. 16w+15 of the CTA's 32 features (lane = feature):
+        // own partial first, then the other CTAs' in rank order, rounded once
+        const int f = grp * 128 + (int)rank * 32 + lane;
+        float r16[16];
 #pragma unroll
-        for (int slot = 0; slot < kSplit - 1; ++slot) {
+        for (int jj = 0; jj < 16; jj += 4) {
+            const int j4 = (warp * 16 + jj) / 4;
+            float4 acc4 = *reinterpret_cast<const float4 *>(red + ((3 * 16 + j4) * 32 + lane) * 4);
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-                const float4 t4 = *reinterpret_cast<const float4 *>(red + ((slot * 16 + j / 4) * 32 + lane) * 4);
-                v[j] += t4.x;
-                v[j + 1] += t4.y;
-                v[j + 2] += t4.z;
-                v[j + 3] += t4.w;
+            for (int sl = 0; sl < kSplit - 1; ++sl) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(red + ((sl * 16 + j4) * 32 + lane) * 4);
+                acc4.x += t4.x;
+                acc4.y += t4.y;
+                acc4.z += t4.z;
+                acc4.w += t4.w;
             }
+            r16[jj] = acc4.x;
+            r16[jj + 1] = acc4.y;
+            r16[jj + 2] = acc4.z;
+            r16[jj + 3] = acc4.w;
         }
-        const int f = grp * 128 + q * 32 + lane;
         uint16_t *out = static_cast<uint16_t *>(p.out);
+        const int j0 = warp * 16;
         if (f < p.Fout) {
             if (FA) {
-                // (N, F) rows: the warp writes 64 contiguous bytes of each minibatch row
+                // (N, F) rows: each store writes 64 contiguous bytes of one minibatch row
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    if (j < p.N) out[(size_t)j * p.Fout + f] = cvt1<BF16>(v[j]);
-            } else if (p.N == 64) {
-                uint16_t *dst = out + (size_t)f * p.N;
+                for (int jj = 0; jj < 16; ++jj)
+                    if (j0 + jj < p.N) out[(size_t)(j0 + jj) * p.Fout + f] = cvt1<BF16>(r16[jj]);
+            } else if (j0 + 16 <= p.N) {
+                uint16_t *dst = out + (size_t)f * p.N + j0;
 #pragma unroll
-                for (int j = 0; j < 64; j += 8) {
+                for (int jj = 0; jj < 16; jj += 8) {
                     uint4 pk;
-                    pk.x = pack2<BF16>(v[j], v[j + 1]);
-                    pk.y = pack2<BF16>(v[j + 2], v[j + 3]);
-                    pk.z = pack2<BF16>(v[j + 4], v[j + 5]);
-                    pk.w = pack2<BF16>(v[j + 6], v[j + 7]);
-                    *reinterpret_cast<uint4 *>(dst + j) = pk;
+                    pk.x = pack2<BF16>(r16[jj], r16[jj + 1]);
+                    pk.y = pack2<BF16>(r16[jj + 2], r16[jj + 3]);
+                    pk.z = pack2<BF16>(r16[jj + 4], r16[jj + 5]);
+                    pk.w = pack2<BF16>(r16[jj + 6], r16[jj + 7]);
+                    *reinterpret_cast<uint4 *>(dst + jj) = pk;
                 }
             } else {
-                uint16_t *dst = out + (size_t)f * p.N;
+                uint16_t *dst = out + (size_t)f * p.N + j0;
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    if (j < p.N) dst[j] = cvt1<BF16>(v[j]);
+                for (int jj = 0; jj < 16; ++jj)
+                    if (j0 + jj < p.N) dst[jj] = cvt1<BF16>(r16[jj]);
             }
         }
     }
