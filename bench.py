@@ -401,10 +401,16 @@ def run_cpu_baseline(wl, inp, Ns, budget_s=10.0):
     scale = max(1, int(budget_s / max(t1, 1e-3)))
     rows = min(1024, nthreads * scale)
     blocks = min(inp.nnz, 64 * scale)
-    f, t = oracle_sample(wl, inp, rows, blocks, nthreads, 1024)
+    # repeat the sample until about three quarters of the budget is spent (at most 8 times)
+    f = t = 0.0
+    reps = 0
+    while reps < 8 and (reps == 0 or t < 0.75 * budget_s):
+        fi, ti = oracle_sample(wl, inp, rows, blocks, nthreads, 1024)
+        f, t, reps = f + fi, t + ti, reps + 1
     return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-            "sample": "float64 dense-W oracle at N=1024: fprop and bprop of %d minibatch rows, updat of %d blocks "
-                      "(%.1f s); effective FLOPs 2*rows*nnz*bs^2 per fwd/bwd + 2*N*bs^2 per block" % (rows, blocks, t)}
+            "sample": "float64 dense-W oracle at N=1024: %d x (fprop and bprop of %d minibatch rows, updat of %d "
+                      "blocks), %.1f s; effective FLOPs 2*rows*nnz*bs^2 per fwd/bwd + 2*N*bs^2 per block" %
+                      (reps, rows, blocks, t)}
 
 
 def run_reference(args):
