@@ -1933,18 +1933,22 @@ k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant_
         tc_fence_after();
         const bool any = len > 4;                     // at least one entry (else the stream is the end marker)
         uint16_t *out = static_cast<uint16_t *>(p.out);
+        // (N,C) outputs: the bf16 tile [256 rows][128 features] is staged in the idle stage
+        // memory 32 rows at a time; each 32-row slice is stored by one TMA store as soon as the
+        // four warps have written it, overlapping the stores with the remaining TMEM reads.
         uint16_t *tile_s = reinterpret_cast<uint16_t *>(smem);
         for (int c0 = 0; c0 < 256; c0 += 32) {
             if (!FA && n0 + c0 >= p.N) break;
             float v[32];
             if (ok && any) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, r0);
+                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0 + 16, r1);
+                tmem_ld_wait();
 #pragma unroll
-                for (int h2 = 0; h2 < 32; h2 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0 + h2, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[h2 + j] = __uint_as_float(r[j]);
+                for (int j = 0; j < 16; ++j) {
+                    v[j] = __uint_as_float(r0[j]);
+                    v[16 + j] = __uint_as_float(r1[j]);
                 }
             } else {
 #pragma unroll
@@ -1953,6 +1957,12 @@ k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant_
             if (FA) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) tile_s[(c0 + j) * 128 + q * 32 + lane] = cvt1<BF16>(v[j]);
+                fence_proxy_async_smem();
+                named_sync(1, 32 * kProducers);
+                if (warp == 0 && lane == 0) {
+                    tma_store_2d(&tm_out, tile_s + c0 * 128, fbase, n0 + c0);
+                    bulk_commit();
+                }
                 continue;
             }
             if (f >= p.Fout) continue;
@@ -1974,15 +1984,7 @@ k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant_
                     if (nb + j < p.N) dst[j] = cvt1<BF16>(v[j]);
             }
         }
-        if (FA) {
-            fence_proxy_async_smem();
-            named_sync(1, 32 * kProducers);
-            if (warp == 0 && lane == 0) {
-                tma_store_2d(&tm_out, tile_s, fbase, n0);
-                bulk_commit();
-                bulk_wait_read();
-            }
-        }
+        if (FA && warp == 0 && lane == 0) bulk_wait_read();   // the slices have left shared memory
     }
     if (aborted) {
         // copies of the pair may still be landing in this CTA: give them time (bounded)
@@ -2514,7 +2516,7 @@ bsmm_status launch_fbd_pair(bsmm_ctx *h, FbDenseSched &fs, const void *act, cons
     else ok = make_map2d(&m_act, act, t, N, Fin, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && make_map2d(&m_w, w, t, 32, (uint64_t)h->nnz * 32, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     ok = ok && make_map2d(&m_zero, st->d_zero, t, 32, kZeroBytes / 64, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (FA) ok = ok && make_map2d(&m_out, out, t, Fout, N, 128, 256, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (FA) ok = ok && make_map2d(&m_out, out, t, Fout, N, 128, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
     else m_out = m_act;                                  // unused for (C,N) outputs
     if (!ok) return BSMM_ERR_CUDA;
     FbdParams p = {};
