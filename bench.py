@@ -322,54 +322,73 @@ def run_ours(args):
 
 
 def run_e2e(m, inp, Ns, passes, dev, args):
-    """The same step through the public API from pinned HOST buffers: H2D of the
-    step's inputs, the six passes, D2H of the results, all inside the timed region."""
+    """The same step through the public API from pinned HOST buffers: every step uploads its
+    inputs, runs the six passes and downloads its results, all inside the timed region.  Steps
+    are pipelined over three streams (uploads, passes, downloads) with two device buffer sets
+    ordered by events, so step i+1's uploads and step i-1's downloads overlap step i's passes."""
     from block_sparse_matrix_gb300 import bsmm
     wl = wk.CONFIGS["cfg2_n1024"]
     C, K, bs, nnz = wl.C, wl.K, wl.bs, m.nnz
     host = {"w": inp.w.pin_memory()}
-    devb = {"w": torch.empty_like(inp.w, device=dev)}
     for N in Ns:
         host["x%d" % N] = wk.normals((N, C), 9300 + N, 1.0, wl.dtype).pin_memory()
         host["dy%d" % N] = wk.normals((N, K), 9400 + N, 1.0, wl.dtype).pin_memory()
         for k, shape, dt in (("y", (N, K), torch.bfloat16), ("dx", (N, C), torch.bfloat16),
                              ("dw", (nnz, bs, bs), torch.float32)):
             host["%s%d" % (k, N)] = torch.empty(shape, dtype=dt).pin_memory()
-        for k in ("x", "dy", "y", "dx", "dw"):
-            devb["%s%d" % (k, N)] = torch.empty_like(host["%s%d" % (k, N)], device=dev)
+    devb = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
     ins = ["w"] + ["x%d" % N for N in Ns] + ["dy%d" % N for N in Ns]
     outs = ["%s%d" % (k, N) for N in Ns for k in ("y", "dx", "dw")]
     h2d = sum(host[k].numel() * host[k].element_size() for k in ins)
     d2h = sum(host[k].numel() * host[k].element_size() for k in outs)
     steps = max(10, min(args.steps, 200))
+    s_up, s_cmp, s_dn = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_up = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_dn = [torch.cuda.Event() for _ in range(2)]
 
-    def one():
-        for k in ins:
-            devb[k].copy_(host[k], non_blocking=True)
+    def one(i):
+        b = i % 2
+        d = devb[b]
+        with torch.cuda.stream(s_up):
+            if i >= 2:
+                s_up.wait_event(ev_cmp[b])          # step i-2's passes have read this input set
+            for k in ins:
+                d[k].copy_(host[k], non_blocking=True)
+            ev_up[b].record(s_up)
+        s_cmp.wait_event(ev_up[b])
+        if i >= 2:
+            s_cmp.wait_event(ev_dn[b])              # step i-2's results have left this output set
         for name, N, _, _ in passes:
             kind = name.split("_n")[0]
             if kind == "fprop":
-                bsmm.bsmm_fprop(m.handle, devb["x%d" % N], devb["w"], devb["y%d" % N], N)
+                bsmm.bsmm_fprop(m.handle, d["x%d" % N], d["w"], d["y%d" % N], N, stream=s_cmp)
             elif kind == "bprop":
-                bsmm.bsmm_bprop(m.handle, devb["dy%d" % N], devb["w"], devb["dx%d" % N], N)
+                bsmm.bsmm_bprop(m.handle, d["dy%d" % N], d["w"], d["dx%d" % N], N, stream=s_cmp)
             else:
-                bsmm.bsmm_updat(m.handle, devb["x%d" % N], devb["dy%d" % N], devb["dw%d" % N], N)
-        for k in outs:
-            host[k].copy_(devb[k], non_blocking=True)
+                bsmm.bsmm_updat(m.handle, d["x%d" % N], d["dy%d" % N], d["dw%d" % N], N, stream=s_cmp)
+        ev_cmp[b].record(s_cmp)
+        with torch.cuda.stream(s_dn):
+            s_dn.wait_event(ev_cmp[b])
+            for k in outs:
+                host[k].copy_(d[k], non_blocking=True)
+            ev_dn[b].record(s_dn)
 
-    for _ in range(3):
-        one()
+    for i in range(3):
+        one(i)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        one()
-    b.record()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_up)
+    for i in range(steps):
+        one(i)
+    e.record(s_dn)                                   # after the last step's downloads
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
+    m.sync_status()
+    ms = a.elapsed_time(e) / steps
     flops = sum(p[2] for p in passes)
     return {"value": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4), "steps": steps}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4), "steps": steps,
+            "pipelined": "uploads, passes and downloads on three streams, two device buffer sets"}
 
 
 # ---- CPU oracle --------------------------------------------------------------------------
