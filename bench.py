@@ -66,6 +66,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, ws, device):
+    """The largest value of x over the ranks of the default process group (x itself at
+    world size 1): the job's time is that of its slowest replica."""
+    if ws <= 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ws, step_flops, steps, dev_ms):
+    """Whole-job effective TFLOP/s: every replica does step_flops per step (weak scaling),
+    and the job takes the slowest replica's dev_ms for `steps` steps."""
+    return ws * step_flops * steps / (dev_ms * 1e-3) / 1e12
+
+
 # ---- pass bookkeeping -------------------------------------------------------------------
 
 def pass_list(nnz, bs, C, K, Ns, e=2):
@@ -276,12 +293,9 @@ def run_ours(args):
     pass_us = {}
     for j, p in enumerate(passes):
         pass_us[p[0]] = 1000.0 * sum(ev_pass[i][j][0].elapsed_time(ev_pass[i][j][1]) for i in range(K_steps)) / K_steps
-    if ws > 1:
-        t = torch.tensor([dev_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dev_ms = float(t.item())
+    dev_ms = max_over_ranks(dev_ms, ws, dev)
     ms_per_step = dev_ms / K_steps
-    value = ws * step_flops * K_steps / (dev_ms * 1e-3) / 1e12
+    value = job_value(ws, step_flops, K_steps, dev_ms)
 
     peaks, peak_src = load_peaks()
     per_pass = {}
