@@ -40,7 +40,7 @@ def _worker(rank, ws, port, out):
 
 def test_two_rank_max_and_value():
     ws, port = 2, _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_worker, args=(ws, port, out), nprocs=ws, join=True)
     for r in range(ws):
         t, v = out[r]
