@@ -581,6 +581,7 @@ constexpr int kProducers = 4;                    // fprop/bprop: producer+epilog
 constexpr int kFbThreads = 32 * (kProducers + 1);
 constexpr int kUpThreads = 32 * (kProducers + 5);        // updat: producers, MMA warp, 4 epilogue warps
 static_assert(16 % kProducers == 0, "stage counts must be multiples of the producer count");
+constexpr int kFbpThreads = 32 * (kProducers + 5);      // CTA-pair fprop/bprop: + 4 epilogue warps
 constexpr int kZeroTiles = 2048;                 // 8x8 zero tiles in the zero buffer (256 KB)
 constexpr int kZeroBytes = kZeroTiles * 128;
 
@@ -1791,7 +1792,7 @@ k_tc_fbd(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUt
 //   the even CTA's commits release the stage in both CTAs and finally signal both
 //   accumulators.  Operand layouts per CTA are those of k_tc_fbd with 128 activation rows.
 template <int FA, bool BWD, bool BF16>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFbThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFbpThreads, 1)
 k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_w,
               const __grid_constant__ CUtensorMap tm_zero, const __grid_constant__ CUtensorMap tm_out,
               const FbdParams p)
@@ -1924,9 +1925,13 @@ k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant_
         }
         __syncwarp();
     }
-    if (warp < kProducers) {
-        // epilogue: warp q holds output features 32q..32q+31 of this CTA's half, lane = feature
+    if (warp != kProducers) {
+        // epilogue, 8 warps: warp w holds output features 32q..32q+31 (q = w mod 4, lane =
+        // feature) of this CTA's half for minibatch columns 128h..128h+127 (h = 0 for warps
+        // 0-3, 1 for warps 5-8)
         const int q = warp & 3;
+        const int h = warp < kProducers ? 0 : 1;
+        const int lead = h ? kProducers + 1 : 0;      // warp that stores the half's slices
         const int fbase = grp * 256 + (int)rank * 128;
         const int f = fbase + q * 32 + lane;
         const bool ok = mbar_wait_warp(&acc_full, 0, p.status, 256);
@@ -1935,9 +1940,9 @@ k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant_
         uint16_t *out = static_cast<uint16_t *>(p.out);
         // (N,C) outputs: the bf16 tile [256 rows][128 features] is staged in the idle stage
         // memory 32 rows at a time; each 32-row slice is stored by one TMA store as soon as the
-        // four warps have written it, overlapping the stores with the remaining TMEM reads.
+        // half's four warps have written it, overlapping the stores with the remaining TMEM reads.
         uint16_t *tile_s = reinterpret_cast<uint16_t *>(smem);
-        for (int c0 = 0; c0 < 256; c0 += 32) {
+        for (int c0 = h * 128; c0 < h * 128 + 128; c0 += 32) {
             if (!FA && n0 + c0 >= p.N) break;
             float v[32];
             if (ok && any) {
@@ -1958,8 +1963,8 @@ k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant_
 #pragma unroll
                 for (int j = 0; j < 32; ++j) tile_s[(c0 + j) * 128 + q * 32 + lane] = cvt1<BF16>(v[j]);
                 fence_proxy_async_smem();
-                named_sync(1, 32 * kProducers);
-                if (warp == 0 && lane == 0) {
+                named_sync(1 + h, 128);
+                if (warp == lead && lane == 0) {
                     tma_store_2d(&tm_out, tile_s + c0 * 128, fbase, n0 + c0);
                     bulk_commit();
                 }
@@ -1984,7 +1989,7 @@ k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant_
                     if (nb + j < p.N) dst[j] = cvt1<BF16>(v[j]);
             }
         }
-        if (FA && warp == 0 && lane == 0) bulk_wait_read();   // the slices have left shared memory
+        if (FA && warp == lead && lane == 0) bulk_wait_read();   // the slices have left shared memory
     }
     if (aborted) {
         // copies of the pair may still be landing in this CTA: give them time (bounded)
@@ -2003,8 +2008,9 @@ k_tc_fbd_pair(const __grid_constant__ CUtensorMap tm_act, const __grid_constant_
 // tile's source pairs.  The partial tiles are then summed across the cluster in distributed
 // shared memory, each CTA owning 32 of the tile's 128 output features: it receives the other
 // three CTAs' fp32 partials of its features into its (then idle) stage memory, next to its
-// own, and its four warps add them for 16 minibatch columns each, round once and store.  No atomics and no global scratch; with the reduction buffer inside
-// the stage memory, 8 stages of 24 KB keep the weight stream from HBM in flight.
+// own, and its four warps add them for 16 minibatch columns each, round once and store.  No
+// atomics and no global scratch; with the reduction buffer inside the stage memory, 8 stages
+// of 24 KB keep the weight stream from HBM in flight.
 constexpr int kSplit = 4;
 
 template <int FA, bool BWD, bool BF16>
@@ -2536,7 +2542,7 @@ bsmm_status launch_fbd_pair(bsmm_ctx *h, FbDenseSched &fs, const void *act, cons
             return BSMM_ERR_CUDA;
         attr_set.store(h->device);
     }
-    const cudaError_t le = launch_pdl(kern, dim3(fs.ngroups * p.n_tiles * 2), dim3(kFbThreads), smem, s, true, m_act,
+    const cudaError_t le = launch_pdl(kern, dim3(fs.ngroups * p.n_tiles * 2), dim3(kFbpThreads), smem, s, true, m_act,
                                       m_w, m_zero, m_out, p);
     g_bsmm_launches += 1;
     return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
