@@ -17,6 +17,7 @@
  *   - identity_init: identity initialisation of the weight blocks.
  *   - group_param_grads: the weight gradients of up to 8 timesteps sharing one
  *     weight are summed (cast32: in float32 or wider).
+ * and its section "blocksparse.norms" for layer_norm (at the end of this file).
  *
  * Readings where the page is silent (each one also listed in the design notes):
  *   - block ids are assigned in row-major scan order of the layout
@@ -30,6 +31,7 @@
  * beyond the definition: each output is accumulated over its reduction index
  * in increasing order.  OpenMP only splits independent outputs across threads.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -319,4 +321,42 @@ int oracle_max_threads(void)
 #else
     return 1;
 #endif
+}
+
+/*
+ * layer_norm(x, g, b, axis, epsilon, relu)  [blocksparse README, section
+ * "blocksparse.norms": a layernorm for both bsmm feature_axis activation layouts,
+ * with an optional relu applied at the end].  The page gives the signature only;
+ * the readings taken:
+ *   - the statistics of sample n run over its C features: row n of an (N,C)
+ *     array for axis = 1, column n of a (C,N) array for axis = 0 (the same
+ *     meaning as feature_axis);
+ *   - the variance is the biased one (divided by C), epsilon is added to it
+ *     inside the square root, and g, b are per-feature scale and shift:
+ *       y[n][f] = g[f] * (x[n][f] - mean_n) / sqrt(var_n + epsilon) + b[f];
+ *   - relu replaces negative outputs by zero after the shift.
+ * Mean first, then the variance of the deviations (two passes), all float64,
+ * features in increasing order.
+ */
+void oracle_layer_norm(const double *x, const double *g, const double *b, double *y,
+                       int N, int C, int axis, double epsilon, int relu)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        double s = 0.0;
+        for (int64_t f = 0; f < C; ++f)
+            s += act(x, n, f, N, C, axis);
+        const double mean = s / (double)C;
+        double v = 0.0;
+        for (int64_t f = 0; f < C; ++f) {
+            const double d = act(x, n, f, N, C, axis) - mean;
+            v += d * d;
+        }
+        const double sd = sqrt(v / (double)C + epsilon);
+        for (int64_t f = 0; f < C; ++f) {
+            double o = g[f] * (act(x, n, f, N, C, axis) - mean) / sd + b[f];
+            if (relu && o < 0.0)
+                o = 0.0;
+            *act_ptr(y, n, f, N, C, axis) = o;
+        }
+    }
 }

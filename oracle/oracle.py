@@ -4,8 +4,8 @@ TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
 benchmark's CPU-baseline leg may import this module.  It shares no code with
 the CUDA library.  Every function follows the blocksparse README, section
 "API Documentation: blocksparse.matmul" (BlocksparseMatMul, block_coord,
-identity_init, __call__, group_param_grads); the C file states the readings
-taken where the page is silent.
+identity_init, __call__, group_param_grads), or its "blocksparse.norms" section
+(layer_norm); the C file states the readings taken where the page is silent.
 
 Inputs are numpy arrays; floating-point inputs are converted to float64
 exactly (bf16/fp16/fp32 values widen without rounding).
@@ -36,7 +36,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp%d" % os.getpid()
         subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
-                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp])
+                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -59,6 +59,7 @@ def _load():
         lib.oracle_fprop_at.argtypes = [_u8, _c, _c, _c, _d, _d, _c, _c, _i64, _i64, _l, _d]
         lib.oracle_bprop_at.argtypes = [_u8, _c, _c, _c, _d, _d, _c, _c, _i64, _i64, _l, _d]
         lib.oracle_updat_at.argtypes = [_u8, _c, _c, _c, _d, _d, _c, _c, _i64, _i64, _i64, _l, _d]
+        lib.oracle_layer_norm.argtypes = [_d, _d, _d, _d, _c, _c, _c, ctypes.c_double, _c]
         lib.oracle_max_threads.restype = _c
         _lib = lib
     return _lib
@@ -220,3 +221,16 @@ def updat_at(L, bs: int, x, dy, feature_axis: int, b_idx, i_idx, j_idx) -> np.nd
                             feature_axis, _p(b_idx, _i64), _p(i_idx, _i64), _p(j_idx, _i64),
                             len(b_idx), _p(out, _d))
     return out
+
+
+def layer_norm(x, g, b, axis: int = 1, epsilon: float = 1e-6, relu: bool = False) -> np.ndarray:
+    """layer_norm of the README's "blocksparse.norms" section (the readings are stated in the
+    C source): x is (N, C) for axis = 1 or (C, N) for axis = 0; g, b have C entries."""
+    x, g, b = _f64(x), _f64(g).reshape(-1), _f64(b).reshape(-1)
+    assert x.ndim == 2 and axis in (0, 1)
+    C = x.shape[1] if axis == 1 else x.shape[0]
+    N = x.shape[0] if axis == 1 else x.shape[1]
+    assert g.size == C and b.size == C
+    y = np.empty_like(x)
+    _load().oracle_layer_norm(_p(x, _d), _p(g, _d), _p(b, _d), _p(y, _d), N, C, axis, float(epsilon), int(relu))
+    return y

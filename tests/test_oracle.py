@@ -7,6 +7,7 @@ swapped feature_axis) fails at least one of them.
 """
 import itertools
 import json
+import math
 import os
 
 import numpy as np
@@ -274,3 +275,69 @@ def test_workload_layouts():
     wl = wk.CONFIGS["cfg5"]
     L = wk.make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 5000)
     assert np.all(L.sum(1) == 9) and np.all(np.diag(L) == 1)
+
+
+# ---- layer_norm (README "blocksparse.norms"): pins independent of the oracle's code ----------
+
+def _ln_inputs(N, C, seed):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((N, C)) * 3.0 + 1.5, rng.standard_normal(C), rng.standard_normal(C)
+
+
+def test_layer_norm_hand_example():
+    """x = (1, 2, 3, 4): mean 5/2 and biased variance 5/4 by hand, so the normalised values
+    are (x - 5/2) / sqrt(5/4); then scale, shift and relu elementwise."""
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    g = np.array([1.0, 2.0, 0.5, -1.0])
+    b = np.array([0.0, 1.0, -1.0, 0.25])
+    z = (x[0] - 2.5) / math.sqrt(1.25)
+    want = g * z + b
+    got = o.layer_norm(x, g, b, axis=1, epsilon=0.0)
+    assert np.allclose(got[0], want, rtol=0, atol=1e-15)
+    got_r = o.layer_norm(x, g, b, axis=1, epsilon=0.0, relu=True)
+    assert np.array_equal(got_r[0], np.maximum(got[0], 0.0))
+
+
+def test_layer_norm_output_statistics():
+    """With g = 1, b = 0 every sample's output has mean 0 and mean square var / (var + eps)
+    (numpy's biased variance of the input)."""
+    x, _, _ = _ln_inputs(7, 37, 1)
+    eps = 1e-3
+    y = o.layer_norm(x, np.ones(37), np.zeros(37), axis=1, epsilon=eps)
+    var = np.var(x, axis=1)
+    assert np.allclose(y.mean(axis=1), 0.0, atol=1e-13)
+    assert np.allclose((y * y).mean(axis=1), var / (var + eps), rtol=1e-12)
+
+
+def test_layer_norm_constant_sample_gives_shift():
+    x = np.full((3, 16), 0.5)
+    x[1] = -2.0
+    g, b = np.arange(16.0) - 3, np.linspace(-1, 1, 16)
+    for relu in (False, True):
+        y = o.layer_norm(x, g, b, axis=1, epsilon=1e-6, relu=relu)
+        assert np.array_equal(y, np.tile(np.maximum(b, 0.0) if relu else b, (3, 1)))
+
+
+def test_layer_norm_affine_invariance():
+    """layer_norm(a x + c) with epsilon scaled by a^2 equals layer_norm(x): a wrong centring,
+    a wrong variance divisor or epsilon outside the square root breaks this."""
+    x, g, b = _ln_inputs(5, 64, 2)
+    a, c, eps = 3.0, -7.0, 1e-2
+    y1 = o.layer_norm(x, g, b, axis=1, epsilon=eps)
+    y2 = o.layer_norm(a * x + c, g, b, axis=1, epsilon=eps * a * a)
+    assert np.allclose(y1, y2, rtol=1e-11, atol=1e-12)
+
+
+def test_layer_norm_axis_layouts_agree():
+    x, g, b = _ln_inputs(6, 40, 3)
+    y1 = o.layer_norm(x, g, b, axis=1, epsilon=1e-6, relu=True)
+    y0 = o.layer_norm(x.T.copy(), g, b, axis=0, epsilon=1e-6, relu=True)
+    assert np.array_equal(y0, y1.T)
+
+
+def test_layer_norm_matches_numpy_definition():
+    """Against numpy's own mean / biased variance, written independently of the oracle."""
+    x, g, b = _ln_inputs(9, 33, 4)
+    eps = 1e-6
+    want = g * (x - x.mean(axis=1, keepdims=True)) / np.sqrt(x.var(axis=1, keepdims=True) + eps) + b
+    assert np.allclose(o.layer_norm(x, g, b, axis=1, epsilon=eps), want, rtol=1e-12, atol=1e-12)
