@@ -167,9 +167,10 @@ def traffic_for(kernel_pass):
 
 
 def source_sha():
+    """Hash of the sources of the step's kernels (layer_norm is not part of the step)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_sparse_matrix_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(n for n in os.listdir(csrc) if n != "bsmm_norm.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -476,6 +477,52 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_norm(args):
+    """layer_norm (README "blocksparse.norms") on the step's activation shape, N = 1024
+    samples of C = 4096 bf16 features, in both layouts; 16 rotating input/output sets
+    (256 MB > L2).  Bytes per launch = read x + write y + g, b.  One JSON line."""
+    from block_sparse_matrix_gb300 import bsmm
+    dev = torch.device("cuda", 0)
+    N, C, sets = 1024, 4096, 16
+    peaks, peak_src = load_peaks()
+    g = torch.randn(C, device=dev)
+    b = torch.randn(C, device=dev)
+    out = {}
+    for axis in (1, 0):
+        shape = (N, C) if axis == 1 else (C, N)
+        xs = [wk.normals(shape, 500 + i, 1.0, "bf16").to(dev) for i in range(sets)]
+        ys = [torch.empty_like(x) for x in xs]
+        for i in range(max(3, args.warmup)):
+            bsmm.layer_norm(xs[i % sets], g, b, axis=axis, y=ys[i % sets])
+        torch.cuda.synchronize()
+        # host time per call, then chunks of launches queued behind a device sleep that covers
+        # their enqueueing, so the GPU never waits for the host inside a chunk
+        t0 = time.perf_counter()
+        for i in range(20):
+            bsmm.layer_norm(xs[i % sets], g, b, axis=axis, y=ys[i % sets])
+        host_s = (time.perf_counter() - t0) / 20
+        torch.cuda.synchronize()
+        chunk = 50
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(0, args.steps, chunk)]
+        for c, c0 in enumerate(range(0, args.steps, chunk)):
+            torch.cuda._sleep(int(host_s * 1.5 * chunk * 2.1e9) + 100000)
+            ev[c][0].record()
+            for i in range(c0, min(args.steps, c0 + chunk)):
+                bsmm.layer_norm(xs[i % sets], g, b, axis=axis, y=ys[i % sets])
+            ev[c][1].record()
+        torch.cuda.synchronize()
+        us = sum(a.elapsed_time(e) for a, e in ev) * 1000 / args.steps
+        byts = 2 * N * C * 2 + 2 * C * 4
+        gbs = byts / us / 1e3
+        out["axis%d" % axis] = {"us": round(us, 3), "gbs": round(gbs, 1), "bytes": byts,
+                                 "roofline_frac": round(gbs / peaks["hbm_gbs"], 4)}
+    print(json.dumps({"metric": "layer_norm GB/s (read x + write y) on 1 GB300", "unit": "GB/s",
+                      "value": round(min(v["gbs"] for v in out.values()), 1), "dtype": "bf16",
+                      "config": {"workload": "N=1024 samples x C=4096 features, bf16, g/b fp32, 16 rotating sets"},
+                      "peak": peaks["hbm_gbs"], "peak_source": peak_src, "passes": out}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -486,8 +533,12 @@ def main():
                     help="seconds of CPU time for the oracle baseline sample (0 skips it)")
     ap.add_argument("--only", default="",
                     help="time a single pass (e.g. fprop_n1024) instead of the whole step; for kernel profiling")
+    ap.add_argument("--norm", action="store_true",
+                    help="time layer_norm on the step's activation shape instead of the step")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.norm:
+        run_norm(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

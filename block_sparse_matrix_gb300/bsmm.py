@@ -59,6 +59,7 @@ def lib():
             "bsmm_sync_status": [vp, vp],
             "bsmm_selftest_wait_timeout": [vp, ctypes.c_uint64, vp],
             "bsmm_updat_noalloc": [vp, vp, vp, vp, i, i, i, vp],
+            "bsmm_layer_norm": [vp, vp, vp, vp, i, i, i, ctypes.c_float, i, i, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -301,3 +302,29 @@ def group_param_grads(bsmm: BlocksparseMatMul, xs, dys, group_size: int = 8, dw=
         dw = bsmm.updat_grouped(xs[g0:g0 + group_size], dys[g0:g0 + group_size], dw=dw,
                                 accumulate=accumulate or g0 > 0)
     return dw
+
+
+def bsmm_layer_norm(x, g, b, y, N: int, C: int, axis: int = 1, epsilon: float = 1e-6, relu: bool = False,
+                    stream=None):
+    _check(lib().bsmm_layer_norm(_ptr(x), _ptr(g), _ptr(b), _ptr(y), N, C, axis, float(epsilon), int(relu),
+                                 _DT[x.dtype], _stream(stream)), "bsmm_layer_norm")
+
+
+def layer_norm(x, g, b, axis: int = 1, epsilon: float = 1e-6, relu: bool = False, y=None, stream=None):
+    """layer_norm(x, g, b, axis=1, epsilon=1e-6, relu=False) of the README's
+    "blocksparse.norms" section: x is (N, C) for axis = 1 or (C, N) for axis = 0 (the
+    matmul's feature_axis), g and b are float32 vectors of C values; returns y (x's dtype).
+    y may be x (in place)."""
+    for t, what in ((x, "x"), (g, "g"), (b, "b")):
+        _dev(t, what)
+    if x.dim() != 2 or axis not in (0, 1):
+        raise ValueError("x must be 2-D and axis 0 or 1")
+    C = x.shape[1] if axis == 1 else x.shape[0]
+    N = x.shape[0] if axis == 1 else x.shape[1]
+    if g.dtype != torch.float32 or b.dtype != torch.float32 or g.numel() != C or b.numel() != C:
+        raise ValueError("g and b must be float32 with C = %d values" % C)
+    if y is None:
+        y = torch.empty_like(x)
+    _dev(y, "y")
+    bsmm_layer_norm(x, g, b, y, N, C, axis, epsilon, relu, stream)
+    return y

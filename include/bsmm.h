@@ -167,6 +167,23 @@ bsmm_status bsmm_updat_grouped(bsmm_t h, const void *const *xs, const void *cons
 bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *dy, float *dw, int N, bsmm_dtype t,
                                int accumulate, void *stream);
 
+/*
+ * layer_norm(x, g, b, axis, epsilon, relu) [README, section "blocksparse.norms": a layernorm
+ * for both bsmm feature_axis activation layouts, with an optional relu applied at the end].
+ * For every sample n its C features are normalised with their mean and biased variance:
+ *   y[n][f] = g[f] * (x[n][f] - mean_n) / sqrt(var_n + epsilon) + b[f],  then max(y, 0) if relu.
+ * x, y: DEVICE pointers of dtype t, (N, C) row-major for axis = 1 or (C, N) for axis = 0 (the
+ * meaning of feature_axis); g, b: DEVICE pointers to C float32 values.  Statistics and
+ * arithmetic in float32, one rounding of y to t.  y may equal x (in place).  Needs no handle;
+ * enqueued on `stream`.  N = 0 is a no-op (the pointers are then not used and may be NULL).
+ * Errors: INVALID (null pointers, N < 0, C < 1, axis not 0/1, epsilon negative or NaN),
+ * ALIGN (pointers not 16-byte aligned, the row pitch -- C for axis = 1, N for axis = 0 --
+ * times the element size not a multiple of 16 bytes, or axis = 0 with N not a multiple of 8),
+ * UNSUPPORTED (axis = 1 with C > 16384), CUDA.
+ */
+bsmm_status bsmm_layer_norm(const void *x, const float *g, const float *b, void *y, int N, int C, int axis,
+                            float epsilon, int relu, bsmm_dtype t, void *stream);
+
 /* Kernel family for later calls on this handle (testing / comparison). */
 bsmm_status bsmm_set_kernel(bsmm_t h, bsmm_kernel which);
 

@@ -70,3 +70,22 @@ def test_null_handle_rejected():
 def test_selftest_rejects_bad_arguments_on_host():
     L = bsmm.lib()
     assert L.bsmm_selftest_wait_timeout(None, 1000, None) == bsmm.ERR_INVALID
+
+
+def test_layer_norm_rejects_bad_arguments_on_host():
+    """Every case fails validation before anything is enqueued (the pointers are never used)."""
+    L = bsmm.lib()
+    A, B = 0x10000, 0x20000                     # 16-byte aligned stand-ins, never dereferenced
+    assert L.bsmm_layer_norm(None, A, A, A, 4, 8, 1, 1e-6, 0, 2, None) == bsmm.ERR_INVALID
+    assert L.bsmm_layer_norm(None, None, None, None, 0, 8, 1, 1e-6, 0, 2, None) == bsmm.OK   # N = 0
+    assert L.bsmm_layer_norm(A, A, A, B, 4, 0, 1, 1e-6, 0, 2, None) == bsmm.ERR_INVALID      # C < 1
+    assert L.bsmm_layer_norm(A, A, A, B, -1, 8, 1, 1e-6, 0, 2, None) == bsmm.ERR_INVALID     # N < 0
+    assert L.bsmm_layer_norm(A, A, A, B, 4, 8, 2, 1e-6, 0, 2, None) == bsmm.ERR_INVALID      # axis
+    assert L.bsmm_layer_norm(A, A, A, B, 4, 8, 1, -1.0, 0, 2, None) == bsmm.ERR_INVALID      # epsilon
+    assert L.bsmm_layer_norm(A, A, A, B, 4, 8, 1, float("nan"), 0, 2, None) == bsmm.ERR_INVALID
+    assert L.bsmm_layer_norm(A + 8, A, A, B, 4, 8, 1, 1e-6, 0, 2, None) == bsmm.ERR_ALIGN   # x
+    assert L.bsmm_layer_norm(A, A, A + 4, B, 4, 8, 1, 1e-6, 0, 2, None) == bsmm.ERR_ALIGN   # b
+    assert L.bsmm_layer_norm(A, A, A, B, 4, 12, 1, 1e-6, 0, 2, None) == bsmm.ERR_ALIGN      # C * 2 % 16
+    assert L.bsmm_layer_norm(A, A, A, B, 12, 8, 0, 1e-6, 0, 2, None) == bsmm.ERR_ALIGN      # N * 2 % 16
+    assert L.bsmm_layer_norm(A, A, A, B, 12, 8, 0, 1e-6, 0, 0, None) == bsmm.ERR_ALIGN      # fp32, N % 8
+    assert L.bsmm_layer_norm(A, A, A, B, 4, 16392, 1, 1e-6, 0, 2, None) == bsmm.ERR_UNSUPPORTED
