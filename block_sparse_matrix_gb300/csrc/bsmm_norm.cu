@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(kLnThreads) k_ln_rows(const T *__restrict__ x,
 {
     constexpr int VEC = 16 / sizeof(T);
     __shared__ float red[kLnThreads / 32];
+    tc::pdl_launch_dependents();                       // holds no tensor memory: the next kernel may start
+    tc::pdl_wait();                                    // the previous kernel's writes are visible
     const T *xr = x + (size_t)blockIdx.x * C;
     T *yr = y + (size_t)blockIdx.x * C;
     float v[IT][VEC];
@@ -181,6 +183,8 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
     __shared__ float acc[kLnThreads / 8][kLnCols];                    // per row group, per column
     __shared__ float part1[kLnCols], part2[kLnCols];                  // this CTA's partial sums
     __shared__ float stat[2][kLnCols];                                // cluster-wide mean, 1 / std
+    tc::pdl_launch_dependents();                       // holds no tensor memory: the next kernel may start
+    tc::pdl_wait();                                    // the previous kernel's writes are visible
     const uint32_t rank = tc::cluster_ctarank();
     const int tile = blockIdx.x / kLnSplit;
     const int rg = threadIdx.x / 8, cc = threadIdx.x & 7;
@@ -301,24 +305,44 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
 
 constexpr int kLnCacheMax = 160 * 1024;            // axis = 0: largest slice kept in shared memory
 
-template <typename T, int IT>
-void launch_rows(const void *x, const float *g, const float *b, void *y, int N, int C, float eps, int relu,
-                 cudaStream_t s)
+// Launch with programmatic stream serialisation: the kernel's launch overlaps the previous
+// kernel's tail; it waits in griddepcontrol.wait before reading anything.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_ln(void (*kern)(KArgs...), int grid, size_t smem, cudaStream_t s, Args... args)
 {
-    k_ln_rows<T, IT><<<N, kLnThreads, 0, s>>>(static_cast<const T *>(x), g, b, static_cast<T *>(y), C, eps, relu);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kLnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename T, int IT>
+cudaError_t launch_rows(const void *x, const float *g, const float *b, void *y, int N, int C, float eps, int relu,
+                        cudaStream_t s)
+{
+    return launch_pdl_ln(k_ln_rows<T, IT>, N, 0, s, static_cast<const T *>(x), g, b, static_cast<T *>(y), C, eps,
+                         relu);
 }
 
 template <typename T>
 cudaError_t launch_ln(const void *x, const float *g, const float *b, void *y, int N, int C, int axis, float eps,
                       int relu, cudaStream_t s)
 {
+    cudaError_t le;
     if (axis == 1) {
         const int need = (C + kLnThreads * (16 / (int)sizeof(T)) - 1) / (kLnThreads * (16 / (int)sizeof(T)));
-        if (need <= 1) launch_rows<T, 1>(x, g, b, y, N, C, eps, relu, s);
-        else if (need <= 2) launch_rows<T, 2>(x, g, b, y, N, C, eps, relu, s);
-        else if (need <= 4) launch_rows<T, 4>(x, g, b, y, N, C, eps, relu, s);
-        else if (need <= 8) launch_rows<T, 8>(x, g, b, y, N, C, eps, relu, s);
-        else launch_rows<T, 16>(x, g, b, y, N, C, eps, relu, s);
+        if (need <= 1) le = launch_rows<T, 1>(x, g, b, y, N, C, eps, relu, s);
+        else if (need <= 2) le = launch_rows<T, 2>(x, g, b, y, N, C, eps, relu, s);
+        else if (need <= 4) le = launch_rows<T, 4>(x, g, b, y, N, C, eps, relu, s);
+        else if (need <= 8) le = launch_rows<T, 8>(x, g, b, y, N, C, eps, relu, s);
+        else le = launch_rows<T, 16>(x, g, b, y, N, C, eps, relu, s);
     } else {
         const int tiles = (N + kLnCols - 1) / kLnCols;
         const int rows = (C + kLnSplit - 1) / kLnSplit;
@@ -334,15 +358,15 @@ cudaError_t launch_ln(const void *x, const float *g, const float *b, void *y, in
                 if (e != cudaSuccess) return e;
                 attr_set.store(dev);
             }
-            kern<<<tiles * kLnSplit, kLnThreads, slice, s>>>(static_cast<const T *>(x), g, b, static_cast<T *>(y), C,
-                                                             N, eps, relu);
+            le = launch_pdl_ln(kern, tiles * kLnSplit, slice, s, static_cast<const T *>(x), g, b, static_cast<T *>(y), C,
+                               N, eps, relu);
         } else {
-            k_ln_cols<T, false><<<tiles * kLnSplit, kLnThreads, 0, s>>>(static_cast<const T *>(x), g, b,
-                                                                        static_cast<T *>(y), C, N, eps, relu);
+            le = launch_pdl_ln(k_ln_cols<T, false>, tiles * kLnSplit, 0, s, static_cast<const T *>(x), g, b,
+                               static_cast<T *>(y), C, N, eps, relu);
         }
     }
     g_bsmm_launches += 1;
-    return cudaGetLastError();
+    return le;
 }
 
 } // namespace
