@@ -29,6 +29,7 @@ constexpr int kLnThreads = 256;
 constexpr int kLnMaxC = 16384;          // axis = 1: at most 16 vectors of 16 bytes per thread
 constexpr int kLnSplit = 8;             // axis = 0: CTAs per cluster along the features
 constexpr int kLnCols = 64;             // axis = 0: samples (columns) per cluster
+constexpr int kLnCacheMax = 160 * 1024; // axis = 0: dynamic shared memory of a CTA (slice + g, b)
 
 template <typename T> __device__ __forceinline__ float ld1(const T *p);
 template <> __device__ __forceinline__ float ld1<float>(const float *p) { return *p; }
@@ -179,7 +180,7 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
           float eps, int relu)
 {
     extern __shared__ __align__(16) uint8_t ln_smem[];
-    Vec8<T> *slice = reinterpret_cast<Vec8<T> *>(ln_smem);          // [rows][8] vectors
+    Vec8<T> *slice = reinterpret_cast<Vec8<T> *>(ln_smem);          // [rows][8] vectors (CACHE)
     __shared__ float acc[kLnThreads / 8][kLnCols];                    // per row group, per column
     __shared__ float part1[kLnCols], part2[kLnCols];                  // this CTA's partial sums
     __shared__ float stat[2][kLnCols];                                // cluster-wide mean, 1 / std
@@ -194,6 +195,13 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
     const int r0 = (int)rank * rows, r1 = min(C, r0 + rows);
     const int nr = max(0, r1 - r0);
     constexpr int RG = kLnThreads / 8;                                 // 32 row groups
+    // g, b of this CTA's rows, staged once so the output pass does not wait on them per row
+    float *sg = reinterpret_cast<float *>(ln_smem + (CACHE ? (size_t)rows * sizeof(Vec8<T>) * 8 : 0));
+    float *sb = sg + rows;
+    for (int i = threadIdx.x; i < nr; i += kLnThreads) {
+        sg[i] = g[r0 + i];
+        sb[i] = b[r0 + i];
+    }
     auto gload = [&](int f) { return *reinterpret_cast<const Vec8<T> *>(x + (size_t)f * N + n0); };
 
     // pass 1: sums.  With CACHE the whole slice is first copied to shared memory with
@@ -289,7 +297,7 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
             const int f = r0 + i;
             float v[8];
             unpack8<T>(CACHE ? slice[i * 8 + cc] : gload(f), v);
-            const float gf = g[f], bf = b[f];
+            const float gf = sg[i], bf = sb[i];
             Vec8<T> o;
             T *e = reinterpret_cast<T *>(&o);
 #pragma unroll
@@ -303,7 +311,6 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
     tc::cluster_sync();                                // no CTA leaves while a peer reads its partials
 }
 
-constexpr int kLnCacheMax = 160 * 1024;            // axis = 0: largest slice kept in shared memory
 
 // Launch with programmatic stream serialisation: the kernel's launch overlaps the previous
 // kernel's tail; it waits in griddepcontrol.wait before reading anything.
@@ -347,7 +354,8 @@ cudaError_t launch_ln(const void *x, const float *g, const float *b, void *y, in
         const int tiles = (N + kLnCols - 1) / kLnCols;
         const int rows = (C + kLnSplit - 1) / kLnSplit;
         const size_t slice = (size_t)rows * kLnCols * sizeof(T);
-        if (slice <= (size_t)kLnCacheMax) {
+        const size_t gb = (size_t)rows * 2 * sizeof(float);             // staged g, b
+        if (slice + gb <= (size_t)kLnCacheMax) {
             auto kern = k_ln_cols<T, true>;
             static std::atomic<int> attr_set{-1};      // device whose limit has been raised
             int dev = 0;
@@ -358,11 +366,22 @@ cudaError_t launch_ln(const void *x, const float *g, const float *b, void *y, in
                 if (e != cudaSuccess) return e;
                 attr_set.store(dev);
             }
-            le = launch_pdl_ln(kern, tiles * kLnSplit, slice, s, static_cast<const T *>(x), g, b, static_cast<T *>(y), C,
-                               N, eps, relu);
-        } else {
-            le = launch_pdl_ln(k_ln_cols<T, false>, tiles * kLnSplit, 0, s, static_cast<const T *>(x), g, b,
+            le = launch_pdl_ln(kern, tiles * kLnSplit, slice + gb, s, static_cast<const T *>(x), g, b,
                                static_cast<T *>(y), C, N, eps, relu);
+        } else {
+            auto kern = k_ln_cols<T, false>;
+            static std::atomic<int> attr_set{-1};
+            int dev = 0;
+            cudaError_t e = cudaGetDevice(&dev);
+            if (e != cudaSuccess) return e;
+            if (attr_set.load() != dev) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kLnCacheMax);
+                if (e != cudaSuccess) return e;
+                attr_set.store(dev);
+            }
+            if (gb > (size_t)kLnCacheMax) return cudaErrorInvalidValue;   // C beyond 8 x 20480 rows
+            le = launch_pdl_ln(kern, tiles * kLnSplit, gb, s, static_cast<const T *>(x), g, b, static_cast<T *>(y), C,
+                               N, eps, relu);
         }
     }
     g_bsmm_launches += 1;
@@ -385,6 +404,8 @@ extern "C" bsmm_status bsmm_layer_norm(const void *x, const float *g, const floa
     if (((size_t)(axis == 1 ? C : N) * e) % 16u) return BSMM_ERR_ALIGN;
     if (axis == 0 && N % 8) return BSMM_ERR_ALIGN;     // (C, N): 8 samples per thread
     if (axis == 1 && C > kLnMaxC) return BSMM_ERR_UNSUPPORTED;
+    if (axis == 0 && (size_t)((C + kLnSplit - 1) / kLnSplit) * 2 * sizeof(float) > (size_t)kLnCacheMax)
+        return BSMM_ERR_UNSUPPORTED;                   // the staged g, b of a CTA's rows must fit
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err;
     if (t == BSMM_F32) err = launch_ln<float>(x, g, b, y, N, C, axis, epsilon, relu, s);

@@ -179,7 +179,7 @@ bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *dy, float *d
  * Errors: INVALID (null pointers, N < 0, C < 1, axis not 0/1, epsilon negative or NaN),
  * ALIGN (pointers not 16-byte aligned, the row pitch -- C for axis = 1, N for axis = 0 --
  * times the element size not a multiple of 16 bytes, or axis = 0 with N not a multiple of 8),
- * UNSUPPORTED (axis = 1 with C > 16384), CUDA.
+ * UNSUPPORTED (axis = 1 with C > 16384, axis = 0 with C > 163840), CUDA.
  */
 bsmm_status bsmm_layer_norm(const void *x, const float *g, const float *b, void *y, int N, int C, int axis,
                             float epsilon, int relu, bsmm_dtype t, void *stream);
