@@ -6,25 +6,24 @@
 // updat dw[b] = x[:, c_b blk]^T . dy[:, k_b blk] and its grouped form
 // (group_param_grads) summed over up to 8 timesteps.
 //
-// Mapping onto the MMA (D[M x N] += A[M x K] . B[K x N], M = 128):
-//   fprop/bprop: M = 128 minibatch rows, N = one output block (bs), K = one input
-//     block (bs).  A is the activation panel (K-major for (N,C) activations,
-//     MN-major for (C,N)), B is the weight block (MN-major for fprop, K-major for
-//     bprop, i.e. W^T is read in place).  A CTA owns a window of up to 256/bs output
-//     blocks (fprop: block columns, bprop: block rows) for one 128-row minibatch
-//     tile; it walks the union of their source blocks, loads each activation panel
-//     once and multiplies it with every weight block of the window that uses it.
-//     Each output block has its own accumulator columns in TMEM, so bprop needs no
-//     atomics, and output blocks without any weight block are written as zeros.
-//   updat: M = 128 = up to 128/bs blocks of one block column stacked, N = bs,
-//     K = the minibatch (and the timesteps of a group).  The dy panel of the column
-//     is shared by the whole stack.
-//   bs = 8 runs on 16 x 16 coarse blocks: each coarse block is assembled in shared
-//     memory from its four 8 x 8 weight blocks, absent ones loaded from a zero tile,
-//     because an M = 128 MMA needs N >= 16 and K = 16.
-//
-// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 issues MMAs (one lane),
-// warps 2..5 drain TMEM and write the outputs.  Every mbarrier wait is bounded.
+// Kernel families (the dispatch is in fbd_try and tc_updat near the end of this file):
+//   k_tc_fbd_pair    fprop/bprop, bs = 32, dense layouts, minibatch > 64: CTA pairs with
+//                    two-SM MMAs (M256 x N256 x K16) on tiles of 8 output blocks x 256 rows,
+//                    absent blocks as zero tiles.
+//   k_tc_fbd_split   fprop/bprop, bs = 32, dense layouts, minibatch <= 64: clusters of 4 CTAs
+//                    split a 4-block x 64-row tile's sources and reduce in distributed shared
+//                    memory.
+//   k_tc_fb          fprop/bprop, any block size: a CTA owns a window of output blocks for a
+//                    128-row tile and issues one N = bs MMA per present block (bs = 8 runs on
+//                    16 x 16 coarse blocks with zero tiles).
+//   k_tc_updat_pair  updat, bs = 32, dense layouts: CTA pairs with two-SM MMAs on 256 x 256
+//                    tiles of x^T.dy, persistent, double-buffered accumulators.
+//   k_tc_updat       updat, any block size: 128/bs blocks of one block column stacked along M.
+//   k_tc_fbd, k_tc_updat_dense   one-CTA forms of the dense tiles (fallback, and a second
+//                    implementation the tests compare with bit for bit).
+// All of them are warp-specialised (producer warps issue each stage's TMA loads as one
+// instruction, one thread issues the MMAs, producer or epilogue warps drain TMEM), launch
+// with programmatic dependent launch, and bound every mbarrier wait.
 #include "bsmm_internal.cuh"
 #include "tc_common.cuh"
 
