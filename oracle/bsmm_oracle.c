@@ -15,6 +15,8 @@
  *   - w_shape: one bs x bs weight block per nonzero layout entry.
  *   - __call__(I, W): y = I . W with W the block-sparse (C x K) weight.
  *   - identity_init: identity initialisation of the weight blocks.
+ *   - l2_normalize: weight normalisation of the block-sparse weight (and its
+ *     gradient), near the end of this file.
  *   - group_param_grads: the weight gradients of up to 8 timesteps sharing one
  *     weight are summed (cast32: in float32 or wider).
  * and its section "blocksparse.norms" for layer_norm (at the end of this file).
@@ -359,4 +361,96 @@ void oracle_layer_norm(const double *x, const double *g, const double *b, double
             *act_ptr(y, n, f, N, C, axis) = o;
         }
     }
+}
+
+/*
+ * l2_normalize(W, gain=None, epsilon=1e-6, dtype)  [blocksparse README, section "API
+ * Documentation: blocksparse.matmul": a BlocksparseMatMul method for weight normalisation].
+ * The page gives the signature only; the readings taken:
+ *   - the norm belongs to one output feature f = k*bs + j and runs over its whole incoming
+ *     weight vector, column f of the dense C x K weight: w[b][i][j] for every block b of
+ *     block column k and every i (weight normalisation of one output unit);
+ *   - epsilon is a lower bound on the squared norm, as in TensorFlow's l2_normalize:
+ *       s_f = sum of w^2 over the column,  y[b][i][j] = gain[f] * w[b][i][j] / sqrt(max(s_f, epsilon));
+ *   - gain, when given, holds one value per output feature (K of them); without it the gain is 1;
+ *   - dtype is the type the result is delivered in (rounding is the caller's).
+ * Blocks of a column are visited in increasing c, rows i in increasing order.
+ */
+void oracle_l2_normalize(const uint8_t *L, int R, int S, int bs, const double *w, const double *gain,
+                         double epsilon, double *y)
+{
+    int32_t *bid = block_id_map(L, R, S);
+    const int64_t bb = (int64_t)bs * bs;
+    for (int k = 0; k < S; ++k)
+        for (int j = 0; j < bs; ++j) {
+            double s = 0.0;
+            for (int c = 0; c < R; ++c) {
+                const int32_t b = bid[(size_t)c * S + k];
+                if (b < 0)
+                    continue;
+                for (int i = 0; i < bs; ++i) {
+                    const double v = w[b * bb + (int64_t)i * bs + j];
+                    s += v * v;
+                }
+            }
+            const double g = gain ? gain[(int64_t)k * bs + j] : 1.0;
+            const double norm = sqrt(s > epsilon ? s : epsilon);
+            for (int c = 0; c < R; ++c) {
+                const int32_t b = bid[(size_t)c * S + k];
+                if (b < 0)
+                    continue;
+                for (int i = 0; i < bs; ++i) {
+                    const int64_t o = b * bb + (int64_t)i * bs + j;
+                    y[o] = g * w[o] / norm;
+                }
+            }
+        }
+    free(bid);
+}
+
+/*
+ * Gradient of l2_normalize, written out from the definition above by the chain rule.  With
+ * rho = 1/sqrt(max(s_f, epsilon)) and D_f = sum over the column of dy * w:
+ *   d y[m] / d w[i]  = gain * (rho * [m == i] - rho^3 * w[m] * w[i])  when s_f >= epsilon
+ *                      (the squared norm is the larger argument of the max; ties go to it, as
+ *                      TensorFlow's maximum does), and gain * rho * [m == i] otherwise;
+ *   dw[i]     = gain * rho * (dy[i] - [s_f >= epsilon] * rho^2 * D_f * w[i]);
+ *   dgain[f]  = rho * D_f  (the derivative with respect to gain, also when no gain was given).
+ * dgain may be NULL.
+ */
+void oracle_l2_normalize_grad(const uint8_t *L, int R, int S, int bs, const double *w, const double *gain,
+                              double epsilon, const double *dy, double *dw, double *dgain)
+{
+    int32_t *bid = block_id_map(L, R, S);
+    const int64_t bb = (int64_t)bs * bs;
+    for (int k = 0; k < S; ++k)
+        for (int j = 0; j < bs; ++j) {
+            double s = 0.0, d = 0.0;
+            for (int c = 0; c < R; ++c) {
+                const int32_t b = bid[(size_t)c * S + k];
+                if (b < 0)
+                    continue;
+                for (int i = 0; i < bs; ++i) {
+                    const int64_t o = b * bb + (int64_t)i * bs + j;
+                    s += w[o] * w[o];
+                    d += dy[o] * w[o];
+                }
+            }
+            const int64_t f = (int64_t)k * bs + j;
+            const double g = gain ? gain[f] : 1.0;
+            const double rho = 1.0 / sqrt(s > epsilon ? s : epsilon);
+            const double cw = s >= epsilon ? rho * rho * d : 0.0;
+            for (int c = 0; c < R; ++c) {
+                const int32_t b = bid[(size_t)c * S + k];
+                if (b < 0)
+                    continue;
+                for (int i = 0; i < bs; ++i) {
+                    const int64_t o = b * bb + (int64_t)i * bs + j;
+                    dw[o] = g * rho * (dy[o] - cw * w[o]);
+                }
+            }
+            if (dgain)
+                dgain[f] = rho * d;
+        }
+    free(bid);
 }

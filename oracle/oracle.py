@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
 benchmark's CPU-baseline leg may import this module.  It shares no code with
 the CUDA library.  Every function follows the blocksparse README, section
 "API Documentation: blocksparse.matmul" (BlocksparseMatMul, block_coord,
-identity_init, __call__, group_param_grads), or its "blocksparse.norms" section
+identity_init, l2_normalize, __call__, group_param_grads), or its "blocksparse.norms" section
 (layer_norm); the C file states the readings taken where the page is silent.
 
 Inputs are numpy arrays; floating-point inputs are converted to float64
@@ -60,6 +60,8 @@ def _load():
         lib.oracle_bprop_at.argtypes = [_u8, _c, _c, _c, _d, _d, _c, _c, _i64, _i64, _l, _d]
         lib.oracle_updat_at.argtypes = [_u8, _c, _c, _c, _d, _d, _c, _c, _i64, _i64, _i64, _l, _d]
         lib.oracle_layer_norm.argtypes = [_d, _d, _d, _d, _c, _c, _c, ctypes.c_double, _c]
+        lib.oracle_l2_normalize.argtypes = [_u8, _c, _c, _c, _d, _d, ctypes.c_double, _d]
+        lib.oracle_l2_normalize_grad.argtypes = [_u8, _c, _c, _c, _d, _d, ctypes.c_double, _d, _d, _d]
         lib.oracle_max_threads.restype = _c
         _lib = lib
     return _lib
@@ -234,3 +236,40 @@ def layer_norm(x, g, b, axis: int = 1, epsilon: float = 1e-6, relu: bool = False
     y = np.empty_like(x)
     _load().oracle_layer_norm(_p(x, _d), _p(g, _d), _p(b, _d), _p(y, _d), N, C, axis, float(epsilon), int(relu))
     return y
+
+
+def _gain(gain, S: int, bs: int):
+    if gain is None:
+        return None
+    g = _f64(gain).reshape(-1)
+    assert g.size == S * bs
+    return g
+
+
+def l2_normalize(L, bs: int, w, gain=None, epsilon: float = 1e-6) -> np.ndarray:
+    """BlocksparseMatMul.l2_normalize (README, "API Documentation: blocksparse.matmul"): each
+    output feature's incoming weights, over every block of its block column, scaled to unit L2
+    norm (squared norm bounded below by epsilon) and multiplied by gain[f] (K values, or 1)."""
+    L = _lay(L)
+    w = _f64(w)
+    assert w.shape == (nnz(L), bs, bs)
+    g = _gain(gain, L.shape[1], bs)
+    y = np.empty_like(w)
+    _load().oracle_l2_normalize(_p(L, _u8), L.shape[0], L.shape[1], bs, _p(w, _d),
+                                None if g is None else _p(g, _d), float(epsilon), _p(y, _d))
+    return y
+
+
+def l2_normalize_grad(L, bs: int, w, dy, gain=None, epsilon: float = 1e-6):
+    """Gradient of l2_normalize: (dw, dgain) for the upstream gradient dy of its output; dgain
+    has one entry per output feature (the derivative with respect to gain, also without one)."""
+    L = _lay(L)
+    w, dy = _f64(w), _f64(dy)
+    assert w.shape == (nnz(L), bs, bs) and dy.shape == w.shape
+    g = _gain(gain, L.shape[1], bs)
+    dw = np.empty_like(w)
+    dgain = np.empty(L.shape[1] * bs)
+    _load().oracle_l2_normalize_grad(_p(L, _u8), L.shape[0], L.shape[1], bs, _p(w, _d),
+                                     None if g is None else _p(g, _d), float(epsilon), _p(dy, _d),
+                                     _p(dw, _d), _p(dgain, _d))
+    return dw, dgain

@@ -341,3 +341,108 @@ def test_layer_norm_matches_numpy_definition():
     eps = 1e-6
     want = g * (x - x.mean(axis=1, keepdims=True)) / np.sqrt(x.var(axis=1, keepdims=True) + eps) + b
     assert np.allclose(o.layer_norm(x, g, b, axis=1, epsilon=eps), want, rtol=1e-12, atol=1e-12)
+
+
+# --- l2_normalize (README, "API Documentation: blocksparse.matmul": weight normalisation) ---
+
+def _wn_inputs(R, S, bs, p, seed, scale=1.0):
+    L = rand_layout(R, S, p, seed)
+    L[0, 0] = 1                                   # at least one block
+    rng = np.random.default_rng(seed + 100)
+    w = rng.standard_normal((int(L.sum()), bs, bs)) * scale
+    gain = rng.uniform(0.5, 2.0, S * bs) * np.where(rng.random(S * bs) < 0.2, -1.0, 1.0)
+    return L, w, gain
+
+
+def test_l2_normalize_hand_example():
+    """Block column 0 holds two all-ones 8x8 blocks: each of its features has 16 ones, norm 4.
+    Block column 1 holds 2*I: each feature has the single entry 2, norm 2."""
+    L = np.array([[1, 0], [1, 1]], np.uint8)      # ids: (0,0) -> 0, (1,0) -> 1, (1,1) -> 2
+    w = np.stack([np.ones((8, 8)), np.ones((8, 8)), 2.0 * np.eye(8)])
+    gain = np.arange(16.0) + 1.0
+    y = o.l2_normalize(L, 8, w)
+    assert np.array_equal(y[0], np.full((8, 8), 0.25)) and np.array_equal(y[1], y[0])
+    assert np.array_equal(y[2], np.eye(8))
+    yg = o.l2_normalize(L, 8, w, gain)
+    assert np.array_equal(yg[0], np.tile(0.25 * gain[:8], (8, 1)))
+    assert np.array_equal(yg[2], np.diag(gain[8:]))
+
+
+def test_l2_normalize_unit_feature_norms():
+    """Without a gain every output feature of the dense weight has unit norm; features of empty
+    block columns stay absent (zero)."""
+    L, w, _ = _wn_inputs(9, 7, 8, 0.4, 1)
+    L2 = L.copy()
+    L2[:, 3] = 0                                   # one empty block column
+    w2 = w[: int(L2.sum())]
+    Yd = o.densify(L2, 8, o.l2_normalize(L2, 8, w2))
+    norms = np.linalg.norm(Yd, axis=0)
+    present = np.repeat(L2.any(axis=0), 8)
+    assert np.allclose(norms[present], 1.0, rtol=1e-13) and np.array_equal(norms[~present], np.zeros((~present).sum()))
+
+
+def test_l2_normalize_matches_dense_numpy():
+    """Against column norms of the dense weight computed by numpy (a route through densify, not
+    through the oracle's block loop): a norm over rows instead of features, or a block of the
+    wrong column, fails here."""
+    for bs, seed in ((8, 2), (16, 3), (32, 4)):
+        L, w, gain = _wn_inputs(5, 6, bs, 0.5, seed)
+        eps = 1e-6
+        Wd = o.densify(L, bs, w)
+        want = Wd * gain / np.sqrt(np.maximum((Wd ** 2).sum(axis=0), eps))
+        got = o.densify(L, bs, o.l2_normalize(L, bs, w, gain, epsilon=eps))
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-15)
+
+
+def test_l2_normalize_epsilon_bounds_the_squared_norm():
+    """A feature whose squared norm is below epsilon is divided by sqrt(epsilon) instead."""
+    L, w, gain = _wn_inputs(4, 4, 8, 0.6, 5, scale=1e-4)   # squared norms ~ 1e-7 * 32
+    eps = 0.25
+    assert np.allclose(o.l2_normalize(L, 8, w, gain, epsilon=eps),
+                       w * gain.reshape(-1, 8)[np.argwhere(L)[:, 1]][:, None, :] / 0.5, rtol=1e-15, atol=0)
+
+
+def test_l2_normalize_scale_invariance():
+    L, w, gain = _wn_inputs(6, 5, 16, 0.5, 6)
+    assert np.allclose(o.l2_normalize(L, 16, 37.5 * w, gain), o.l2_normalize(L, 16, w, gain), rtol=1e-13)
+
+
+def _wn_loss(L, bs, w, dy, gain, eps):
+    return float((o.l2_normalize(L, bs, w, gain, epsilon=eps) * dy).sum())
+
+
+@pytest.mark.parametrize("regime", ["norm", "epsilon"])
+def test_l2_normalize_grad_finite_differences(regime):
+    """dw and dgain against central differences of sum(dy * l2_normalize(w, gain)), in both
+    branches of the max (squared norm above and below epsilon)."""
+    scale, eps = (1.0, 1e-6) if regime == "norm" else (1e-3, 1.0)
+    L, w, gain = _wn_inputs(4, 3, 8, 0.6, 7, scale=scale)
+    dy = np.random.default_rng(8).standard_normal(w.shape)
+    dw, dgain = o.l2_normalize_grad(L, 8, w, dy, gain, epsilon=eps)
+    rng = np.random.default_rng(9)
+    h = 1e-6 * scale
+    for _ in range(12):
+        idx = tuple(rng.integers(0, n) for n in w.shape)
+        wp, wm = w.copy(), w.copy()
+        wp[idx] += h
+        wm[idx] -= h
+        fd = (_wn_loss(L, 8, wp, dy, gain, eps) - _wn_loss(L, 8, wm, dy, gain, eps)) / (2 * h)
+        assert abs(fd - dw[idx]) <= 1e-6 * max(1.0, abs(fd)), (idx, fd, dw[idx])
+    for f in rng.integers(0, gain.size, 8):
+        gp, gm = gain.copy(), gain.copy()
+        gp[f] += 1e-6
+        gm[f] -= 1e-6
+        fd = (_wn_loss(L, 8, w, dy, gp, eps) - _wn_loss(L, 8, w, dy, gm, eps)) / 2e-6
+        assert abs(fd - dgain[f]) <= 1e-6 * max(1.0, abs(fd))
+
+
+def test_l2_normalize_grad_orthogonal_to_w():
+    """Without a gain and above epsilon, the output does not change along w itself, so each
+    feature's dw is orthogonal to its weights; dgain does not depend on whether a gain was given."""
+    L, w, _ = _wn_inputs(7, 6, 8, 0.5, 10)
+    dy = np.random.default_rng(11).standard_normal(w.shape)
+    dw, dgain = o.l2_normalize_grad(L, 8, w, dy)
+    dots = (o.densify(L, 8, dw) * o.densify(L, 8, w)).sum(axis=0)
+    assert np.allclose(dots, 0.0, atol=1e-12)
+    _, dgain1 = o.l2_normalize_grad(L, 8, w, dy, np.ones(6 * 8))
+    assert np.array_equal(dgain, dgain1)
