@@ -167,10 +167,10 @@ def traffic_for(kernel_pass):
 
 
 def source_sha():
-    """Hash of the sources of the step's kernels (layer_norm is not part of the step)."""
+    """Hash of the sources of the step's kernels (the normalisations are not part of the step)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_sparse_matrix_gb300", "csrc")
-    for name in sorted(n for n in os.listdir(csrc) if n != "bsmm_norm.cu"):
+    for name in sorted(n for n in os.listdir(csrc) if n not in ("bsmm_norm.cu", "bsmm_wnorm.cu")):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -477,10 +477,39 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _time_launches(fn, steps, warmup):
+    """Device microseconds per call of fn(i): chunks of launches queued behind a device sleep
+    that covers their enqueueing, so the GPU never waits for the host inside a chunk."""
+    for i in range(max(3, warmup)):
+        fn(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(20):
+        fn(i)
+    host_s = (time.perf_counter() - t0) / 20
+    torch.cuda.synchronize()
+    chunk = 50
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(0, steps, chunk)]
+    for c, c0 in enumerate(range(0, steps, chunk)):
+        torch.cuda._sleep(int(host_s * 1.5 * chunk * 2.1e9) + 100000)
+        ev[c][0].record()
+        for i in range(c0, min(steps, c0 + chunk)):
+            fn(i)
+        ev[c][1].record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(e) for a, e in ev) * 1000 / steps
+
+
 def run_norm(args):
-    """layer_norm (README "blocksparse.norms") on the step's activation shape, N = 1024
-    samples of C = 4096 bf16 features, in both layouts; 16 rotating input/output sets
-    (256 MB > L2).  Bytes per launch = read x + write y + g, b.  One JSON line."""
+    """The normalisations around the step, each on its own.
+    layer_norm (README "blocksparse.norms") on the step's activation shape, N = 1024 samples of
+    C = 4096 bf16 features, in both layouts; 16 rotating input/output sets (256 MB > L2).  Bytes
+    per launch = read x + write y + g, b.
+    l2_normalize (README "blocksparse.matmul", weight normalisation) of the step's float32 weight
+    (hidden 4096, block 32, 50% dense) to bf16, and its gradient (bf16 dy -> float32 dw, dgain);
+    8 rotating sets (> L2).  Bytes per launch: read w (+ dy) + write y (or dw) + gain (+ dgain).
+    One JSON line."""
     from block_sparse_matrix_gb300 import bsmm
     dev = torch.device("cuda", 0)
     N, C, sets = 1024, 4096, 16
@@ -488,38 +517,42 @@ def run_norm(args):
     g = torch.randn(C, device=dev)
     b = torch.randn(C, device=dev)
     out = {}
+
+    def entry(us, byts):
+        gbs = byts / us / 1e3
+        return {"us": round(us, 3), "gbs": round(gbs, 1), "bytes": byts,
+                "roofline_frac": round(gbs / peaks["hbm_gbs"], 4)}
+
     for axis in (1, 0):
         shape = (N, C) if axis == 1 else (C, N)
         xs = [wk.normals(shape, 500 + i, 1.0, "bf16").to(dev) for i in range(sets)]
         ys = [torch.empty_like(x) for x in xs]
-        for i in range(max(3, args.warmup)):
-            bsmm.layer_norm(xs[i % sets], g, b, axis=axis, y=ys[i % sets])
-        torch.cuda.synchronize()
-        # host time per call, then chunks of launches queued behind a device sleep that covers
-        # their enqueueing, so the GPU never waits for the host inside a chunk
-        t0 = time.perf_counter()
-        for i in range(20):
-            bsmm.layer_norm(xs[i % sets], g, b, axis=axis, y=ys[i % sets])
-        host_s = (time.perf_counter() - t0) / 20
-        torch.cuda.synchronize()
-        chunk = 50
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(0, args.steps, chunk)]
-        for c, c0 in enumerate(range(0, args.steps, chunk)):
-            torch.cuda._sleep(int(host_s * 1.5 * chunk * 2.1e9) + 100000)
-            ev[c][0].record()
-            for i in range(c0, min(args.steps, c0 + chunk)):
-                bsmm.layer_norm(xs[i % sets], g, b, axis=axis, y=ys[i % sets])
-            ev[c][1].record()
-        torch.cuda.synchronize()
-        us = sum(a.elapsed_time(e) for a, e in ev) * 1000 / args.steps
-        byts = 2 * N * C * 2 + 2 * C * 4
-        gbs = byts / us / 1e3
-        out["axis%d" % axis] = {"us": round(us, 3), "gbs": round(gbs, 1), "bytes": byts,
-                                 "roofline_frac": round(gbs / peaks["hbm_gbs"], 4)}
-    print(json.dumps({"metric": "layer_norm GB/s (read x + write y) on 1 GB300", "unit": "GB/s",
+        us = _time_launches(lambda i: bsmm.layer_norm(xs[i % sets], g, b, axis=axis, y=ys[i % sets]),
+                            args.steps, args.warmup)
+        out["layer_norm_axis%d" % axis] = entry(us, 2 * N * C * 2 + 2 * C * 4)
+        del xs, ys
+
+    wl = wk.CONFIGS["cfg2_n1024"]
+    lay = wk.make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 1000 * wl.cfg)
+    m = bsmm.BlocksparseMatMul(lay, block_size=wl.bs, feature_axis=wl.feature_axis)
+    wsets = 8
+    ws = [wk.normals(m.w_shape, 700 + i, 0.02, "f32").to(dev) for i in range(wsets)]
+    ys = [torch.empty(m.w_shape, dtype=torch.bfloat16, device=dev) for _ in range(wsets)]
+    gain = torch.rand(m.K, device=dev) + 0.5
+    us = _time_launches(lambda i: m.l2_normalize(ws[i % wsets], gain, y=ys[i % wsets]), args.steps, args.warmup)
+    el = m.nnz * wl.bs * wl.bs
+    out["l2_normalize"] = entry(us, el * (4 + 2) + m.K * 4)
+    dws = [torch.empty(m.w_shape, dtype=torch.float32, device=dev) for _ in range(wsets)]
+    dgain = torch.empty(m.K, device=dev)
+    us = _time_launches(lambda i: m.l2_normalize_grad(ws[i % wsets], ys[i % wsets], gain, dw=dws[i % wsets],
+                                                      dgain=dgain), args.steps, args.warmup)
+    out["l2_normalize_grad"] = entry(us, el * (4 + 2 + 4) + 2 * m.K * 4)
+    m.close()
+    print(json.dumps({"metric": "normalisation GB/s (algorithmic bytes) on 1 GB300", "unit": "GB/s",
                       "value": round(min(v["gbs"] for v in out.values()), 1), "dtype": "bf16",
-                      "config": {"workload": "N=1024 samples x C=4096 features, bf16, g/b fp32, 16 rotating sets"},
+                      "config": {"workload": "layer_norm: N=1024 x C=4096 bf16, 16 rotating sets; "
+                                             "l2_normalize: hidden 4096, block 32, 50%% dense, %d blocks, "
+                                             "float32 w -> bf16, 8 rotating sets" % m.nnz},
                       "peak": peaks["hbm_gbs"], "peak_source": peak_src, "passes": out}), flush=True)
 
 
@@ -534,7 +567,7 @@ def main():
     ap.add_argument("--only", default="",
                     help="time a single pass (e.g. fprop_n1024) instead of the whole step; for kernel profiling")
     ap.add_argument("--norm", action="store_true",
-                    help="time layer_norm on the step's activation shape instead of the step")
+                    help="time layer_norm and l2_normalize (and its gradient) instead of the step")
     args = ap.parse_args()
     if args.norm:
         run_norm(args)

@@ -60,6 +60,8 @@ def lib():
             "bsmm_selftest_wait_timeout": [vp, ctypes.c_uint64, vp],
             "bsmm_updat_noalloc": [vp, vp, vp, vp, i, i, i, vp],
             "bsmm_layer_norm": [vp, vp, vp, vp, i, i, i, ctypes.c_float, i, i, vp],
+            "bsmm_l2_normalize": [vp, vp, vp, vp, ctypes.c_float, i, vp],
+            "bsmm_l2_normalize_grad": [vp, vp, vp, vp, vp, vp, ctypes.c_float, i, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -156,6 +158,16 @@ def bsmm_updat_noalloc(h, x, dy, dw, N: int, accumulate: bool = False, stream=No
                                     _stream(stream)), "bsmm_updat_noalloc")
 
 
+def bsmm_l2_normalize(h, w, gain, y, epsilon: float = 1e-6, stream=None):
+    _check(lib().bsmm_l2_normalize(h, _ptr(w), _ptr(gain), _ptr(y), float(epsilon), _DT[y.dtype], _stream(stream)),
+           "bsmm_l2_normalize")
+
+
+def bsmm_l2_normalize_grad(h, w, gain, dy, dw, dgain, epsilon: float = 1e-6, stream=None):
+    _check(lib().bsmm_l2_normalize_grad(h, _ptr(w), _ptr(gain), _ptr(dy), _ptr(dw), _ptr(dgain), float(epsilon),
+                                        _DT[dy.dtype], _stream(stream)), "bsmm_l2_normalize_grad")
+
+
 def bsmm_sync_status(h, stream=None):
     _check(lib().bsmm_sync_status(h, _stream(stream)), "bsmm_sync_status")
 
@@ -249,6 +261,40 @@ class BlocksparseMatMul:
         _dev(w, "w")
         bsmm_identity_init(self._h, w)
         return w
+
+    def _wn_args(self, w, gain):
+        _dev(w, "w")
+        if w.dtype != torch.float32 or tuple(w.shape) != self.w_shape:
+            raise ValueError("w must be float32 of shape %s" % (self.w_shape,))
+        if gain is not None:
+            _dev(gain, "gain")
+            if gain.dtype != torch.float32 or gain.numel() != self.K:
+                raise ValueError("gain must be float32 with K = %d values" % self.K)
+
+    def l2_normalize(self, w, gain=None, epsilon=1e-6, dtype=torch.float32, y=None, stream=None):
+        """Weight normalisation (README: l2_normalize(W, gain=None, epsilon=1e-6, dtype)): every
+        output feature's incoming weights scaled to unit L2 norm (squared norm at least epsilon),
+        times gain[f]; returned in dtype.  y may be w for float32."""
+        self._wn_args(w, gain)
+        if y is None:
+            y = torch.empty(self.w_shape, dtype=dtype, device=w.device)
+        _dev(y, "y")
+        bsmm_l2_normalize(self._h, w, gain, y, epsilon, stream)
+        return y
+
+    def l2_normalize_grad(self, w, dy, gain=None, epsilon=1e-6, dw=None, dgain=None, stream=None):
+        """(dw, dgain): gradient of l2_normalize for the gradient dy of its output (dy in the
+        output's dtype, dw and dgain float32; dgain has K values)."""
+        self._wn_args(w, gain)
+        _dev(dy, "dy")
+        if tuple(dy.shape) != self.w_shape:
+            raise ValueError("dy must have shape %s" % (self.w_shape,))
+        if dw is None:
+            dw = torch.empty(self.w_shape, dtype=torch.float32, device=w.device)
+        if dgain is None:
+            dgain = torch.empty(self.K, dtype=torch.float32, device=w.device)
+        bsmm_l2_normalize_grad(self._h, w, gain, dy, dw, dgain, epsilon, stream)
+        return dw, dgain
 
     def fprop(self, x, w, y=None, stream=None):
         _dev(x, "x")

@@ -184,6 +184,36 @@ bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *dy, float *d
 bsmm_status bsmm_layer_norm(const void *x, const float *g, const float *b, void *y, int N, int C, int axis,
                             float epsilon, int relu, bsmm_dtype t, void *stream);
 
+/*
+ * l2_normalize(W, gain=None, epsilon=1e-6, dtype) [README, "API Documentation: blocksparse.matmul":
+ * a BlocksparseMatMul method "to implement weight normalization"].  Every output feature
+ * f = k*bs + j has one incoming weight vector, column f of the dense C x K weight: w[b][i][j]
+ * for all blocks b of block column k and all rows i.  With s_f its sum of squares:
+ *   y[b][i][j] = gain[f] * w[b][i][j] / sqrt(max(s_f, epsilon))      (gain = 1 when NULL)
+ * w: DEVICE (nnz, bs, bs) float32; gain: DEVICE K = S*bs float32 values or NULL; y: DEVICE
+ * (nnz, bs, bs) of dtype t (the README's dtype argument), rounded once to nearest-even.  Sums
+ * in float32, added in a fixed order (deterministic).  y may equal w when t = BSMM_F32;
+ * otherwise they must not overlap.  nnz = 0 is a no-op (w, y not used).
+ * Errors: INVALID (null handle or pointers, t unknown, epsilon negative or NaN, y == w with a
+ * 16-bit t), ALIGN (w or y not 16-byte aligned), CUDA.
+ */
+bsmm_status bsmm_l2_normalize(bsmm_t h, const float *w, const float *gain, void *y, float epsilon,
+                              bsmm_dtype t, void *stream);
+
+/*
+ * Gradient of bsmm_l2_normalize with respect to w and gain, for the gradient dy of y.  With
+ * rho_f = 1/sqrt(max(s_f, epsilon)) and D_f = sum of dy * w over feature f's vector:
+ *   dw[b][i][j] = gain[f] * rho_f * (dy[b][i][j] - [s_f >= epsilon] * rho_f^2 * D_f * w[b][i][j])
+ *   dgain[f]    = rho_f * D_f          (also when gain is NULL: the derivative at gain = 1)
+ * w: DEVICE float32 (nnz, bs, bs); gain: DEVICE K float32 or NULL; dy: DEVICE (nnz, bs, bs) of
+ * dtype t; dw: DEVICE float32 (nnz, bs, bs), must not overlap w or dy; dgain: DEVICE K float32
+ * or NULL (not computed).  Features of empty block columns get dgain = 0.
+ * Errors: INVALID (null handle, null w/dy/dw with nnz > 0, dw equal to w or dy, t unknown,
+ * epsilon negative or NaN), ALIGN (w, dy or dw not 16-byte aligned), CUDA.
+ */
+bsmm_status bsmm_l2_normalize_grad(bsmm_t h, const float *w, const float *gain, const void *dy, float *dw,
+                                   float *dgain, float epsilon, bsmm_dtype t, void *stream);
+
 /* Kernel family for later calls on this handle (testing / comparison). */
 bsmm_status bsmm_set_kernel(bsmm_t h, bsmm_kernel which);
 

@@ -89,3 +89,10 @@ def test_layer_norm_rejects_bad_arguments_on_host():
     assert L.bsmm_layer_norm(A, A, A, B, 12, 8, 0, 1e-6, 0, 2, None) == bsmm.ERR_ALIGN      # N * 2 % 16
     assert L.bsmm_layer_norm(A, A, A, B, 12, 8, 0, 1e-6, 0, 0, None) == bsmm.ERR_ALIGN      # fp32, N % 8
     assert L.bsmm_layer_norm(A, A, A, B, 4, 16392, 1, 1e-6, 0, 2, None) == bsmm.ERR_UNSUPPORTED
+
+
+def test_l2_normalize_rejects_null_handle_on_host():
+    L = bsmm.lib()
+    A = 0x10000
+    assert L.bsmm_l2_normalize(None, A, None, A, 1e-6, 0, None) == bsmm.ERR_INVALID
+    assert L.bsmm_l2_normalize_grad(None, A, None, A, A + 0x1000, None, 1e-6, 0, None) == bsmm.ERR_INVALID
