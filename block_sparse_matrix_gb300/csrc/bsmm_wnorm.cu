@@ -6,22 +6,28 @@
 // gradient, with D_f = sum dy * w over the same vector:
 //     dw = gain[f] * rho_f * (dy - [s_f >= epsilon] * rho_f^2 * D_f * w),  dgain[f] = rho_f * D_f.
 //
-// One cluster of kWnSplit CTAs per output block column k.  CTA r of the cluster takes column
+// A cluster of kWnSplit CTAs owns an output block column k.  CTA r of the cluster takes column
 // entries r, r + kWnSplit, ... (the per-column table of the handle lists them, c increasing).
-// Thread t reads 16-byte vectors t, t + 256, ... of the CTA's blocks; because a block is bs*bs/4
-// vectors and 1024 is a multiple of bs, every vector of thread t covers the same four features
-// j0 .. j0 + 3, j0 = 4t mod bs, so each thread keeps four partial sums (two sets for the
+// Thread t handles 16-byte vectors t, t + 256, ... of the CTA's blocks; because a block is
+// bs*bs/4 vectors and 1024 is a multiple of bs, every vector of thread t covers the same four
+// features j0 .. j0 + 3, j0 = 4t mod bs, so each thread keeps four partial sums (two sets for the
 // gradient).  The CTA's partials are added in shared memory, the kWnSplit CTA partials are
 // exchanged through distributed shared memory and added in rank order by every CTA (identical
-// totals in all of them), and the output pass scales the vectors still held in registers: w (and
-// dy) are read from memory once.  Vectors beyond V per thread (very long block columns) are
-// streamed and read a second time in the output pass.
+// totals in all of them), and the output pass scales the vectors the CTA still holds: w (and dy)
+// are read from memory once.  Two forms:
+//   k_l2n    one cluster per column, the vectors held in registers (V per thread; vectors beyond
+//            that, in very long columns, are streamed and read a second time);
+//   k_l2n_p  persistent clusters that walk the columns, the vectors staged in shared memory with
+//            cp.async, double-buffered so the next column's copies overlap the current column's
+//            reduction and output.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 
 #include "bsmm.h"
 #include "bsmm_internal.cuh"
@@ -32,6 +38,22 @@ namespace {
 constexpr int kWnThreads = 256;
 constexpr int kWnSplit = 8;      // CTAs per cluster, one cluster per output block column
 constexpr int kWnMaxV = 8;       // 16-byte vectors a thread keeps in registers (per operand)
+constexpr int kWnSmemMax = 200 * 1024;   // persistent kernel: dynamic shared memory of a CTA, at most
+
+// Kernel form.  By default the gradient takes the persistent kernel wherever a CTA's share of the
+// longest column fits its shared memory, and l2_normalize itself the register kernel (measured on
+// the 4096-wide, block 32, 50% dense weight: forward 17.3 us with registers against 20.4 us
+// persistent; gradient 32.0 us persistent against 44.1 us with registers).
+// BSMM_WN_KERNEL=registers or =persistent (read at every call) forces one form where it fits, for
+// comparison and for testing both.
+enum WnForm { kWnAuto, kWnRegisters, kWnPersistent };
+WnForm wn_form()
+{
+    const char *e = getenv("BSMM_WN_KERNEL");
+    if (e && strcmp(e, "registers") == 0) return kWnRegisters;
+    if (e && strcmp(e, "persistent") == 0) return kWnPersistent;
+    return kWnAuto;
+}
 
 // Four consecutive elements of type T as floats, from a 16-byte (float) or 8-byte (16-bit) load.
 template <typename T> __device__ __forceinline__ float4 ld4(const T *p);
@@ -218,6 +240,189 @@ k_l2n(const int32_t *__restrict__ col_ptr, const int32_t *__restrict__ col_ent, 
     cluster_wait();                                    // no CTA leaves while a peer reads its csum
 }
 
+
+// 16-, 8- and 4-byte asynchronous global -> shared copies; completion: cp.async.wait_group.
+__device__ __forceinline__ void cpa16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa8(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa4(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+template <typename T> __device__ __forceinline__ float4 sh4(const uint8_t *p);
+template <> __device__ __forceinline__ float4 sh4<float>(const uint8_t *p) { return *reinterpret_cast<const float4 *>(p); }
+template <> __device__ __forceinline__ float4 sh4<__half>(const uint8_t *p)
+{
+    const uint2 r = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&r.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&r.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+template <> __device__ __forceinline__ float4 sh4<__nv_bfloat16>(const uint8_t *p)
+{
+    const uint2 r = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Persistent form of k_l2n: gridDim.x / kWnSplit clusters walk the output block columns
+// k = cluster, cluster + clusters, ...  A CTA's share of a column (at most cap blocks) is staged
+// in shared memory with cp.async, double-buffered: the copies of the next column are in flight
+// while the current one is reduced, exchanged and written.  The block ids of a column are copied
+// two columns ahead (three slots), so no copy waits on a table lookup.  Each thread copies and
+// later reads the same 16-byte vectors (u = t, t + 256, ...), so its own cp.async.wait_group
+// orders them; the ids, read by every thread, are published by the barrier after the wait.
+// Shared memory: 2 x cap blocks of w (and dy), then 3 x cap block ids.
+template <bool GRAD, typename T>
+__global__ void __cluster_dims__(kWnSplit, 1, 1) __launch_bounds__(kWnThreads)
+k_l2n_p(const int32_t *__restrict__ col_ptr, const int32_t *__restrict__ col_ent, const float *w,
+        const float *__restrict__ gain, const T *dy, void *out, float *__restrict__ dgain, int S, int bs, int lq,
+        int cap, float eps)
+{
+    extern __shared__ __align__(16) uint8_t wn_smem[];
+    __shared__ float4 part[2][kWnThreads];
+    __shared__ float csum[2][2][32];                   // [column parity][s, D][feature]
+    __shared__ __align__(16) float coef[2][32];
+    constexpr int DSZ = 4 * sizeof(T);                 // bytes of 4 dy elements
+    const size_t wbytes = (size_t)cap << (lq + 4);     // one buffer of w: cap blocks
+    const size_t dbytes = GRAD ? ((size_t)cap << lq) * DSZ : 0;
+    // buffer b of w at wn_smem + b * wbytes, of dy at wn_smem + 2 * wbytes + b * dbytes
+    auto wb = [&](int b) { return wn_smem + b * wbytes; };
+    auto db = [&](int b) { return wn_smem + 2 * wbytes + b * dbytes; };
+    int32_t *ids = reinterpret_cast<int32_t *>(wn_smem + 2 * (wbytes + dbytes));   // [3][cap]
+
+    tc::pdl_launch_dependents();                       // holds no tensor memory: the next kernel may start
+    const int t = threadIdx.x;
+    const int rank = (int)tc::cluster_ctarank();
+    const int clusters = gridDim.x / kWnSplit;
+    const int k0 = blockIdx.x / kWnSplit;
+    const int qmask = (1 << lq) - 1;
+    const size_t bb = (size_t)bs * bs;
+    // (first entry, this CTA's block count) of column k; k >= S gives no blocks
+    auto span = [&](int k, int &e, int &nb) {
+        e = 0;
+        nb = 0;
+        if (k < S) {
+            const int a = __ldg(col_ptr + k), n = __ldg(col_ptr + k + 1) - a;
+            e = a;
+            nb = n > rank ? (n - rank + kWnSplit - 1) / kWnSplit : 0;
+        }
+    };
+    auto copy_ids = [&](int slot, int e, int nb) {
+        for (int m = t; m < nb; m += kWnThreads) cpa4(ids + slot * cap + m, col_ent + 2 * (e + rank + m * kWnSplit));
+    };
+    auto copy_data = [&](int slot, int buf, int nb) {
+        const int units = nb << lq;
+        for (int u = t; u < units; u += kWnThreads) {
+            const size_t o = (size_t)ids[slot * cap + (u >> lq)] * bb + (size_t)(u & qmask) * 4;
+            cpa16(wb(buf) + (size_t)u * 16, w + o);
+            if (GRAD) {
+                if (DSZ == 16) cpa16(db(buf) + (size_t)u * DSZ, dy + o);
+                else cpa8(db(buf) + (size_t)u * DSZ, dy + o);
+            }
+        }
+    };
+
+    // the tables are fixed after creation: read them before waiting on the previous kernel
+    int e_a, nb_a, e_b, nb_b, e_c, nb_c;               // columns i, i + 1, i + 2 of this cluster
+    span(k0, e_a, nb_a);
+    span(k0 + clusters, e_b, nb_b);
+    for (int m = t; m < nb_a; m += kWnThreads) ids[m] = __ldg(col_ent + 2 * (e_a + rank + m * kWnSplit));
+    copy_ids(1, e_b, nb_b);
+    cpa_commit();
+    tc::pdl_wait();                                    // w (and dy) may be the previous kernel's output
+    __syncthreads();                                   // ids of column 0 published
+    copy_data(0, 0, nb_a);
+    cpa_commit();
+
+    const int j0 = (4 * t) & (bs - 1);
+    int i = 0;
+    for (int k = k0; k < S; k += clusters, ++i) {
+        const int p = i & 1;
+        span(k + 2 * clusters, e_c, nb_c);
+        cpa_wait_all();                                // column i's vectors, column i + 1's ids
+        __syncthreads();
+        copy_data((i + 1) % 3, p ^ 1, nb_b);           // column i + 1
+        copy_ids((i + 2) % 3, e_c, nb_c);              // ids of column i + 2
+        cpa_commit();
+
+        const int units = nb_a << lq;
+        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = s4;
+        for (int u = t; u < units; u += kWnThreads) {
+            const float4 a = sh4<float>(wb(p) + (size_t)u * 16);
+            fma4(s4, a, a);
+            if (GRAD) fma4(d4, sh4<T>(db(p) + (size_t)u * DSZ), a);
+        }
+        part[0][t] = s4;
+        if (GRAD) part[1][t] = d4;
+        __syncthreads();
+        if (t < bs) {
+            const float *p0 = reinterpret_cast<const float *>(part[0]);
+            const float *p1 = reinterpret_cast<const float *>(part[1]);
+            float a = 0.f, d = 0.f;
+            for (int q = t; q < kWnThreads * 4; q += bs) {
+                a += p0[q];
+                if (GRAD) d += p1[q];
+            }
+            csum[p][0][t] = a;
+            if (GRAD) csum[p][1][t] = d;
+        }
+        tc::cluster_sync();                            // every CTA's csum[p] is written
+        if (t < bs) {
+            float s = 0.f, d = 0.f;
+            const uint32_t a0 = tc::smem_u32(&csum[p][0][t]), a1 = tc::smem_u32(&csum[p][1][t]);
+#pragma unroll
+            for (int r = 0; r < kWnSplit; ++r) {       // rank order: identical totals in every CTA
+                s += ld_cluster(tc::map_to_rank(a0, (uint32_t)r));
+                if (GRAD) d += ld_cluster(tc::map_to_rank(a1, (uint32_t)r));
+            }
+            const int f = k * bs + t;
+            const float g = gain ? gain[f] : 1.f;
+            const float rho = 1.f / sqrtf(fmaxf(s, eps));
+            coef[0][t] = g * rho;
+            if (GRAD) {
+                coef[1][t] = s >= eps ? rho * rho * d : 0.f;
+                if (dgain && rank == 0) dgain[f] = rho * d;
+            }
+        }
+        __syncthreads();
+        const float4 ca = *reinterpret_cast<const float4 *>(&coef[0][j0]);
+        float4 cc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (GRAD) cc = *reinterpret_cast<const float4 *>(&coef[1][j0]);
+        const int32_t *cid = ids + (i % 3) * cap;
+        for (int u = t; u < units; u += kWnThreads) {
+            const size_t o = (size_t)cid[u >> lq] * bb + (size_t)(u & qmask) * 4;
+            const float4 a = sh4<float>(wb(p) + (size_t)u * 16);
+            if (GRAD) {
+                const float4 g = sh4<T>(db(p) + (size_t)u * DSZ);
+                float4 r;
+                r.x = ca.x * (g.x - cc.x * a.x);
+                r.y = ca.y * (g.y - cc.y * a.y);
+                r.z = ca.z * (g.z - cc.z * a.z);
+                r.w = ca.w * (g.w - cc.w * a.w);
+                st4<float>(static_cast<float *>(out) + o, r);
+            } else {
+                st4<T>(static_cast<T *>(out) + o, make_float4(ca.x * a.x, ca.y * a.y, ca.z * a.z, ca.w * a.w));
+            }
+        }
+        e_a = e_b;
+        nb_a = nb_b;
+        e_b = e_c;
+        nb_b = nb_c;
+    }
+    cpa_wait_all();                                    // no copy outlives the CTA
+    tc::cluster_sync();                                // no CTA leaves while a peer reads its csum
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl_wn(void (*kern)(KArgs...), int grid, cudaStream_t s, Args... args)
 {
@@ -243,6 +448,54 @@ cudaError_t launch_v(bsmm_ctx *h, const float *w, const float *gain, const void 
                          eps);
 }
 
+// Dynamic shared memory of the persistent kernel: both buffers of w (and dy) plus three id slots.
+size_t persistent_smem(bool grad, int esz, int bs, int cap)
+{
+    const size_t blk = (size_t)bs * bs * (4 + (grad ? esz : 0));
+    return 2 * blk * cap + 3 * sizeof(int32_t) * cap;
+}
+
+template <bool GRAD, typename T>
+cudaError_t launch_persistent(bsmm_ctx *h, const float *w, const float *gain, const void *dy, void *out,
+                              float *dgain, int lq, int cap, size_t smem, float eps, cudaStream_t s)
+{
+    auto kern = k_l2n_p<GRAD, T>;
+    static std::atomic<int> attr_dev{-1};              // device whose shared-memory limit has been raised
+    static std::atomic<long long> occ{-1};             // device << 48 | smem << 16 | resident clusters
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (attr_dev.load() != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kWnSmemMax);
+        if (e != cudaSuccess) return e;
+        attr_dev.store(dev);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kWnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    const long long key = ((long long)dev << 48) | ((long long)smem << 16);
+    int clusters = 0;
+    const long long c = occ.load();
+    if (c >= 0 && (c & ~0xffffll) == key) {
+        clusters = (int)(c & 0xffff);
+    } else {
+        cfg.gridDim = dim3(h->S * kWnSplit);           // cluster shape: the kernel's __cluster_dims__
+        e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        occ.store(key | (long long)std::min(clusters, 0xffff));
+    }
+    clusters = std::max(1, std::min(clusters, h->S));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(clusters * kWnSplit);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, (const int32_t *)h->d_col_ptr, (const int32_t *)h->d_col_ent, w, gain,
+                              static_cast<const T *>(dy), out, dgain, h->S, h->bs, lq, cap, eps);
+}
+
 template <bool GRAD, typename T>
 cudaError_t launch_wn(bsmm_ctx *h, const float *w, const float *gain, const void *dy, void *out, float *dgain,
                       float eps, cudaStream_t s)
@@ -250,13 +503,20 @@ cudaError_t launch_wn(bsmm_ctx *h, const float *w, const float *gain, const void
     int maxcol = 0;
     for (int k = 0; k < h->S; ++k) maxcol = std::max(maxcol, h->h_col_ptr[k + 1] - h->h_col_ptr[k]);
     const int lq = h->bs == 32 ? 8 : h->bs == 16 ? 6 : 4;
-    const int64_t units = (int64_t)((maxcol + kWnSplit - 1) / kWnSplit) << lq;       // per CTA, at most
-    const int64_t need = (units + kWnThreads - 1) / kWnThreads;                       // vectors per thread
+    const int cap = std::max(1, (maxcol + kWnSplit - 1) / kWnSplit);                // blocks per CTA, at most
     cudaError_t e;
-    if (need <= 1) e = launch_v<GRAD, T, 1>(h, w, gain, dy, out, dgain, lq, eps, s);
-    else if (need <= 2) e = launch_v<GRAD, T, 2>(h, w, gain, dy, out, dgain, lq, eps, s);
-    else if (need <= 4) e = launch_v<GRAD, T, 4>(h, w, gain, dy, out, dgain, lq, eps, s);
-    else e = launch_v<GRAD, T, kWnMaxV>(h, w, gain, dy, out, dgain, lq, eps, s);
+    const size_t smem = persistent_smem(GRAD, (int)sizeof(T), h->bs, cap);
+    const WnForm form = wn_form();
+    const bool persistent = form == kWnPersistent || (form == kWnAuto && GRAD);
+    if (persistent && smem <= (size_t)kWnSmemMax) {
+        e = launch_persistent<GRAD, T>(h, w, gain, dy, out, dgain, lq, cap, smem, eps, s);
+    } else {
+        const int64_t need = (((int64_t)cap << lq) + kWnThreads - 1) / kWnThreads; // vectors per thread
+        if (need <= 1) e = launch_v<GRAD, T, 1>(h, w, gain, dy, out, dgain, lq, eps, s);
+        else if (need <= 2) e = launch_v<GRAD, T, 2>(h, w, gain, dy, out, dgain, lq, eps, s);
+        else if (need <= 4) e = launch_v<GRAD, T, 4>(h, w, gain, dy, out, dgain, lq, eps, s);
+        else e = launch_v<GRAD, T, kWnMaxV>(h, w, gain, dy, out, dgain, lq, eps, s);
+    }
     g_bsmm_launches += 1;
     return e;
 }

@@ -34,16 +34,33 @@ def _case(R, S, bs, p, seed, scale=1.0, zero_col=None, kind="bernoulli"):
     return L, m, w, gain
 
 
-SHAPES = [  # R, S, bs, density: several CTAs per cluster, ragged columns, long streamed columns
-    (8, 8, 32, 0.5), (128, 128, 32, 0.5), (40, 24, 16, 0.3), (512, 64, 8, 0.05),
-    (256, 3, 32, 1.0), (2048, 2, 8, 1.0), (1, 5, 16, 1.0),
+SHAPES = [  # R, S, bs, density: several CTAs per cluster, ragged columns, long columns (the
+    # last two exceed the persistent kernel's shared memory for float32 gradients / at bs 32 and
+    # stream in the register kernel), more columns than resident clusters (1024 x 8)
+    (8, 8, 32, 0.5), (128, 128, 32, 0.5), (40, 24, 16, 0.3), (512, 64, 8, 0.05), (16, 1024, 8, 0.2),
+    (1, 5, 16, 1.0), (256, 3, 32, 1.0), (2048, 2, 8, 1.0),
 ]
+
+
+# "auto": the library's choice; "registers": the one-pass register kernel everywhere;
+# "persistent": the persistent shared-memory kernel wherever a column share fits (the register
+# kernel beyond).
+FORMS = ["auto", "registers", "persistent"]
+
+
+@pytest.fixture(params=FORMS)
+def form(request, monkeypatch):
+    if request.param == "auto":
+        monkeypatch.delenv("BSMM_WN_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("BSMM_WN_KERNEL", request.param)
+    return request.param
 
 
 @pytest.mark.parametrize("R,S,bs,p", SHAPES)
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("with_gain", [False, True])
-def test_l2_normalize_parity(R, S, bs, p, dtype, with_gain):
+def test_l2_normalize_parity(R, S, bs, p, dtype, with_gain, form):
     L, m, w, gain = _case(R, S, bs, p, 7 * R + S + bs, zero_col=S // 2 if S > 2 else None)
     g = gain if with_gain else None
     y = m.l2_normalize(w.cuda(), None if g is None else g.cuda(), dtype=DT[dtype])
@@ -56,7 +73,7 @@ def test_l2_normalize_parity(R, S, bs, p, dtype, with_gain):
 @pytest.mark.parametrize("R,S,bs,p", SHAPES)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("with_gain", [False, True])
-def test_l2_normalize_grad_parity(R, S, bs, p, dtype, with_gain):
+def test_l2_normalize_grad_parity(R, S, bs, p, dtype, with_gain, form):
     L, m, w, gain = _case(R, S, bs, p, 11 * R + S + bs, zero_col=S // 2 if S > 2 else None)
     g = gain if with_gain else None
     dy = wk.normals(m.w_shape, 3 * R + 1, 1.0, dtype)
@@ -69,7 +86,7 @@ def test_l2_normalize_grad_parity(R, S, bs, p, dtype, with_gain):
 
 
 @pytest.mark.parametrize("bs", [32, 8])
-def test_l2_normalize_epsilon_branch(bs):
+def test_l2_normalize_epsilon_branch(bs, form):
     """Features whose squared norm is below epsilon (tiny weights), forward and gradient."""
     L, m, w, gain = _case(16, 6, bs, 0.5, 5, scale=1e-4)
     eps = 1e-2
@@ -102,7 +119,7 @@ def test_l2_normalize_exact_cases():
     m.close()
 
 
-def test_l2_normalize_in_place_deterministic_and_empty():
+def test_l2_normalize_in_place_deterministic_and_empty(form):
     L, m, w, gain = _case(64, 16, 32, 0.5, 9)
     wd = w.cuda()
     y1 = m.l2_normalize(wd, gain.cuda())
