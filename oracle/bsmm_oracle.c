@@ -17,6 +17,8 @@
  *   - identity_init: identity initialisation of the weight blocks.
  *   - l2_normalize: weight normalisation of the block-sparse weight (and its
  *     gradient), near the end of this file.
+ *   - SparseProj: gather / scatter projections over a one-to-one feature map (at
+ *     the end of this file).
  *   - group_param_grads: the weight gradients of up to 8 timesteps sharing one
  *     weight are summed (cast32: in float32 or wider).
  * and its section "blocksparse.norms" for layer_norm (at the end of this file).
@@ -453,4 +455,64 @@ void oracle_l2_normalize_grad(const uint8_t *L, int R, int S, int bs, const doub
                 dgain[f] = rho * d;
         }
     free(bid);
+}
+
+/*
+ * SparseProj(nhidden, nproj, proj_stride, block_size, gather_lut) with gather, scatter,
+ * scatter_add and scatter_mul  [blocksparse README, section "API Documentation:
+ * blocksparse.matmul", class SparseProj: dense-to-sparse and sparse-to-dense projections like the
+ * TensorFlow gather/scatter ops, over a unique one-to-one mapping].  The page gives the signatures
+ * only; the readings taken:
+ *   - gather_lut lists nproj distinct feature indices in [0, nhidden): sparse feature p is dense
+ *     feature lut[p];
+ *   - without gather_lut the map keeps runs of block_size consecutive features, one run starting
+ *     every proj_stride features (proj_stride defaults to block_size):
+ *       lut[r*block_size + i] = r*proj_stride + i;
+ *   - activations are (N, F) row-major for axis = 1 and (F, N) for axis = 0 (the meaning of the
+ *     matmul's feature_axis);
+ *   - gather(x)          out[n][p] = x[n][lut[p]]                         (N, nproj)
+ *     scatter(x)         out[n][lut[p]] = x[n][p], every other feature 0   (N, nhidden)
+ *     scatter_add(x, y)  out = x, then out[n][lut[p]] = x[n][lut[p]] + y[n][p]
+ *     scatter_mul(x, y)  out = x, then out[n][lut[p]] = x[n][lut[p]] * y[n][p]
+ *     gather_mul(x, y)   out[n][p] = x[n][lut[p]] * y[n][lut[p]]  (x, y dense; the gradient of
+ *                        scatter_mul with respect to its sparse operand is gather_mul(dout, x)).
+ * Values are float64; the caller rounds.
+ */
+void oracle_proj_default_lut(int nproj, int proj_stride, int block_size, int32_t *lut)
+{
+    for (int p = 0; p < nproj; ++p)
+        lut[p] = (p / block_size) * proj_stride + p % block_size;
+}
+
+static double *proj_at(double *a, int64_t n, int64_t f, int64_t N, int64_t F, int axis)
+{
+    return axis == 1 ? a + n * F + f : a + f * N + n;
+}
+
+/* op: 0 gather, 1 scatter, 2 scatter_add, 3 scatter_mul, 4 gather_mul. */
+void oracle_sparse_proj(int op, const double *x, const double *y, double *out, const int32_t *lut,
+                        int N, int nhidden, int nproj, int axis)
+{
+    double *xm = (double *)x, *ym = (double *)y;
+    if (op == 1 || op == 2 || op == 3) {          /* dense output: start from 0 or from x */
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t f = 0; f < nhidden; ++f)
+                *proj_at(out, n, f, N, nhidden, axis) = op == 1 ? 0.0 : *proj_at(xm, n, f, N, nhidden, axis);
+    }
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t p = 0; p < nproj; ++p) {
+            const int64_t f = lut[p];
+            if (op == 0) {
+                *proj_at(out, n, p, N, nproj, axis) = *proj_at(xm, n, f, N, nhidden, axis);
+            } else if (op == 1) {
+                *proj_at(out, n, f, N, nhidden, axis) = *proj_at(xm, n, p, N, nproj, axis);
+            } else if (op == 2) {
+                *proj_at(out, n, f, N, nhidden, axis) += *proj_at(ym, n, p, N, nproj, axis);
+            } else if (op == 3) {
+                *proj_at(out, n, f, N, nhidden, axis) *= *proj_at(ym, n, p, N, nproj, axis);
+            } else {
+                *proj_at(out, n, p, N, nproj, axis) =
+                    *proj_at(xm, n, f, N, nhidden, axis) * *proj_at(ym, n, f, N, nhidden, axis);
+            }
+        }
 }

@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
 benchmark's CPU-baseline leg may import this module.  It shares no code with
 the CUDA library.  Every function follows the blocksparse README, section
 "API Documentation: blocksparse.matmul" (BlocksparseMatMul, block_coord,
-identity_init, l2_normalize, __call__, group_param_grads), or its "blocksparse.norms" section
+identity_init, l2_normalize, __call__, group_param_grads, SparseProj), or its "blocksparse.norms" section
 (layer_norm); the C file states the readings taken where the page is silent.
 
 Inputs are numpy arrays; floating-point inputs are converted to float64
@@ -62,6 +62,8 @@ def _load():
         lib.oracle_layer_norm.argtypes = [_d, _d, _d, _d, _c, _c, _c, ctypes.c_double, _c]
         lib.oracle_l2_normalize.argtypes = [_u8, _c, _c, _c, _d, _d, ctypes.c_double, _d]
         lib.oracle_l2_normalize_grad.argtypes = [_u8, _c, _c, _c, _d, _d, ctypes.c_double, _d, _d, _d]
+        lib.oracle_proj_default_lut.argtypes = [_c, _c, _c, _i32]
+        lib.oracle_sparse_proj.argtypes = [_c, _d, _d, _d, _i32, _c, _c, _c, _c]
         lib.oracle_max_threads.restype = _c
         _lib = lib
     return _lib
@@ -273,3 +275,35 @@ def l2_normalize_grad(L, bs: int, w, dy, gain=None, epsilon: float = 1e-6):
                                      None if g is None else _p(g, _d), float(epsilon), _p(dy, _d),
                                      _p(dw, _d), _p(dgain, _d))
     return dw, dgain
+
+
+PROJ_OPS = {"gather": 0, "scatter": 1, "scatter_add": 2, "scatter_mul": 3, "gather_mul": 4}
+
+
+def proj_default_lut(nproj: int, proj_stride: int, block_size: int) -> np.ndarray:
+    """SparseProj's map without gather_lut (README, class SparseProj; the reading is stated in
+    the C source): runs of block_size features, one starting every proj_stride features."""
+    lut = np.empty(nproj, np.int32)
+    _load().oracle_proj_default_lut(nproj, proj_stride, block_size, _p(lut, _i32))
+    return lut
+
+
+def sparse_proj(op: str, lut, x, y=None, nhidden: int = None, axis: int = 1) -> np.ndarray:
+    """SparseProj.gather / scatter / scatter_add / scatter_mul (and gather_mul, the sparse-operand
+    gradient of scatter_mul), float64.  Activations are (N, F) for axis = 1, (F, N) for axis = 0;
+    x is dense (nhidden features) except for scatter, whose x is sparse (nproj features)."""
+    lut = np.ascontiguousarray(lut, dtype=np.int32)
+    x = _f64(x)
+    nproj = lut.size
+    N = x.shape[0] if axis == 1 else x.shape[1]
+    if op == "scatter":
+        assert nhidden is not None
+    else:
+        nhidden = x.shape[1] if axis == 1 else x.shape[0]
+    dense = (N, nhidden) if axis == 1 else (nhidden, N)
+    sparse = (N, nproj) if axis == 1 else (nproj, N)
+    yv = _f64(y) if y is not None else np.zeros(1)
+    out = np.empty(sparse if op in ("gather", "gather_mul") else dense)
+    _load().oracle_sparse_proj(PROJ_OPS[op], _p(x, _d), _p(yv, _d), _p(out, _d), _p(lut, _i32), N, nhidden,
+                               nproj, axis)
+    return out

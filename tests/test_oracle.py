@@ -446,3 +446,79 @@ def test_l2_normalize_grad_orthogonal_to_w():
     assert np.allclose(dots, 0.0, atol=1e-12)
     _, dgain1 = o.l2_normalize_grad(L, 8, w, dy, np.ones(6 * 8))
     assert np.array_equal(dgain, dgain1)
+
+
+# --- SparseProj (README, "API Documentation: blocksparse.matmul", class SparseProj) ---
+
+def _proj_inputs(N, nhidden, nproj, seed):
+    rng = np.random.default_rng(seed)
+    lut = rng.permutation(nhidden)[:nproj].astype(np.int32)       # distinct: one to one
+    return lut, rng.standard_normal((N, nhidden)), rng.standard_normal((N, nproj))
+
+
+def test_sparse_proj_hand_example():
+    lut = [4, 1, 3]
+    x = np.array([[10., 11., 12., 13., 14., 15.]])
+    s = np.array([[2., 3., 5.]])
+    assert np.array_equal(o.sparse_proj("gather", lut, x), [[14., 11., 13.]])
+    assert np.array_equal(o.sparse_proj("scatter", lut, s, nhidden=6), [[0., 3., 0., 5., 2., 0.]])
+    assert np.array_equal(o.sparse_proj("scatter_add", lut, x, s), [[10., 14., 12., 18., 16., 15.]])
+    assert np.array_equal(o.sparse_proj("scatter_mul", lut, x, s), [[10., 33., 12., 65., 28., 15.]])
+    assert np.array_equal(o.sparse_proj("gather_mul", lut, x, x), [[196., 121., 169.]])
+
+
+def test_sparse_proj_default_lut():
+    """Runs of block_size features, one every proj_stride features (the reading of the defaults)."""
+    assert o.proj_default_lut(8, 6, 4).tolist() == [0, 1, 2, 3, 6, 7, 8, 9]
+    assert o.proj_default_lut(6, 2, 2).tolist() == [0, 1, 2, 3, 4, 5]
+    assert o.proj_default_lut(96, 64, 32).tolist() == list(range(32)) + list(range(64, 96)) + list(range(128, 160))
+
+
+def test_sparse_proj_against_numpy_indexing():
+    """Against numpy fancy indexing, a route independent of the oracle's loops."""
+    lut, x, s = _proj_inputs(5, 40, 17, 1)
+    assert np.array_equal(o.sparse_proj("gather", lut, x), x[:, lut])
+    want = np.zeros((5, 40))
+    want[:, lut] = s
+    assert np.array_equal(o.sparse_proj("scatter", lut, s, nhidden=40), want)
+    want = x.copy()
+    want[:, lut] += s
+    assert np.array_equal(o.sparse_proj("scatter_add", lut, x, s), want)
+    want = x.copy()
+    want[:, lut] *= s
+    assert np.array_equal(o.sparse_proj("scatter_mul", lut, x, s), want)
+    z = np.random.default_rng(2).standard_normal((5, 40))
+    assert np.array_equal(o.sparse_proj("gather_mul", lut, x, z), x[:, lut] * z[:, lut])
+
+
+def test_sparse_proj_adjoint_and_round_trips():
+    """gather and scatter are adjoint (so each is the other's gradient, with no collisions to
+    sum); scatter then gather is the identity; gather then scatter keeps only the mapped features."""
+    lut, x, s = _proj_inputs(7, 33, 12, 3)
+    g = o.sparse_proj("gather", lut, x)
+    sc = o.sparse_proj("scatter", lut, s, nhidden=33)
+    assert np.isclose((g * s).sum(), (x * sc).sum(), rtol=1e-13)
+    assert np.array_equal(o.sparse_proj("gather", lut, sc), s)
+    mask = np.zeros(33)
+    mask[lut] = 1
+    assert np.array_equal(o.sparse_proj("scatter", lut, g, nhidden=33), x * mask)
+
+
+def test_sparse_proj_scatter_mul_gradient():
+    """<dout, scatter_mul(x, y)> is affine in y with slope gather_mul(dout, x): the sparse-operand
+    gradient of scatter_mul."""
+    lut, x, s = _proj_inputs(4, 20, 9, 4)
+    dout = np.random.default_rng(5).standard_normal((4, 20))
+    f = lambda y: (dout * o.sparse_proj("scatter_mul", lut, x, y)).sum()
+    gm = o.sparse_proj("gather_mul", lut, dout, x)
+    d = np.random.default_rng(6).standard_normal(s.shape)
+    assert np.isclose(f(s + d) - f(s), (gm * d).sum(), rtol=1e-12)
+
+
+def test_sparse_proj_axis_layouts_agree():
+    lut, x, s = _proj_inputs(6, 24, 10, 7)
+    for op, a, b, kw in (("gather", x, None, {}), ("scatter", s, None, {"nhidden": 24}),
+                         ("scatter_add", x, s, {}), ("scatter_mul", x, s, {}), ("gather_mul", x, x, {})):
+        r1 = o.sparse_proj(op, lut, a, b, axis=1, **kw)
+        r0 = o.sparse_proj(op, lut, a.T.copy(), None if b is None else b.T.copy(), axis=0, **kw)
+        assert np.array_equal(r0, r1.T), op
