@@ -167,10 +167,11 @@ def traffic_for(kernel_pass):
 
 
 def source_sha():
-    """Hash of the sources of the step's kernels (the normalisations are not part of the step)."""
+    """Hash of the sources of the step's kernels (the normalisations and projections are not part
+    of the step)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_sparse_matrix_gb300", "csrc")
-    for name in sorted(n for n in os.listdir(csrc) if n not in ("bsmm_norm.cu", "bsmm_wnorm.cu")):
+    for name in sorted(n for n in os.listdir(csrc) if n not in ("bsmm_norm.cu", "bsmm_wnorm.cu", "bsmm_proj.cu")):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -502,13 +503,14 @@ def _time_launches(fn, steps, warmup):
 
 
 def run_norm(args):
-    """The normalisations around the step, each on its own.
+    """The normalisations and projections around the step, each on its own.
     layer_norm (README "blocksparse.norms") on the step's activation shape, N = 1024 samples of
     C = 4096 bf16 features, in both layouts; 16 rotating input/output sets (256 MB > L2).  Bytes
     per launch = read x + write y + g, b.
     l2_normalize (README "blocksparse.matmul", weight normalisation) of the step's float32 weight
     (hidden 4096, block 32, 50% dense) to bf16, and its gradient (bf16 dy -> float32 dw, dgain);
     8 rotating sets (> L2).  Bytes per launch: read w (+ dy) + write y (or dw) + gain (+ dgain).
+    SparseProj gather and scatter between 4096 and 2048 bf16 features at N = 1024, both layouts.
     One JSON line."""
     from block_sparse_matrix_gb300 import bsmm
     dev = torch.device("cuda", 0)
@@ -547,12 +549,33 @@ def run_norm(args):
     us = _time_launches(lambda i: m.l2_normalize_grad(ws[i % wsets], ys[i % wsets], gain, dw=dws[i % wsets],
                                                       dgain=dgain), args.steps, args.warmup)
     out["l2_normalize_grad"] = entry(us, el * (4 + 2 + 4) + 2 * m.K * 4)
+    nnz = m.nnz
     m.close()
-    print(json.dumps({"metric": "normalisation GB/s (algorithmic bytes) on 1 GB300", "unit": "GB/s",
+    del ws, ys, dws
+
+    # SparseProj (README "blocksparse.matmul"): runs of 32 features every 64 of the 4096 hidden
+    # features (nproj 2048), N = 1024 bf16 samples; bytes = read + write of the moved elements
+    # (scatter writes every dense element).
+    for axis in (1, 0):
+        sp = bsmm.SparseProj(C, nproj=2048, proj_stride=64, block_size=32, feature_axis=axis)
+        dense = (N, C) if axis == 1 else (C, N)
+        sparse = (N, sp.nproj) if axis == 1 else (sp.nproj, N)
+        xs = [wk.normals(dense, 800 + i, 1.0, "bf16").to(dev) for i in range(sets)]
+        ss = [torch.empty(sparse, dtype=torch.bfloat16, device=dev) for _ in range(sets)]
+        us = _time_launches(lambda i: sp.gather(xs[i % sets], out=ss[i % sets]), args.steps, args.warmup)
+        out["sparse_proj_gather_axis%d" % axis] = entry(us, 2 * N * sp.nproj * 2)
+        us = _time_launches(lambda i: sp.scatter(ss[i % sets], out=xs[i % sets]), args.steps, args.warmup)
+        out["sparse_proj_scatter_axis%d" % axis] = entry(us, N * sp.nproj * 2 + N * C * 2)
+        sp.close()
+        del xs, ss
+    print(json.dumps({"metric": "normalisation and projection GB/s (algorithmic bytes) on 1 GB300",
+                      "unit": "GB/s",
                       "value": round(min(v["gbs"] for v in out.values()), 1), "dtype": "bf16",
                       "config": {"workload": "layer_norm: N=1024 x C=4096 bf16, 16 rotating sets; "
                                              "l2_normalize: hidden 4096, block 32, 50%% dense, %d blocks, "
-                                             "float32 w -> bf16, 8 rotating sets" % m.nnz},
+                                             "float32 w -> bf16, 8 rotating sets; SparseProj: N=1024 x "
+                                             "4096 -> 2048 features (runs of 32 every 64), bf16, 16 rotating "
+                                             "sets" % nnz},
                       "peak": peaks["hbm_gbs"], "peak_source": peak_src, "passes": out}), flush=True)
 
 
@@ -567,7 +590,7 @@ def main():
     ap.add_argument("--only", default="",
                     help="time a single pass (e.g. fprop_n1024) instead of the whole step; for kernel profiling")
     ap.add_argument("--norm", action="store_true",
-                    help="time layer_norm and l2_normalize (and its gradient) instead of the step")
+                    help="time layer_norm, l2_normalize (and its gradient) and SparseProj instead of the step")
     args = ap.parse_args()
     if args.norm:
         run_norm(args)

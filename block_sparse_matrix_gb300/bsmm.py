@@ -62,6 +62,11 @@ def lib():
             "bsmm_layer_norm": [vp, vp, vp, vp, i, i, i, ctypes.c_float, i, i, vp],
             "bsmm_l2_normalize": [vp, vp, vp, vp, ctypes.c_float, i, vp],
             "bsmm_l2_normalize_grad": [vp, vp, vp, vp, vp, vp, ctypes.c_float, i, vp],
+            "bsmm_proj_create": [ctypes.POINTER(vp), i, i, i, i, pi32],
+            "bsmm_proj_destroy": [vp],
+            "bsmm_proj_info": [vp, pi, pi],
+            "bsmm_proj_get_lut": [vp, pi32],
+            "bsmm_proj": [vp, i, vp, vp, vp, i, i, i, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -374,3 +379,126 @@ def layer_norm(x, g, b, axis: int = 1, epsilon: float = 1e-6, relu: bool = False
     _dev(y, "y")
     bsmm_layer_norm(x, g, b, y, N, C, axis, epsilon, relu, stream)
     return y
+
+
+# ---- SparseProj -------------------------------------------------------------------------
+
+PROJ_OPS = {"gather": 0, "scatter": 1, "scatter_add": 2, "scatter_mul": 3, "gather_mul": 4}
+
+
+def bsmm_proj_create(nhidden: int, nproj=None, proj_stride=None, block_size: int = 32, gather_lut=None):
+    h = ctypes.c_void_p()
+    lut = None
+    if gather_lut is not None:
+        lut = np.ascontiguousarray(np.asarray(gather_lut), dtype=np.int32).reshape(-1)
+        nproj = lut.size
+    _check(lib().bsmm_proj_create(ctypes.byref(h), int(nhidden), int(nproj or 0), int(proj_stride or 0),
+                                  int(block_size), None if lut is None else
+                                  lut.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))), "bsmm_proj_create")
+    return h
+
+
+def bsmm_proj_destroy(h):
+    _check(lib().bsmm_proj_destroy(h), "bsmm_proj_destroy")
+
+
+def bsmm_proj(h, op: str, x, y, out, N: int, axis: int = 1, stream=None):
+    _check(lib().bsmm_proj(h, PROJ_OPS[op], _ptr(x), _ptr(y), _ptr(out), int(N), int(axis), _DT[x.dtype],
+                           _stream(stream)), "bsmm_proj")
+
+
+class SparseProj:
+    """SparseProj(nhidden, nproj=None, proj_stride=None, block_size=32, gather_lut=None) of the
+    README ("API Documentation: blocksparse.matmul"): dense <-> sparse feature projections over a
+    one-to-one map.  Sparse feature p is dense feature lut[p]; without gather_lut the map keeps
+    runs of block_size features, one run every proj_stride (default block_size) features.
+    Activations are (N, F) for feature_axis = 1 and (F, N) for feature_axis = 0."""
+
+    def __init__(self, nhidden, nproj=None, proj_stride=None, block_size=32, gather_lut=None, feature_axis=1):
+        if feature_axis not in (0, 1):
+            raise ValueError("feature_axis must be 0 or 1")
+        self.feature_axis = feature_axis
+        self._h = bsmm_proj_create(nhidden, nproj, proj_stride, block_size, gather_lut)
+        a, b = ctypes.c_int(), ctypes.c_int()
+        _check(lib().bsmm_proj_info(self._h, ctypes.byref(a), ctypes.byref(b)), "bsmm_proj_info")
+        self.nhidden, self.nproj = a.value, b.value
+
+    def close(self):
+        if getattr(self, "_h", None):
+            bsmm_proj_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def lut(self):
+        out = np.empty(self.nproj, np.int32)
+        _check(lib().bsmm_proj_get_lut(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+               "bsmm_proj_get_lut")
+        return out
+
+    def _n(self, a, F, what):
+        _dev(a, what)
+        if a.dim() != 2:
+            raise ValueError("%s must be 2-D" % what)
+        f, n = (a.shape[1], a.shape[0]) if self.feature_axis == 1 else (a.shape[0], a.shape[1])
+        if f != F:
+            raise ValueError("%s has %d features, expected %d" % (what, f, F))
+        return n
+
+    def _shape(self, N, F):
+        return (N, F) if self.feature_axis == 1 else (F, N)
+
+    def _run(self, op, x, y, out, N, stream):
+        bsmm_proj(self._h, op, x, y, out, N, self.feature_axis, stream)
+        return out
+
+    def gather(self, x, out=None, stream=None):
+        N = self._n(x, self.nhidden, "x")
+        out = torch.empty(self._shape(N, self.nproj), dtype=x.dtype, device=x.device) if out is None else out
+        return self._run("gather", x, None, out, N, stream)
+
+    def scatter(self, x, out=None, stream=None):
+        N = self._n(x, self.nproj, "x")
+        out = torch.empty(self._shape(N, self.nhidden), dtype=x.dtype, device=x.device) if out is None else out
+        return self._run("scatter", x, None, out, N, stream)
+
+    def scatter_add(self, x, y, out=None, stream=None):
+        """x (dense) with y (sparse) added at the mapped features; out may be x (in place)."""
+        N = self._n(x, self.nhidden, "x")
+        self._n(y, self.nproj, "y")
+        out = torch.empty_like(x) if out is None else out
+        return self._run("scatter_add", x, y, out, N, stream)
+
+    def scatter_mul(self, x, y, out=None, stream=None):
+        """x (dense) with its mapped features multiplied by y (sparse); out may be x (in place)."""
+        N = self._n(x, self.nhidden, "x")
+        self._n(y, self.nproj, "y")
+        out = torch.empty_like(x) if out is None else out
+        return self._run("scatter_mul", x, y, out, N, stream)
+
+    def gather_mul(self, x, y, out=None, stream=None):
+        """gather(x) * gather(y) for two dense operands, in one pass."""
+        N = self._n(x, self.nhidden, "x")
+        self._n(y, self.nhidden, "y")
+        out = torch.empty(self._shape(N, self.nproj), dtype=x.dtype, device=x.device) if out is None else out
+        return self._run("gather_mul", x, y, out, N, stream)
+
+    # Gradients: with a one-to-one map gather and scatter are each other's adjoint.
+    def gather_grad(self, dy):
+        return self.scatter(dy)
+
+    def scatter_grad(self, dout):
+        return self.gather(dout)
+
+    def scatter_add_grad(self, dout):
+        """(dx, dy) of scatter_add(x, y)."""
+        return dout, self.gather(dout)
+
+    def scatter_mul_grad(self, dout, x, y):
+        """(dx, dy) of scatter_mul(x, y)."""
+        return self.scatter_mul(dout, y), self.gather_mul(dout, x)

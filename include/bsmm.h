@@ -214,6 +214,51 @@ bsmm_status bsmm_l2_normalize(bsmm_t h, const float *w, const float *gain, void 
 bsmm_status bsmm_l2_normalize_grad(bsmm_t h, const float *w, const float *gain, const void *dy, float *dw,
                                    float *dgain, float epsilon, bsmm_dtype t, void *stream);
 
+/*
+ * SparseProj(nhidden, nproj=None, proj_stride=None, block_size=32, gather_lut=None) [README,
+ * "API Documentation: blocksparse.matmul", class SparseProj: dense-to-sparse and sparse-to-dense
+ * projections like the TensorFlow gather / scatter ops, over a unique one-to-one mapping so that
+ * no backward op needs atomics].
+ * The map: sparse feature p (p < nproj) is dense feature lut[p] (lut[p] < nhidden).
+ * gather_lut: HOST array of nproj distinct indices in [0, nhidden) (copied), or NULL for runs of
+ * block_size consecutive features, one run starting every proj_stride features:
+ *   lut[r*block_size + i] = r*proj_stride + i,
+ * where proj_stride <= 0 means block_size and nproj <= 0 means as many runs as fit in nhidden.
+ * Copies the map and its inverse to the current device (synchronously).  On success *out owns
+ * device memory freed by bsmm_proj_destroy.
+ * Errors: INVALID (null out, nhidden < 1, entries out of range or repeated, nproj > nhidden, a
+ * default map that does not fit, nproj not a multiple of block_size), OOM, CUDA.
+ */
+typedef struct bsmm_proj_ctx *bsmm_proj_t;
+bsmm_status bsmm_proj_create(bsmm_proj_t *out, int nhidden, int nproj, int proj_stride, int block_size,
+                             const int32_t *gather_lut);
+bsmm_status bsmm_proj_destroy(bsmm_proj_t p);                      /* waits for the device; NULL is OK */
+bsmm_status bsmm_proj_info(bsmm_proj_t p, int *nhidden, int *nproj);
+bsmm_status bsmm_proj_get_lut(bsmm_proj_t p, int32_t *lut);        /* HOST array of nproj entries */
+
+typedef enum {
+    BSMM_PROJ_GATHER = 0,       /* out[n][p] = x[n][lut[p]]                         x dense, out sparse */
+    BSMM_PROJ_SCATTER = 1,      /* out[n][lut[p]] = x[n][p], other features 0       x sparse, out dense */
+    BSMM_PROJ_SCATTER_ADD = 2,  /* out = x; out[n][lut[p]] = x[n][lut[p]] + y[n][p]  x, out dense; y sparse */
+    BSMM_PROJ_SCATTER_MUL = 3,  /* out = x; out[n][lut[p]] = x[n][lut[p]] * y[n][p]  x, out dense; y sparse */
+    BSMM_PROJ_GATHER_MUL = 4    /* out[n][p] = x[n][lut[p]] * y[n][lut[p]]           x, y dense; out sparse
+                                   (the gradient of scatter_mul with respect to y is gather_mul(dout, x)) */
+} bsmm_proj_op;
+
+/*
+ * One SparseProj operation.  x, y, out: DEVICE pointers of dtype t, 16-byte aligned; dense
+ * arrays have nhidden features, sparse ones nproj; (N, F) row-major for axis = 1, (F, N) for
+ * axis = 0 (feature_axis), and for axis = 0 N * sizeof(element) must be a multiple of 16 bytes.
+ * y is read only by SCATTER_ADD, SCATTER_MUL and GATHER_MUL.  Sums and products are formed in
+ * float32 and rounded to t once (exact copies otherwise).  out may equal x for SCATTER_ADD and
+ * SCATTER_MUL (then only the mapped features are read and written); otherwise out must not
+ * overlap x or y.  N = 0 is a no-op.  Enqueued on `stream`.
+ * Errors: INVALID (null handle or pointers, N < 0, op, axis or t unknown, out == x for another
+ * op, out == y), ALIGN, CUDA.
+ */
+bsmm_status bsmm_proj(bsmm_proj_t p, bsmm_proj_op op, const void *x, const void *y, void *out, int N, int axis,
+                      bsmm_dtype t, void *stream);
+
 /* Kernel family for later calls on this handle (testing / comparison). */
 bsmm_status bsmm_set_kernel(bsmm_t h, bsmm_kernel which);
 

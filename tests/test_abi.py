@@ -96,3 +96,30 @@ def test_l2_normalize_rejects_null_handle_on_host():
     A = 0x10000
     assert L.bsmm_l2_normalize(None, A, None, A, 1e-6, 0, None) == bsmm.ERR_INVALID
     assert L.bsmm_l2_normalize_grad(None, A, None, A, A + 0x1000, None, 1e-6, 0, None) == bsmm.ERR_INVALID
+
+
+def test_proj_create_rejects_bad_maps_on_host():
+    """The map is validated on the host before any CUDA call."""
+    L = bsmm.lib()
+    h = ctypes.c_void_p()
+
+    def create(nhidden, nproj, stride, bs, lut=None):
+        arr = None
+        if lut is not None:
+            lut = np.ascontiguousarray(lut, dtype=np.int32)
+            arr = lut.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        return L.bsmm_proj_create(ctypes.byref(h), nhidden, nproj, stride, bs, arr)
+
+    assert create(8, 3, 0, 1, [1, 5, 1]) == bsmm.ERR_INVALID          # repeated feature
+    assert create(8, 3, 0, 1, [1, 5, 8]) == bsmm.ERR_INVALID          # out of range
+    assert create(8, 3, 0, 1, [1, -1, 2]) == bsmm.ERR_INVALID
+    assert create(2, 3, 0, 1, [0, 1, 2]) == bsmm.ERR_INVALID          # nproj > nhidden
+    assert create(0, 0, 0, 32) == bsmm.ERR_INVALID                    # nhidden < 1
+    assert create(100, 96, 64, 32) == bsmm.ERR_INVALID                # third run ends at 160 > 100
+    assert create(256, 48, 64, 32) == bsmm.ERR_INVALID                # nproj not a multiple of block_size
+    assert create(256, 64, 16, 32) == bsmm.ERR_INVALID                # runs would overlap
+    assert create(16, 0, 0, 32) == bsmm.ERR_INVALID                   # no run fits
+    assert L.bsmm_proj_create(None, 8, 0, 0, 4, None) == bsmm.ERR_INVALID
+    A = 0x10000
+    assert L.bsmm_proj(None, 0, A, None, A + 0x100, 4, 1, 2, None) == bsmm.ERR_INVALID
+    assert L.bsmm_proj_destroy(None) == bsmm.OK
