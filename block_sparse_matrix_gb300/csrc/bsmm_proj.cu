@@ -9,7 +9,8 @@
 //
 // Every dense or sparse output element is written by exactly one thread:
 //   (F, N) layout (axis 0): a work item is one 16-byte vector of an output row (rows are features);
-//   (N, F) layout (axis 1): a work item is one element.
+//   (N, F) layout (axis 1): a work item is 16 bytes of consecutive walked features when both row
+//   pitches are multiples of 16 bytes (k_proj_vec), else one element (k_proj_elems).
 // Ops whose output is dense (scatter, and scatter_add / scatter_mul out of place) walk the dense
 // features and look their source up in inv; gather, gather_mul and the in-place updates walk the
 // sparse features through lut.
@@ -134,6 +135,81 @@ k_proj_elems(const T *x, const T *y, T *out, const int32_t *__restrict__ lut, co
     }
 }
 
+
+// (N, F) with both row pitches a multiple of 16 bytes: an item is E = 16 / sizeof(T) consecutive
+// walked features of one sample.  Their E map entries are read as one vector; when they name E
+// consecutive features starting on a 16-byte boundary (runs of the default map, identity-like
+// stretches of a given one) the source moves as one 16-byte vector, otherwise element by element.
+// The output always moves as one vector except for the scattered in-place update of a broken run.
+template <int OP, typename T>
+__global__ void __launch_bounds__(kPjThreads)
+k_proj_vec(const T *x, const T *y, T *out, const int32_t *__restrict__ lut, const int32_t *__restrict__ inv,
+           int64_t items, int64_t vpr, int64_t nhidden, int64_t nproj, int in_place)
+{
+    tc::pdl_launch_dependents();
+    tc::pdl_wait();
+    constexpr int E = 16 / sizeof(T);
+    const bool sparse_walk = OP == BSMM_PROJ_GATHER || OP == BSMM_PROJ_GATHER_MUL || in_place;
+    const int32_t *map = sparse_walk ? lut : inv;
+    for (int64_t i = blockIdx.x * (int64_t)kPjThreads + threadIdx.x; i < items; i += (int64_t)gridDim.x * kPjThreads) {
+        const int64_t n = i / vpr, c0 = (i - n * vpr) * E;
+        const int64_t dn = n * nhidden, sn = n * nproj;
+        int idx[E];
+#pragma unroll
+        for (int q = 0; q < E; q += 4) *reinterpret_cast<int4 *>(idx + q) = *reinterpret_cast<const int4 *>(map + c0 + q);
+        bool run = (idx[0] % E) == 0, none = true;
+#pragma unroll
+        for (int q = 0; q < E; ++q) {
+            run = run && idx[q] == idx[0] + q;
+            none = none && idx[q] < 0;
+        }
+        run = run && idx[0] >= 0;
+        auto vec = [](const T *a) { return *reinterpret_cast<const uint4 *>(a); };
+        uint4 v;
+        T *ev = reinterpret_cast<T *>(&v);
+        if (OP == BSMM_PROJ_GATHER || OP == BSMM_PROJ_GATHER_MUL) {
+            if (run) {
+                v = vec(x + dn + idx[0]);
+                if (OP == BSMM_PROJ_GATHER_MUL) v = combine4<OP, T>(v, vec(y + dn + idx[0]));
+            } else {
+#pragma unroll
+                for (int q = 0; q < E; ++q)
+                    ev[q] = OP == BSMM_PROJ_GATHER ? x[dn + idx[q]] : combine<OP, T>(x[dn + idx[q]], y[dn + idx[q]]);
+            }
+            *reinterpret_cast<uint4 *>(out + sn + c0) = v;
+        } else if (OP == BSMM_PROJ_SCATTER) {
+            if (none) {
+                v = make_uint4(0u, 0u, 0u, 0u);
+            } else if (run) {
+                v = vec(x + sn + idx[0]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < E; ++q) ev[q] = idx[q] >= 0 ? x[sn + idx[q]] : pt<T>(0.f);
+            }
+            *reinterpret_cast<uint4 *>(out + dn + c0) = v;
+        } else if (in_place) {                      // scatter_add / scatter_mul into x itself
+            const uint4 b = vec(y + sn + c0);
+            if (run) {
+                *reinterpret_cast<uint4 *>(out + dn + idx[0]) = combine4<OP, T>(vec(x + dn + idx[0]), b);
+            } else {
+                const T *eb = reinterpret_cast<const T *>(&b);
+#pragma unroll
+                for (int q = 0; q < E; ++q) out[dn + idx[q]] = combine<OP, T>(x[dn + idx[q]], eb[q]);
+            }
+        } else {
+            v = vec(x + dn + c0);
+            if (run) {
+                v = combine4<OP, T>(v, vec(y + sn + idx[0]));
+            } else if (!none) {
+#pragma unroll
+                for (int q = 0; q < E; ++q)
+                    if (idx[q] >= 0) ev[q] = combine<OP, T>(ev[q], y[sn + idx[q]]);
+            }
+            *reinterpret_cast<uint4 *>(out + dn + c0) = v;
+        }
+    }
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl_pj(void (*kern)(KArgs...), int grid, cudaStream_t s, Args... args)
 {
@@ -163,6 +239,15 @@ cudaError_t launch_op(bsmm_proj_ctx *p, const void *x, const void *y, void *out,
         const int grid = (int)std::min<int64_t>((items + kPjThreads - 1) / kPjThreads, (int64_t)p->sm_count * 16);
         return launch_pdl_pj(k_proj_rows<OP, T>, std::max(grid, 1), s, xt, yt, ot, (const int32_t *)p->d_lut,
                              (const int32_t *)p->d_inv, items, vpr, (int64_t)N, (int)in_place);
+    }
+    constexpr int E = 16 / (int)sizeof(T);
+    if ((p->nhidden % E) == 0 && (p->nproj % E) == 0) {       // both row pitches 16-byte multiples
+        const int64_t vpr = cols / E;
+        items = (int64_t)N * vpr;
+        const int grid = (int)std::min<int64_t>((items + kPjThreads - 1) / kPjThreads, (int64_t)p->sm_count * 16);
+        return launch_pdl_pj(k_proj_vec<OP, T>, std::max(grid, 1), s, xt, yt, ot, (const int32_t *)p->d_lut,
+                             (const int32_t *)p->d_inv, items, vpr, (int64_t)p->nhidden, (int64_t)p->nproj,
+                             (int)in_place);
     }
     items = cols * (int64_t)N;
     const int grid = (int)std::min<int64_t>((items + kPjThreads - 1) / kPjThreads, (int64_t)p->sm_count * 16);

@@ -24,7 +24,17 @@ MAPS = {   # name: (nhidden, SparseProj keyword arguments)
     "default": (4096, lambda: {"nproj": 2048, "proj_stride": 64, "block_size": 32}),
     "permutation": (520, lambda: {"gather_lut": np.random.default_rng(2).permutation(520)}),
     "single": (72, lambda: {"gather_lut": [71]}),
+    "mixed": (4096, lambda: {"gather_lut": _mixed_lut()}),
 }
+
+
+def _mixed_lut():
+    """Runs of 32 every 64 features, with a swapped pair and one reversed run: some 16-byte groups
+    of the map are aligned runs and some are not."""
+    lut = o.proj_default_lut(2048, 64, 32)
+    lut[[5, 6]] = lut[[6, 5]]
+    lut[64:96] = lut[64:96][::-1].copy()
+    return lut
 
 
 def _exact(ref, dtype):
