@@ -326,6 +326,7 @@ extern "C" bsmm_status bsmm_proj_create(bsmm_proj_t *out, int nhidden, int nproj
 extern "C" bsmm_status bsmm_proj_destroy(bsmm_proj_t p)
 {
     if (!p) return BSMM_OK;
+    cudaSetDevice(p->device);
     cudaDeviceSynchronize();
     cudaFree(p->d_lut);
     cudaFree(p->d_inv);
