@@ -105,6 +105,20 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
+def _want(t, what, shape, dtype=None, device=None):
+    """A caller's tensor must have exactly the shape (and dtype, device) the call reads or writes:
+    the C calls see only pointers, so a mismatch would read or write outside the tensor."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (what, tuple(shape), tuple(t.shape)))
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (what, dtype, t.dtype))
+    if t.dtype not in _DT:
+        raise ValueError("%s has unsupported dtype %s" % (what, t.dtype))
+    if device is not None and t.device != device:
+        raise ValueError("%s must be on %s, got %s" % (what, device, t.device))
+    _dev(t, what)
+
+
 def _dev(t, what):
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % what)
@@ -263,18 +277,14 @@ class BlocksparseMatMul:
     def identity_init(self, w=None, dtype=torch.float32, device="cuda"):
         if w is None:
             w = torch.empty(self.w_shape, dtype=dtype, device=device)
-        _dev(w, "w")
+        _want(w, "w", self.w_shape)
         bsmm_identity_init(self._h, w)
         return w
 
     def _wn_args(self, w, gain):
-        _dev(w, "w")
-        if w.dtype != torch.float32 or tuple(w.shape) != self.w_shape:
-            raise ValueError("w must be float32 of shape %s" % (self.w_shape,))
+        _want(w, "w", self.w_shape, torch.float32)
         if gain is not None:
-            _dev(gain, "gain")
-            if gain.dtype != torch.float32 or gain.numel() != self.K:
-                raise ValueError("gain must be float32 with K = %d values" % self.K)
+            _want(gain, "gain", (self.K,), torch.float32, w.device)
 
     def l2_normalize(self, w, gain=None, epsilon=1e-6, dtype=torch.float32, y=None, stream=None):
         """Weight normalisation (README: l2_normalize(W, gain=None, epsilon=1e-6, dtype)): every
@@ -283,7 +293,7 @@ class BlocksparseMatMul:
         self._wn_args(w, gain)
         if y is None:
             y = torch.empty(self.w_shape, dtype=dtype, device=w.device)
-        _dev(y, "y")
+        _want(y, "y", self.w_shape, None, w.device)
         bsmm_l2_normalize(self._h, w, gain, y, epsilon, stream)
         return y
 
@@ -291,22 +301,23 @@ class BlocksparseMatMul:
         """(dw, dgain): gradient of l2_normalize for the gradient dy of its output (dy in the
         output's dtype, dw and dgain float32; dgain has K values)."""
         self._wn_args(w, gain)
-        _dev(dy, "dy")
-        if tuple(dy.shape) != self.w_shape:
-            raise ValueError("dy must have shape %s" % (self.w_shape,))
+        _want(dy, "dy", self.w_shape, None, w.device)
         if dw is None:
             dw = torch.empty(self.w_shape, dtype=torch.float32, device=w.device)
         if dgain is None:
             dgain = torch.empty(self.K, dtype=torch.float32, device=w.device)
+        _want(dw, "dw", self.w_shape, torch.float32, w.device)
+        _want(dgain, "dgain", (self.K,), torch.float32, w.device)
         bsmm_l2_normalize_grad(self._h, w, gain, dy, dw, dgain, epsilon, stream)
         return dw, dgain
 
     def fprop(self, x, w, y=None, stream=None):
         _dev(x, "x")
-        _dev(w, "w")
         N = self._N(x, self.C)
+        _want(w, "w", self.w_shape, x.dtype, x.device)
         if y is None:
             y = torch.empty(self.o_shape(N), dtype=x.dtype, device=x.device)
+        _want(y, "y", self.o_shape(N), x.dtype, x.device)
         bsmm_fprop(self._h, x, w, y, N, stream)
         return y
 
@@ -314,10 +325,11 @@ class BlocksparseMatMul:
 
     def bprop(self, dy, w, dx=None, stream=None):
         _dev(dy, "dy")
-        _dev(w, "w")
         N = self._N(dy, self.K)
+        _want(w, "w", self.w_shape, dy.dtype, dy.device)
         if dx is None:
             dx = torch.empty(self.i_shape(N), dtype=dy.dtype, device=dy.device)
+        _want(dx, "dx", self.i_shape(N), dy.dtype, dy.device)
         bsmm_bprop(self._h, dy, w, dx, N, stream)
         return dx
 
@@ -327,8 +339,10 @@ class BlocksparseMatMul:
         N = self._N(x, self.C)
         if self._N(dy, self.K) != N:
             raise ValueError("x and dy minibatch sizes differ")
+        _want(dy, "dy", self.o_shape(N), x.dtype, x.device)
         if dw is None:
             dw = torch.empty(self.w_shape, dtype=dw_dtype, device=x.device)
+        _want(dw, "dw", self.w_shape, None, x.device)
         bsmm_updat(self._h, x, dy, dw, N, accumulate, stream)
         return dw
 
@@ -338,8 +352,14 @@ class BlocksparseMatMul:
         for a in list(xs) + list(dys):
             _dev(a, "activation")
         N = self._N(xs[0], self.C)
+        x0 = xs[0]
+        for a in xs:
+            _want(a, "x", self.i_shape(N), x0.dtype, x0.device)
+        for a in dys:
+            _want(a, "dy", self.o_shape(N), x0.dtype, x0.device)
         if dw is None:
-            dw = torch.empty(self.w_shape, dtype=torch.float32, device=xs[0].device)
+            dw = torch.empty(self.w_shape, dtype=torch.float32, device=x0.device)
+        _want(dw, "dw", self.w_shape, torch.float32, x0.device)
         bsmm_updat_grouped(self._h, xs, dys, dw, N, accumulate, stream)
         return dw
 
@@ -374,9 +394,11 @@ def layer_norm(x, g, b, axis: int = 1, epsilon: float = 1e-6, relu: bool = False
     N = x.shape[0] if axis == 1 else x.shape[1]
     if g.dtype != torch.float32 or b.dtype != torch.float32 or g.numel() != C or b.numel() != C:
         raise ValueError("g and b must be float32 with C = %d values" % C)
+    if g.device != x.device or b.device != x.device:
+        raise ValueError("g and b must be on %s" % x.device)
     if y is None:
         y = torch.empty_like(x)
-    _dev(y, "y")
+    _want(y, "y", x.shape, x.dtype, x.device)
     bsmm_layer_norm(x, g, b, y, N, C, axis, epsilon, relu, stream)
     return y
 
@@ -457,36 +479,40 @@ class SparseProj:
         bsmm_proj(self._h, op, x, y, out, N, self.feature_axis, stream)
         return out
 
+    def _out(self, out, x, N, F):
+        if out is None:
+            return torch.empty(self._shape(N, F), dtype=x.dtype, device=x.device)
+        _want(out, "out", self._shape(N, F), x.dtype, x.device)
+        return out
+
+    def _operand(self, y, x, N, F):
+        _want(y, "y", self._shape(N, F), x.dtype, x.device)
+
     def gather(self, x, out=None, stream=None):
         N = self._n(x, self.nhidden, "x")
-        out = torch.empty(self._shape(N, self.nproj), dtype=x.dtype, device=x.device) if out is None else out
-        return self._run("gather", x, None, out, N, stream)
+        return self._run("gather", x, None, self._out(out, x, N, self.nproj), N, stream)
 
     def scatter(self, x, out=None, stream=None):
         N = self._n(x, self.nproj, "x")
-        out = torch.empty(self._shape(N, self.nhidden), dtype=x.dtype, device=x.device) if out is None else out
-        return self._run("scatter", x, None, out, N, stream)
+        return self._run("scatter", x, None, self._out(out, x, N, self.nhidden), N, stream)
 
     def scatter_add(self, x, y, out=None, stream=None):
         """x (dense) with y (sparse) added at the mapped features; out may be x (in place)."""
         N = self._n(x, self.nhidden, "x")
-        self._n(y, self.nproj, "y")
-        out = torch.empty_like(x) if out is None else out
-        return self._run("scatter_add", x, y, out, N, stream)
+        self._operand(y, x, N, self.nproj)
+        return self._run("scatter_add", x, y, self._out(out, x, N, self.nhidden), N, stream)
 
     def scatter_mul(self, x, y, out=None, stream=None):
         """x (dense) with its mapped features multiplied by y (sparse); out may be x (in place)."""
         N = self._n(x, self.nhidden, "x")
-        self._n(y, self.nproj, "y")
-        out = torch.empty_like(x) if out is None else out
-        return self._run("scatter_mul", x, y, out, N, stream)
+        self._operand(y, x, N, self.nproj)
+        return self._run("scatter_mul", x, y, self._out(out, x, N, self.nhidden), N, stream)
 
     def gather_mul(self, x, y, out=None, stream=None):
         """gather(x) * gather(y) for two dense operands, in one pass."""
         N = self._n(x, self.nhidden, "x")
-        self._n(y, self.nhidden, "y")
-        out = torch.empty(self._shape(N, self.nproj), dtype=x.dtype, device=x.device) if out is None else out
-        return self._run("gather_mul", x, y, out, N, stream)
+        self._operand(y, x, N, self.nhidden)
+        return self._run("gather_mul", x, y, self._out(out, x, N, self.nproj), N, stream)
 
     # Gradients: with a one-to-one map gather and scatter are each other's adjoint.
     def gather_grad(self, dy):

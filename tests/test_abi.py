@@ -123,3 +123,20 @@ def test_proj_create_rejects_bad_maps_on_host():
     A = 0x10000
     assert L.bsmm_proj(None, 0, A, None, A + 0x100, 4, 1, 2, None) == bsmm.ERR_INVALID
     assert L.bsmm_proj_destroy(None) == bsmm.OK
+
+
+def test_binding_checks_caller_tensors_before_any_call():
+    """The object API refuses a caller's tensor whose shape, dtype or device differs from what the
+    C call will read or write (the C ABI sees only pointers)."""
+    import torch
+    t = torch.zeros(4, 6, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="shape"):
+        bsmm._want(t, "y", (4, 7))
+    with pytest.raises(ValueError, match="must be torch.float32"):
+        bsmm._want(t, "dw", (4, 6), torch.float32)
+    with pytest.raises(ValueError, match="unsupported dtype"):
+        bsmm._want(torch.zeros(4, 6, dtype=torch.float64), "x", (4, 6))
+    with pytest.raises(ValueError, match="must be on"):
+        bsmm._want(t, "y", (4, 6), torch.bfloat16, torch.device("cuda", 0))
+    with pytest.raises(ValueError, match="CUDA tensor"):           # right shape and dtype, host memory
+        bsmm._want(t, "y", (4, 6), torch.bfloat16)
