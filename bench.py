@@ -186,7 +186,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    wl = wk.CONFIGS["cfg2_n1024"]
+    wl = wk.CONFIGS["h4096_b32_p50_n1024"]
     Ns = [1024, 64]
     inp = wk.make_inputs(wl)
     L, bs, C, K = inp.layout, wl.bs, wl.C, wl.K
@@ -343,7 +343,7 @@ def run_e2e(m, inp, Ns, passes, dev, args):
     are pipelined over three streams (uploads, passes, downloads) with two device buffer sets
     ordered by events, so step i+1's uploads and step i-1's downloads overlap step i's passes."""
     from block_sparse_matrix_gb300 import bsmm
-    wl = wk.CONFIGS["cfg2_n1024"]
+    wl = wk.CONFIGS["h4096_b32_p50_n1024"]
     C, K, bs, nnz = wl.C, wl.K, wl.bs, m.nnz
     host = {"w": inp.w.pin_memory()}
     for N in Ns:
@@ -454,7 +454,7 @@ def run_reference(args):
         return
     from oracle import oracle as o
     o.build()
-    wl = wk.CONFIGS["cfg2_n1024"]
+    wl = wk.CONFIGS["h4096_b32_p50_n1024"]
     inp = wk.make_inputs(wl)
     nthreads = len(os.sched_getaffinity(0))
     rows, blocks = nthreads, 128
@@ -534,8 +534,8 @@ def run_norm(args):
         out["layer_norm_axis%d" % axis] = entry(us, 2 * N * C * 2 + 2 * C * 4)
         del xs, ys
 
-    wl = wk.CONFIGS["cfg2_n1024"]
-    lay = wk.make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 1000 * wl.cfg)
+    wl = wk.CONFIGS["h4096_b32_p50_n1024"]
+    lay = wk.make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 1000 * wl.seed_ns)
     m = bsmm.BlocksparseMatMul(lay, block_size=wl.bs, feature_axis=wl.feature_axis)
     wsets = 8
     ws = [wk.normals(m.w_shape, 700 + i, 0.02, "f32").to(dev) for i in range(wsets)]

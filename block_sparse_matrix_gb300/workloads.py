@@ -5,10 +5,10 @@ the method's arithmetic, so both the CUDA path's tests/benchmarks and the CPU
 oracle can take their inputs from it without sharing any computation.
 
 Workloads follow the usage example of the blocksparse README (hidden 4096,
-block size 32, minibatch 64, random 0/1 layout: "Usage" section) and the five
-benchmark configurations of this library (sizes below).  All draws use numpy's
-PCG64 generator (``numpy.random.default_rng(seed)``) with
-``seed = 1000 * cfg + stream`` where stream 0 = layout, 1 = x, 2 = w, 3 = dy,
+block size 32, minibatch 64, random 0/1 layout: "Usage" section) and the
+benchmark workloads of this library (named by their sizes, below).  All draws use
+numpy's PCG64 generator (``numpy.random.default_rng(seed)``) with
+``seed = 1000 * seed_ns + stream`` where stream 0 = layout, 1 = x, 2 = w, 3 = dy,
 10 + t = x of timestep t, 30 + t = dy of timestep t.  Normals are drawn in
 float32 and rounded to nearest-even into the compute dtype by torch.
 """
@@ -26,7 +26,7 @@ DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    cfg: int               # seed namespace
+    seed_ns: int           # seed namespace: inputs draw from seeds 1000 * seed_ns + stream
     C: int                 # input features
     K: int                 # output features
     bs: int                # block size (32, 16 or 8)
@@ -49,19 +49,21 @@ class Workload:
         return self.K // self.bs
 
 
-# The five benchmark configurations.  cfg2 is quoted at N=64 and N=1024.
+# The benchmark workloads, named by hidden size, block size and density; the 4096-wide, block 32,
+# 50% dense one is quoted at N=64 and at N=1024.
 CONFIGS = {
-    "cfg1": Workload("cfg1", 1, 256, 256, 32, "bernoulli", 0.5, True, 64, "f32", 1, 1.0 / 256),
-    "cfg2_n64": Workload("cfg2_n64", 2, 4096, 4096, 32, "bernoulli", 0.5, False, 64, "bf16", 1,
-                         1.0 / (4096 * 0.5)),
-    "cfg2_n1024": Workload("cfg2_n1024", 2, 4096, 4096, 32, "bernoulli", 0.5, False, 1024, "bf16", 1,
-                           1.0 / (4096 * 0.5)),
-    "cfg3": Workload("cfg3", 3, 8192, 8192, 16, "bernoulli", 0.10, True, 512, "f16", 0,
-                     1.0 / (8192 * 0.10)),
-    "cfg4": Workload("cfg4", 4, 4096, 4096, 8, "bernoulli", 0.05, True, 2048, "bf16", 0,
-                     1.0 / (4096 * 0.05)),
-    "cfg5": Workload("cfg5", 5, 6144, 6144, 32, "blockdiag_plus", 8, True, 128, "bf16", 1,
-                     1.0 / (9 * 32), steps=16, group=8),
+    "h256_b32_fp32": Workload("h256_b32_fp32", 1, 256, 256, 32, "bernoulli", 0.5, True, 64, "f32", 1,
+                              1.0 / 256),
+    "h4096_b32_p50_n64": Workload("h4096_b32_p50_n64", 2, 4096, 4096, 32, "bernoulli", 0.5, False, 64, "bf16",
+                                  1, 1.0 / (4096 * 0.5)),
+    "h4096_b32_p50_n1024": Workload("h4096_b32_p50_n1024", 2, 4096, 4096, 32, "bernoulli", 0.5, False, 1024,
+                                    "bf16", 1, 1.0 / (4096 * 0.5)),
+    "h8192_b16_p10": Workload("h8192_b16_p10", 3, 8192, 8192, 16, "bernoulli", 0.10, True, 512, "f16", 0,
+                              1.0 / (8192 * 0.10)),
+    "h4096_b8_p5": Workload("h4096_b8_p5", 4, 4096, 4096, 8, "bernoulli", 0.05, True, 2048, "bf16", 0,
+                            1.0 / (4096 * 0.05)),
+    "h6144_b32_recurrent": Workload("h6144_b32_recurrent", 5, 6144, 6144, 32, "blockdiag_plus", 8, True, 128,
+                                    "bf16", 1, 1.0 / (9 * 32), steps=16, group=8),
 }
 
 
@@ -125,9 +127,9 @@ class Inputs:
 def make_inputs(wl: Workload, N: Optional[int] = None, steps: Optional[int] = None) -> Inputs:
     """All inputs of a workload on the CPU, in the workload's dtype."""
     N = wl.N if N is None else N
-    lay = make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 1000 * wl.cfg + 0)
+    lay = make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 1000 * wl.seed_ns + 0)
     nnz = int(lay.sum())
-    base = 1000 * wl.cfg
+    base = 1000 * wl.seed_ns
     x = normals(act_shape(wl.C, N, wl.feature_axis), base + 1, 1.0, wl.dtype)
     w = normals((nnz, wl.bs, wl.bs), base + 2, float(np.sqrt(wl.w_var)), wl.dtype)
     dy = normals(act_shape(wl.K, N, wl.feature_axis), base + 3, 1.0, wl.dtype)

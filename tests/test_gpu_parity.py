@@ -224,7 +224,7 @@ def _sample_check(m, L, bs, fa, dtype, x, w, dy, y, dx, dw, rng, n_samples=384):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-@pytest.mark.parametrize("name", ["cfg1", "cfg2_n64", "cfg2_n1024", "cfg3", "cfg4"])
+@pytest.mark.parametrize("name", ["h256_b32_fp32", "h4096_b32_p50_n64", "h4096_b32_p50_n1024", "h8192_b16_p10", "h4096_b8_p5"])
 def test_config_full_size(kernel, name):
     wl = wk.CONFIGS[name]
     inp = wk.make_inputs(wl)
@@ -234,8 +234,8 @@ def test_config_full_size(kernel, name):
     y, dx, dw = m.fprop(x, w), m.bprop(dy, w), m.updat(x, dy)
     m.sync_status()
     _sample_check(m, L, wl.bs, wl.feature_axis, wl.dtype, inp.x, inp.w, inp.dy, y, dx, dw,
-                  np.random.default_rng(wl.cfg))
-    if name == "cfg1":   # small enough for the full oracle
+                  np.random.default_rng(wl.seed_ns))
+    if name == "h256_b32_fp32":   # small enough for the full oracle
         assert rel_fro(cpu64(y), o.fprop(L, wl.bs, inp.x, inp.w, 1)) <= TOL["f32"]
         assert rel_fro(cpu64(dx), o.bprop(L, wl.bs, inp.dy, inp.w, 1)) <= TOL["f32"]
         assert rel_fro(cpu64(dw), o.updat(L, wl.bs, inp.x, inp.dy, 1)) <= TOL["f32"]
@@ -245,7 +245,7 @@ def test_config_full_size(kernel, name):
 def test_config5_recurrent_grouped(kernel):
     """16 timesteps share W: per-step fprop/bprop, weight gradient grouped 8 steps per
     call and summed into one float32 dW (group_param_grads)."""
-    wl = wk.CONFIGS["cfg5"]
+    wl = wk.CONFIGS["h6144_b32_recurrent"]
     inp = wk.make_inputs(wl)
     L, bs = inp.layout, wl.bs
     m = make(L, bs, 1, kernel)

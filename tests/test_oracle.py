@@ -268,11 +268,11 @@ def test_golden_usage_example_ones():
 
 def test_workload_layouts():
     """The synthetic layouts have the stated structure (diagonal forced, 8 extra per row)."""
-    for name in ("cfg1", "cfg3", "cfg4"):
+    for name in ("h256_b32_fp32", "h8192_b16_p10", "h4096_b8_p5"):
         wl = wk.CONFIGS[name]
-        L = wk.make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 1000 * wl.cfg)
+        L = wk.make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 1000 * wl.seed_ns)
         assert np.all(np.diag(L) == 1)
-    wl = wk.CONFIGS["cfg5"]
+    wl = wk.CONFIGS["h6144_b32_recurrent"]
     L = wk.make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 5000)
     assert np.all(L.sum(1) == 9) and np.all(np.diag(L) == 1)
 
