@@ -154,16 +154,21 @@ class ClockSampler:
 # ---- our implementation --------------------------------------------------------------------
 
 def traffic_for(kernel_pass):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
+    """(read, write) DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else (None, None)).  ncu counts DRAM traffic inside the
+    kernel's own duration: the kernel's outputs are written into the 129 MB L2 and reach DRAM
+    after the kernel ends, so the write figure is not the kernel's write-back."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
-        return None
+        return None, None
     with open(p) as f:
         d = json.load(f)
     if d.get("src_sha") != source_sha():
-        return None
-    return d.get("passes", {}).get(kernel_pass)
+        return None, None
+    e = d.get("passes", {}).get(kernel_pass)
+    if not isinstance(e, dict):
+        return None, None
+    return e.get("read"), e.get("write")
 
 
 def source_sha():
@@ -315,11 +320,19 @@ def run_ours(args):
         achieved, peak, unit = f / t / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     else:
         achieved, peak, unit = b / t / 1e9, peaks["hbm_gbs"], "GB/s"
+    rd, wr = traffic_for(name)
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": traffic_for(name), "kernel": name,
-                "algorithmic_bytes": b, "flops": f, "peak_source": peak_src + " (burst)"}
+                "frac": round(achieved / peak, 4),
+                "traffic": (rd + wr) if rd is not None and wr is not None else None,
+                "dram_read_bytes": rd, "dram_write_bytes": wr,
+                "dram_write_note": "ncu counts DRAM bytes inside the kernel's duration; outputs are written into "
+                                   "L2 and written back to DRAM after the kernel, so the write field does not "
+                                   "measure this kernel's write-back",
+                "kernel": name, "algorithmic_bytes": b, "flops": f, "peak_source": peak_src + " (burst)"}
 
     e2e = run_e2e(m, inp, Ns, passes, dev, args) if (rank == 0 and not args.only) else None
+    configs = run_configs(dev, peaks, args.config_reps) if (rank == 0 and not args.only and
+                                                             args.config_reps > 0) else None
     cpu = (run_cpu_baseline(wl, inp, Ns, budget_s=args.cpu_budget)
            if (rank == 0 and ws == 1 and args.cpu_budget > 0) else None)
 
@@ -329,7 +342,7 @@ def run_ours(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normals)",
                 "config": {"workload": WORKLOAD, "nnz": nnz, "l2": "4 rotating input/output sets, ~330 MB > 2x L2",
                            "parallelism": "replicas" if ws > 1 else "single GPU"},
-                "passes": per_pass, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "passes": per_pass, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "configs": configs,
                 "clocks": clocks, "gpu_launches": launches_per_step * K_steps,
                 "wall_s_timed_region": round(wall1 - wall0, 3)}
         print(json.dumps(line), flush=True)
@@ -405,6 +418,86 @@ def run_e2e(m, inp, Ns, passes, dev, args):
     return {"value": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4), "steps": steps,
             "pipelined": "uploads, passes and downloads on three streams, two device buffer sets"}
+
+
+# ---- every benchmark configuration, pass by pass ---------------------------------------------
+
+# Derived fp32 FFMA peak for the fp32 configuration (no tensor cores): 152 SMs x 128 FMA/clk x
+# 2 FLOP x 2.07 GHz (the unit counts and the maximum SM clock of a GB300).
+FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def config_passes(wl, nnz):
+    """(pass name, flops, algorithmic bytes, callable builder key) of one workload: fprop, bprop
+    and updat at its minibatch, and for a workload with timesteps the per-step fprop/bprop and the
+    grouped weight gradient of `group` steps accumulated into float32 dW."""
+    e = 4 if wl.dtype == "f32" else 2
+    N, C, K, bs = wl.N, wl.C, wl.K, wl.bs
+    f = wk.effective_flops(N, nnz, bs)
+    act = (N * C + N * K) * e
+    out = [("fprop", f, act + nnz * bs * bs * e), ("bprop", f, act + nnz * bs * bs * e),
+           ("updat", f, act + nnz * bs * bs * 4)]
+    if wl.steps > 1:
+        G = wl.group
+        out.append(("updat_grouped_g%d" % G, G * f, G * act + 2 * nnz * bs * bs * 4))
+    return out
+
+
+def run_configs(dev, peaks, reps):
+    """Each benchmark configuration on its own: every pass timed alone with CUDA events, cold
+    (a 256 MB read-only sweep evicts the L2 before each timed launch), median over reps."""
+    from block_sparse_matrix_gb300 import bsmm
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    out = {}
+    for name, wl in wk.CONFIGS.items():
+        inp = wk.make_inputs(wl, steps=min(wl.steps, wl.group) if wl.steps > 1 else None)
+        m = bsmm.BlocksparseMatMul(inp.layout, block_size=wl.bs, feature_axis=wl.feature_axis)
+        x, w, dy = inp.x.to(dev), inp.w.to(dev), inp.dy.to(dev)
+        y = torch.empty(m.o_shape(wl.N), dtype=x.dtype, device=dev)
+        dx = torch.empty(m.i_shape(wl.N), dtype=x.dtype, device=dev)
+        dw = torch.zeros(m.w_shape, dtype=torch.float32, device=dev)
+        calls = {"fprop": lambda: m.fprop(x, w, y), "bprop": lambda: m.bprop(dy, w, dx),
+                 "updat": lambda: m.updat(x, dy, dw)}
+        if wl.steps > 1:
+            xs = [a.to(dev) for a in inp.xs]
+            dys = [a.to(dev) for a in inp.dys]
+            calls["updat_grouped_g%d" % wl.group] = lambda: m.updat_grouped(xs, dys, dw=dw, accumulate=True)
+        res = {}
+        for pname, flops, byts in config_passes(wl, m.nnz):
+            fn = calls[pname]
+            for _ in range(3):
+                fn()
+            evs = []
+            for _ in range(reps):
+                flush.sum()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                evs.append((a, b))
+            torch.cuda.synchronize()
+            us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1000.0
+            if wl.dtype == "f32":
+                t_c, bound_c = flops / (FFMA_TFLOPS * 1e12), "alu"
+            else:
+                t_c, bound_c = flops / (peaks["bf16_tflops"] * 1e12), "tensor"
+            t_m = byts / (peaks["hbm_gbs"] * 1e9)
+            tr = max(t_c, t_m)
+            res[pname] = {"us": round(us, 3), "tflops": round(flops / (us * 1e-6) / 1e12, 2),
+                          "roofline_us": round(tr * 1e6, 3), "bound": bound_c if t_c >= t_m else "hbm",
+                          "roofline_frac": round(tr / (us * 1e-6), 4)}
+        m.sync_status()
+        out[name] = {"shape": "C=%d K=%d bs=%d density=%s N=%d %s fa=%d nnz=%d%s" % (
+            wl.C, wl.K, wl.bs, wl.density, wl.N, wl.dtype, wl.feature_axis, m.nnz,
+            (" steps=%d group=%d" % (wl.steps, wl.group)) if wl.steps > 1 else ""), "passes": res}
+        m.close()
+        del x, w, dy, y, dx, dw
+    del flush
+    out["_timing"] = ("each pass alone between CUDA events on the launching stream, median of %d, after a "
+                      "256 MB read-only sweep that evicts L2; peaks: %s" % (
+                          reps, "tensor = MEASURED_PEAKS bf16_tflops (fp16 the same rate), hbm = hbm_gbs, "
+                          "alu = derived fp32 FFMA peak %.1f TFLOP/s" % FFMA_TFLOPS))
+    return out
 
 
 # ---- CPU oracle --------------------------------------------------------------------------
@@ -589,6 +682,8 @@ def main():
                     help="seconds of CPU time for the oracle baseline sample (0 skips it)")
     ap.add_argument("--only", default="",
                     help="time a single pass (e.g. fprop_n1024) instead of the whole step; for kernel profiling")
+    ap.add_argument("--config-reps", type=int, default=20,
+                    help="timed launches per pass for the per-configuration table (0 skips it)")
     ap.add_argument("--norm", action="store_true",
                     help="time layer_norm, l2_normalize (and its gradient) and SparseProj instead of the step")
     args = ap.parse_args()

@@ -170,9 +170,26 @@ def bsmm_updat_grouped(h, xs, dys, dw, N: int, accumulate: bool = False, stream=
            "bsmm_updat_grouped")
 
 
+def _handle_shapes(h):
+    """(nnz, bs, C, K, feature_axis) of a handle, read through the C ABI."""
+    nnz, bs = ctypes.c_int64(), ctypes.c_int()
+    R, S, fa = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().bsmm_w_shape(h, ctypes.byref(nnz), ctypes.byref(bs)), "bsmm_w_shape")
+    _check(lib().bsmm_layout_info(h, ctypes.byref(R), ctypes.byref(S), ctypes.byref(fa)), "bsmm_layout_info")
+    return int(nnz.value), bs.value, R.value * bs.value, S.value * bs.value, fa.value
+
+
 def bsmm_updat_noalloc(h, x, dy, dw, N: int, accumulate: bool = False, stream=None):
     """Weight gradient that allocates no device memory (see include/bsmm.h): for callers
-    whose allocator or memory budget forbids cudaMalloc.  dw must be float32."""
+    whose allocator or memory budget forbids cudaMalloc.  x and dy are 16-bit activations
+    of minibatch N in the handle's layout, dw is float32 (nnz, bs, bs) on the same device:
+    the C call sees only pointers, so every shape is checked here first."""
+    nnz, bs, C, K, fa = _handle_shapes(h)
+    act = (lambda F: (N, F)) if fa == 1 else (lambda F: (F, N))
+    _dev(x, "x")
+    _want(x, "x", act(C), None, x.device)
+    _want(dy, "dy", act(K), x.dtype, x.device)
+    _want(dw, "dw", (nnz, bs, bs), torch.float32, x.device)
     _check(lib().bsmm_updat_noalloc(h, _ptr(x), _ptr(dy), _ptr(dw), N, _DT[x.dtype], int(accumulate),
                                     _stream(stream)), "bsmm_updat_noalloc")
 
@@ -344,6 +361,19 @@ class BlocksparseMatMul:
             dw = torch.empty(self.w_shape, dtype=dw_dtype, device=x.device)
         _want(dw, "dw", self.w_shape, None, x.device)
         bsmm_updat(self._h, x, dy, dw, N, accumulate, stream)
+        return dw
+
+    def updat_noalloc(self, x, dy, dw=None, accumulate=False, stream=None):
+        """updat with dw_dtype float32 through bsmm_updat_noalloc: the library allocates no
+        device memory for it (dw is allocated here only when not given)."""
+        _dev(x, "x")
+        _dev(dy, "dy")
+        N = self._N(x, self.C)
+        if self._N(dy, self.K) != N:
+            raise ValueError("x and dy minibatch sizes differ")
+        if dw is None:
+            dw = torch.empty(self.w_shape, dtype=torch.float32, device=x.device)
+        bsmm_updat_noalloc(self._h, x, dy, dw, N, accumulate, stream)
         return dw
 
     def updat_grouped(self, xs, dys, dw=None, accumulate=False, stream=None):

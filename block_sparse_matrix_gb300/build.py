@@ -26,12 +26,9 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _flags(debug: bool):
-    f = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),
-         "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"] + ARCH
-    if debug:
-        f += ["-DBSMM_DEBUG=1"]
-    return f
+def _flags():
+    return ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),
+            "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"] + ARCH
 
 
 def _deps_mtime() -> float:
@@ -39,7 +36,7 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, debug: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False) -> str:
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
@@ -47,7 +44,7 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
 
     def one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc, "-c", os.path.join(CSRC, src), "-o", obj] + _flags(debug)
+        cmd = [cc, "-c", os.path.join(CSRC, src), "-o", obj] + _flags()
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed on %s:\n%s\n%s" % (src, r.stdout, r.stderr))
@@ -68,4 +65,4 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, debug="--debug" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True))

@@ -2920,6 +2920,12 @@ extern "C" bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *d
     if (cudaSetDevice(h->device) != cudaSuccess) return BSMM_ERR_CUDA;
     if (!tc_supported(h, t)) return BSMM_ERR_UNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
+    // The table reaches the device by a copy from one shared host buffer that the next call
+    // overwrites; a graph captured around this call would replay that copy later and read
+    // another call's table.  Refuse before anything is enqueued.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return BSMM_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return BSMM_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_dev_ptr[h->device]) {
         // One-time set-up on this device: the array's device address (a host-side symbol
@@ -2938,7 +2944,8 @@ extern "C" bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *d
     const int ctas = noalloc_build(h);
     if (ctas < 0) return BSMM_ERR_UNSUPPORTED;       // layout needs more than the fixed 4 MB table
     if (ctas == 0) return BSMM_OK;
-    // Pageable copy: returns once the host buffer has been staged, ordered before the kernel.
+    // Pageable copy: returns once the host buffer has been staged, ordered before the kernel,
+    // which is launched without programmatic dependent launch (nothing to overlap with a copy).
     if (cudaMemcpyAsync(table, g_noalloc_host, (size_t)ctas * kTableWords * sizeof(int32_t), cudaMemcpyHostToDevice,
                         s) != cudaSuccess)
         return BSMM_ERR_CUDA;
@@ -2955,8 +2962,8 @@ extern "C" bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *d
     bsmm_status st = BSMM_ERR_UNSUPPORTED;
 #define NA_CASE(BS_, FA_)                                                                      \
     if (h->bs == BS_ && h->fa == FA_)                                                          \
-        st = bf ? launch_up<BS_, FA_, true>(h, us, g, dw, N, t, acc, s)                        \
-                : launch_up<BS_, FA_, false>(h, us, g, dw, N, t, acc, s);
+        st = bf ? launch_up<BS_, FA_, true>(h, us, g, dw, N, t, acc, s, false)                 \
+                : launch_up<BS_, FA_, false>(h, us, g, dw, N, t, acc, s, false);
     NA_CASE(32, 1)
     NA_CASE(32, 0)
     NA_CASE(16, 1)

@@ -160,9 +160,11 @@ bsmm_status bsmm_updat_grouped(bsmm_t h, const void *const *xs, const void *cons
  *   rewrites the part it uses (copied from the host, ordered on `stream` before the
  *   kernel), so calls on one stream are safe in sequence, but calls that overlap on the
  *   GPU (other streams, other threads) race on the array and must not be issued.
- * - Errors: INVALID (null handle or pointers, N < 0), ALIGN, UNSUPPORTED (fp32 inputs, or a
+ * - Errors: INVALID (null handle or pointers, N < 0), ALIGN, UNSUPPORTED (fp32 inputs, a
  *   layout whose work tables need more than the 4 MB array: about 23,000 stacks of
- *   128/bs blocks, e.g. ~95,000 blocks at bs 32), CUDA.
+ *   128/bs blocks, e.g. ~95,000 blocks at bs 32; or `stream` is capturing a graph, because
+ *   the table is copied from a host buffer that the next call overwrites), CUDA.  Every
+ *   error is returned before anything is enqueued.
  */
 bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *dy, float *dw, int N, bsmm_dtype t,
                                int accumulate, void *stream);

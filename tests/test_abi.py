@@ -140,3 +140,30 @@ def test_binding_checks_caller_tensors_before_any_call():
         bsmm._want(t, "y", (4, 6), torch.bfloat16, torch.device("cuda", 0))
     with pytest.raises(ValueError, match="CUDA tensor"):           # right shape and dtype, host memory
         bsmm._want(t, "y", (4, 6), torch.bfloat16)
+
+
+def test_noalloc_binding_checks_every_tensor_before_the_c_call(monkeypatch):
+    """bsmm_updat_noalloc's binding checks x, dy and dw against the handle's shapes (the C call
+    sees only pointers): a wrong dtype or shape raises before the library is reached."""
+    import torch
+
+    class _NoLib:
+        def __getattr__(self, name):
+            raise AssertionError("C call reached: " + name)
+
+    monkeypatch.setattr(bsmm, "_handle_shapes", lambda h: (3, 32, 96, 128, 1))   # nnz, bs, C, K, fa
+    monkeypatch.setattr(bsmm, "_dev", lambda t, what: None)                      # CPU tensors stand in
+    monkeypatch.setattr(bsmm, "lib", lambda: _NoLib())
+    x = torch.zeros((64, 96), dtype=torch.bfloat16)
+    dy = torch.zeros((64, 128), dtype=torch.bfloat16)
+    dw = torch.zeros((3, 32, 32), dtype=torch.float32)
+    bad = [(x, dy, dw.bfloat16()),                       # dw not float32
+           (x, dy, dw[:2]),                              # dw shape
+           (x[:32], dy, dw),                             # x minibatch
+           (x, dy[:, :96], dw),                          # dy features
+           (x, dy.half(), dw)]                           # dy dtype differs from x
+    for a, b, c in bad:
+        with pytest.raises(ValueError):
+            bsmm.bsmm_updat_noalloc(None, a, b, c, 64)
+    with pytest.raises(AssertionError, match="C call reached"):
+        bsmm.bsmm_updat_noalloc(None, x, dy, dw, 64)
