@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbsmm.so")
-SOURCES = ["bsmm_api.cu", "bsmm_lut.cu", "bsmm_simt.cu", "bsmm_tc.cu", "bsmm_norm.cu", "bsmm_wnorm.cu", "bsmm_proj.cu"]
+SOURCES = ["bsmm_api.cu", "bsmm_lut.cu", "bsmm_simt.cu", "bsmm_tc.cu", "bsmm_sp.cu", "bsmm_norm.cu",
+           "bsmm_wnorm.cu", "bsmm_proj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

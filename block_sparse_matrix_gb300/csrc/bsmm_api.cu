@@ -38,6 +38,7 @@ bool use_tc(bsmm_ctx *h, bsmm_dtype t)
 void free_ctx(bsmm_ctx *h)
 {
     tc_release(h);
+    sp_release(h);
     cudaFree(h->d_layout);
     cudaFree(h->d_row_ptr);
     cudaFree(h->d_row_ent);

@@ -33,6 +33,7 @@ struct bsmm_ctx {
 
     // Tensor-core schedules (built lazily by the tcgen05 path).
     void *tc = nullptr;
+    void *sp = nullptr;        // sparse-window kernel plans and (F, N) panel scratch (bsmm_sp.cu)
     int tc_wlog = -1;   // fprop/bprop window size override (log2), from BSMM_TC_WLOG; -1 = automatic
     int tc_stage_kb = -1;  // fprop/bprop per-CTA stage budget override (KB), from BSMM_TC_STAGE_KB
 };
@@ -76,4 +77,10 @@ bsmm_status tc_bprop(bsmm_ctx *h, const void *dy, const void *w, void *dx, int N
 bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dtype t,
                      int accumulate, cudaStream_t s);
 void tc_release(bsmm_ctx *h);
+
+// Sparse-window fprop/bprop with the activation operand in tensor memory (bsmm_sp.cu).
+bool sp_supported(const bsmm_ctx *h, bsmm_dtype t);
+bsmm_status sp_fb(bsmm_ctx *h, bool bwd, const void *act, const void *w, void *out, int N, bsmm_dtype t,
+                  cudaStream_t s);
+void sp_release(bsmm_ctx *h);
 bsmm_status launch_wait_selftest(bsmm_ctx *h, uint64_t limit_ns, cudaStream_t s);

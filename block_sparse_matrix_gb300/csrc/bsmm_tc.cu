@@ -2721,18 +2721,35 @@ bool tc_supported(bsmm_ctx *h, bsmm_dtype t)
     return major == 10 && minor == 3;
 }
 
+// fprop/bprop dispatch: the dense-tile kernels (bs = 32, at least a quarter of the layout
+// present); the sparse-window kernel for block sizes 16 and 8 (k_tc_sp, bsmm_sp.cu); else the
+// window kernel, which is faster for sparse bs = 32 layouts at a minibatch of 128 (fewer, larger
+// blocks per source).  BSMM_TC_FB = window | sp | dense | dense1 forces a family.
+template <bool BWD>
+bsmm_status fb_tc(bsmm_ctx *h, const void *act, const void *w, void *out, int N, bsmm_dtype t, cudaStream_t s)
+{
+    const char *e = getenv("BSMM_TC_FB");
+    const bool force_window = e && !strcmp(e, "window");
+    const bool force_sp = e && !strcmp(e, "sp");
+    if (!force_window && !force_sp) {
+        const bsmm_status st = fbd_try<BWD>(h, act, w, out, N, t, s);
+        if (st != BSMM_ERR_UNSUPPORTED) return st;
+    }
+    if (force_sp || (!force_window && h->bs != 32)) {
+        const bsmm_status st = sp_fb(h, BWD, act, w, out, N, t, s);
+        if (st != BSMM_ERR_UNSUPPORTED) return st;
+    }
+    return fb_dispatch<BWD>(h, act, w, out, N, t, s);
+}
+
 bsmm_status tc_fprop(bsmm_ctx *h, const void *x, const void *w, void *y, int N, bsmm_dtype t, cudaStream_t s)
 {
-    const bsmm_status st = fbd_try<false>(h, x, w, y, N, t, s);
-    if (st != BSMM_ERR_UNSUPPORTED) return st;
-    return fb_dispatch<false>(h, x, w, y, N, t, s);
+    return fb_tc<false>(h, x, w, y, N, t, s);
 }
 
 bsmm_status tc_bprop(bsmm_ctx *h, const void *dy, const void *w, void *dx, int N, bsmm_dtype t, cudaStream_t s)
 {
-    const bsmm_status st = fbd_try<true>(h, dy, w, dx, N, t, s);
-    if (st != BSMM_ERR_UNSUPPORTED) return st;
-    return fb_dispatch<true>(h, dy, w, dx, N, t, s);
+    return fb_tc<true>(h, dy, w, dx, N, t, s);
 }
 
 bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dtype t, int accumulate,

@@ -203,6 +203,27 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- cp.async (LSU path: any 16-byte chunk to any 16-byte aligned shared address) ----------
+
+// Copies 16 bytes global -> shared when `pred` is set; with src_bytes = 0 nothing is read and
+// the 16 bytes are zero-filled.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16_if(uint32_t pred, void *dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q cp.async.cg.shared.global [%1], [%2], 16, %3;\n\t}" ::"r"(pred),
+                 "r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has landed; the arrival
+// counts against the barrier's expected count (.noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---- Tensor Memory ---------------------------------------------------------------------
 
 // Whole warp: allocate ncols (power of two >= 32) columns; base address written to *dst.
@@ -296,6 +317,15 @@ __device__ __forceinline__ void mma_pair_commit_mc(uint64_t *bar, uint16_t cta_m
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
                      smem_u32(bar)),
                  "h"(cta_mask)
+                 : "memory");
+}
+
+// Commit performed only when `issue` is set (one lane of a warp that runs its loop converged).
+__device__ __forceinline__ void mma_commit_if(uint32_t issue, uint64_t *bar)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+                 "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(issue),
+                 "r"(smem_u32(bar))
                  : "memory");
 }
 

@@ -298,6 +298,7 @@ def test_window_sizes_bit_identical(monkeypatch, bs, fa, dtype):
     L, x, w, dy, ref_y, ref_dx, _ = small_case(bs, fa, dtype)
     xc, wc, dyc = x.cuda(), w.cuda(), dy.cuda()
     outs = []
+    monkeypatch.setenv("BSMM_TC_FB", "window")
     for wlog in range(0, 5):
         monkeypatch.setenv("BSMM_TC_WLOG", str(wlog))
         m = make(L, bs, fa, "auto")
@@ -391,7 +392,7 @@ def test_fprop_bprop_variants_bs32(monkeypatch, fa, dtype, R, S, p, N):
     w = wk.normals((nnz, bs, bs), 900 + R + S, float(1 / np.sqrt(R * bs * p)), dtype)
     ref_y, ref_dx = o.fprop(L, bs, x, w, fa), o.bprop(L, bs, dy, w, fa)
     outs = {}
-    for variant in ("window", "dense1", "dense"):
+    for variant in ("window", "sp", "dense1", "dense"):
         monkeypatch.setenv("BSMM_TC_FB", variant)
         m = make(L, bs, fa, "auto")
         y = torch.full(m.o_shape(N), float("nan"), dtype=DT[dtype], device="cuda")
@@ -402,9 +403,10 @@ def test_fprop_bprop_variants_bs32(monkeypatch, fa, dtype, R, S, p, N):
         assert rel_fro(cpu64(y), ref_y) <= TIGHT[dtype]
         assert rel_fro(cpu64(dx), ref_dx) <= TIGHT[dtype]
         outs[variant] = (cpu64(y), cpu64(dx))
-    # both schemes accumulate in fp32 and round once: they agree to a few output ulps
-    for a, b in zip(outs["window"], outs["dense"]):
-        assert rel_fro(a, b) <= TIGHT[dtype]
+    # every scheme accumulates in fp32 and rounds once: they agree to a few output ulps
+    for other in ("sp", "dense"):
+        for a, b in zip(outs["window"], outs[other]):
+            assert rel_fro(a, b) <= TIGHT[dtype]
     # one-CTA and CTA-pair dense tiles add the same products in the same order
     for a, b in zip(outs["dense1"], outs["dense"]):
         assert np.array_equal(a, b)
