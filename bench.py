@@ -17,6 +17,10 @@ prologues under programmatic dependent launch).  A second pass over the same K
 steps brackets every kernel with events, which gives each kernel's own duration
 for the per-pass table and the roofline object.
 
+With --gpus N under torchrun every rank holds its own minibatch rows (a global minibatch of N
+times as many rows, weak scaling) and the replicated weight; each weight gradient is summed over
+the ranks by one NCCL all-reduce inside the timed step (block_sparse_matrix_gb300.dp).
+
 --impl reference times the float64 CPU oracle (the only other implementation
 of the method here) on a bounded sample of the same workload.
 """
@@ -37,7 +41,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from block_sparse_matrix_gb300 import workloads as wk  # noqa: E402
+from block_sparse_matrix_gb300 import dp, workloads as wk  # noqa: E402
 
 METRIC = "effective TFLOP/s per pass (fprop/bprop/updat) and % of roofline on 1 GB300"
 WORKLOAD = ("hidden C=K=4096, block_size=32, 128x128 Bernoulli(0.5) layout, bf16 inputs with fp32 accumulate, "
@@ -228,10 +232,18 @@ def run_ours(args):
         else:
             bsmm.bsmm_updat(m.handle, d["x%d" % N], d["dy%d" % N], d["dw%d" % N], N)
 
+    def exchange(name, d):
+        # Data parallel over the minibatch: every rank holds its own N rows of a global minibatch of
+        # N * world rows and the replicated weight; the weight gradient is summed over the ranks
+        # (one NCCL all-reduce per weight gradient; none on one GPU).
+        if ws > 1 and name.startswith("updat"):
+            dp.allreduce_dw(d["dw%s" % name.split("_n")[1]])
+
     def step(i):
         d = sets[i % NSETS]
         for p in passes:
             launch_pass(p[0], d)
+            exchange(p[0], d)
 
     # Warm-up (W steps), then count our launches per step.
     warm = max(3, args.warmup)
@@ -275,6 +287,7 @@ def run_ours(args):
                     launch_pass(p[0], d)
                     if per_pass:
                         ev_pass[i][j][1].record(stream)
+                    exchange(p[0], d)
                 ev_step[i][1].record(stream)
         return ev_step, ev_pass
 
@@ -341,7 +354,9 @@ def run_ours(args):
                 "warmup": warm, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normals)",
                 "config": {"workload": WORKLOAD, "nnz": nnz, "l2": "4 rotating input/output sets, ~330 MB > 2x L2",
-                           "parallelism": "replicas" if ws > 1 else "single GPU"},
+                           "parallelism": ("data parallel over the minibatch: %d rows per GPU, weight gradients "
+                                           "all-reduced over NCCL inside the step" % max(Ns)) if ws > 1
+                           else "single GPU"},
                 "passes": per_pass, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "configs": configs,
                 "clocks": clocks, "gpu_launches": launches_per_step * K_steps,
                 "wall_s_timed_region": round(wall1 - wall0, 3)}

@@ -1,8 +1,9 @@
-"""Host logic of the multi-GPU bench (replicas, weak scaling) on CPU: two gloo ranks.
+"""Host logic of the multi-GPU bench (weak scaling) on CPU: two gloo ranks.
 
-Each rank of `bench.py --gpus N` runs the whole step on its own GPU (the path has no data
-exchange in this configuration: replicas only).  The job's step time is the slowest rank's,
-its value the sum of the ranks' work over that time; the reference arm runs on rank 0 only.
+Each rank of `bench.py --gpus N` runs the step on its own share of the minibatch and all-reduces
+the weight gradients (block_sparse_matrix_gb300.dp; tests/test_data_parallel.py checks the sum).
+The job's step time is the slowest rank's, its value the sum of the ranks' work over that time;
+the reference arm runs on rank 0 only.
 """
 import os
 import socket
