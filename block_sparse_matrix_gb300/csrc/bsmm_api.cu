@@ -206,7 +206,7 @@ static bsmm_status updat_common(bsmm_ctx *h, const GroupPtrs &g, void *dw, int N
         if (!g.x[i] || !g.dy[i]) return BSMM_ERR_INVALID;
         if (!aligned16(g.x[i]) || !aligned16(g.dy[i])) return BSMM_ERR_ALIGN;
     }
-    if (dw_t == BSMM_F32 && use_tc(h, t)) return tc_updat(h, g, (float *)dw, N, t, accumulate, s);
+    if (use_tc(h, t)) return tc_updat(h, g, dw, N, t, dw_t, accumulate, s);
     return simt_updat(h, g, dw, N, t, dw_t, accumulate, s);
 }
 

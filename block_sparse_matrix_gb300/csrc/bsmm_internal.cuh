@@ -74,7 +74,7 @@ bsmm_status tc_fprop(bsmm_ctx *h, const void *x, const void *w, void *y, int N, 
                      cudaStream_t s);
 bsmm_status tc_bprop(bsmm_ctx *h, const void *dy, const void *w, void *dx, int N, bsmm_dtype t,
                      cudaStream_t s);
-bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dtype t,
+bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, void *dw, int N, bsmm_dtype t, bsmm_dtype dw_t,
                      int accumulate, cudaStream_t s);
 void tc_release(bsmm_ctx *h);
 

@@ -916,11 +916,42 @@ struct UpMaps {
 };
 
 struct UpParams {
-    float *dw;
+    void *dw;                   // dw_dtype: float32, or the inputs' 16-bit type
     const int32_t *table;
     int32_t *status;
     int N, G, accumulate;
+    int dwt;                    // 0: float32 dW, 1: fp16, 2: bf16
 };
+
+// Stores 4 consecutive dW values at element `off` in the output type; with accumulate, adds the
+// stored values in float32 first and rounds the sum once.
+__device__ __forceinline__ void up_store4(void *dw, size_t off, float4 v, int accumulate, int dwt)
+{
+    if (dwt == 0) {
+        float *d = static_cast<float *>(dw) + off;
+        if (accumulate) {
+            const float4 a = *reinterpret_cast<const float4 *>(d);
+            v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+        }
+        *reinterpret_cast<float4 *>(d) = v;
+        return;
+    }
+    uint16_t *d = static_cast<uint16_t *>(dw) + off;
+    if (accumulate) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(d);
+        float f[4];
+        const uint16_t hs[4] = {(uint16_t)(a.x & 0xFFFFu), (uint16_t)(a.x >> 16), (uint16_t)(a.y & 0xFFFFu),
+                                (uint16_t)(a.y >> 16)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            f[i] = dwt == 2 ? __uint_as_float((uint32_t)hs[i] << 16) : __half2float(__ushort_as_half(hs[i]));
+        v.x += f[0]; v.y += f[1]; v.z += f[2]; v.w += f[3];
+    }
+    uint2 o;
+    o.x = dwt == 2 ? pack2<true>(v.x, v.y) : pack2<false>(v.x, v.y);
+    o.y = dwt == 2 ? pack2<true>(v.z, v.w) : pack2<false>(v.z, v.w);
+    *reinterpret_cast<uint2 *>(d) = o;
+}
 
 template <int BSE, int FA> struct UpGeo {
     static constexpr int TK = 64;                                   // minibatch rows per stage
@@ -1111,15 +1142,8 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
                     const int sl = q * (32 / BSE) + o / BLK;
                     const int r = o / BS, c = (o % BS) / 4;
                     const float4 val = *reinterpret_cast<const float4 *>(stg + r * BS + ((c ^ (r & (CH - 1))) * 4));
-                    if (sl < ut[1] && !aborted) {
-                        float *dst = p.dw + (size_t)ut[2 + 5 * sl + 1] * (BS * BS) + (o % BLK);
-                        float4 r4 = val;
-                        if (p.accumulate) {
-                            const float4 a = *reinterpret_cast<const float4 *>(dst);
-                            r4.x += a.x; r4.y += a.y; r4.z += a.z; r4.w += a.w;
-                        }
-                        *reinterpret_cast<float4 *>(dst) = r4;
-                    }
+                    if (sl < ut[1] && !aborted)
+                        up_store4(p.dw, (size_t)ut[2 + 5 * sl + 1] * (BS * BS) + (o % BLK), val, p.accumulate, p.dwt);
                 }
                 __syncwarp();                                   // reads done before the next unit's writes
             } else if (slot < ut[1] && !aborted) {
@@ -1130,16 +1154,11 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
                     for (int ks = 0; ks < 2; ++ks) {
                         const int32_t id = rec[1 + cs * 2 + ks];
                         if (id < 0) continue;
-                        float *dst = p.dw + ((size_t)id * 8 + i8) * 8;
 #pragma unroll
-                        for (int j = 0; j < 8; j += 4) {
-                            float4 o = make_float4(v[ks * 8 + j], v[ks * 8 + j + 1], v[ks * 8 + j + 2], v[ks * 8 + j + 3]);
-                            if (p.accumulate) {
-                                float4 a = *reinterpret_cast<float4 *>(dst + j);
-                                o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
-                            }
-                            *reinterpret_cast<float4 *>(dst + j) = o;
-                        }
+                        for (int j = 0; j < 8; j += 4)
+                            up_store4(p.dw, ((size_t)id * 8 + i8) * 8 + j,
+                                      make_float4(v[ks * 8 + j], v[ks * 8 + j + 1], v[ks * 8 + j + 2], v[ks * 8 + j + 3]),
+                                      p.accumulate, p.dwt);
                     }
                 }
             }
@@ -1323,16 +1342,12 @@ k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
                         make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
                 __syncwarp();
                 if (!aborted) {
-                    float *blk = p.dw + (size_t)id * 1024;
 #pragma unroll
                     for (int k4 = 0; k4 < 8; ++k4) {
                         const int o = k4 * 128 + lane * 4, r = o / 32, c = (o % 32) / 4;
-                        float4 r4 = *reinterpret_cast<const float4 *>(stg + r * 32 + ((c ^ (r & 7)) * 4));
-                        if (p.accumulate) {
-                            const float4 a = *reinterpret_cast<const float4 *>(blk + o);
-                            r4.x += a.x; r4.y += a.y; r4.z += a.z; r4.w += a.w;
-                        }
-                        *reinterpret_cast<float4 *>(blk + o) = r4;
+                        up_store4(p.dw, (size_t)id * 1024 + o,
+                                  *reinterpret_cast<const float4 *>(stg + r * 32 + ((c ^ (r & 7)) * 4)), p.accumulate,
+                                  p.dwt);
                     }
                 }
                 __syncwarp();                                   // reads done before the next block's writes
@@ -1543,16 +1558,12 @@ k_tc_updat_pair(const __grid_constant__ UpMaps maps, const UpParams p)
                         make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
                 __syncwarp();
                 if (!aborted) {
-                    float *blk = p.dw + (size_t)id * 1024;
 #pragma unroll
                     for (int k4 = 0; k4 < 8; ++k4) {
                         const int o = k4 * 128 + lane * 4, r = o / 32, c = (o % 32) / 4;
-                        float4 r4 = *reinterpret_cast<const float4 *>(stg + r * 32 + ((c ^ (r & 7)) * 4));
-                        if (p.accumulate) {
-                            const float4 a = *reinterpret_cast<const float4 *>(blk + o);
-                            r4.x += a.x; r4.y += a.y; r4.z += a.z; r4.w += a.w;
-                        }
-                        *reinterpret_cast<float4 *>(blk + o) = r4;
+                        up_store4(p.dw, (size_t)id * 1024 + o,
+                                  *reinterpret_cast<const float4 *>(stg + r * 32 + ((c ^ (r & 7)) * 4)), p.accumulate,
+                                  p.dwt);
                     }
                 }
                 __syncwarp();                                   // reads done before the next block's writes
@@ -2304,9 +2315,11 @@ bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const FbStages &geo, const void 
     return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
+int dw_code(bsmm_dtype dw_t) { return dw_t == BSMM_F32 ? 0 : dw_t == BSMM_F16 ? 1 : 2; }
+
 template <int BS, int FA, bool BF16>
-bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, float *dw, int N, bsmm_dtype t, int acc,
-                      cudaStream_t s, bool pdl = true)
+bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, void *dw, int N, bsmm_dtype t, int acc,
+                      cudaStream_t s, bsmm_dtype dw_t = BSMM_F32, bool pdl = true)
 {
     constexpr int BSE = BS == 8 ? 16 : BS;
     using G = UpGeo<BSE, FA>;
@@ -2331,6 +2344,7 @@ bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, float *dw, i
     p.N = N;
     p.G = g.G;
     p.accumulate = acc;
+    p.dwt = dw_code(dw_t);
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat<BS, FA, BF16>;
     static std::atomic<int> attr_set{-1};
@@ -2390,8 +2404,8 @@ FbStages choose_stages(const bsmm_ctx *h, int N, int64_t units, int W)
 }
 
 template <int FA, bool BF16>
-bsmm_status launch_up_dense(bsmm_ctx *h, UpDenseSched &us, const GroupPtrs &g, float *dw, int N, bsmm_dtype t,
-                            int acc, cudaStream_t s)
+bsmm_status launch_up_dense(bsmm_ctx *h, UpDenseSched &us, const GroupPtrs &g, void *dw, int N, bsmm_dtype t,
+                            int acc, cudaStream_t s, bsmm_dtype dw_t)
 {
     using G = UpDenseGeo;
     const int C = h->R * 32, K = h->S * 32;
@@ -2415,6 +2429,7 @@ bsmm_status launch_up_dense(bsmm_ctx *h, UpDenseSched &us, const GroupPtrs &g, f
     p.N = N;
     p.G = g.G;
     p.accumulate = acc;
+    p.dwt = dw_code(dw_t);
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat_dense<FA, BF16>;
     static std::atomic<int> attr_set{-1};
@@ -2429,8 +2444,8 @@ bsmm_status launch_up_dense(bsmm_ctx *h, UpDenseSched &us, const GroupPtrs &g, f
 }
 
 template <int FA, bool BF16>
-bsmm_status launch_up_pair(bsmm_ctx *h, UpPairSched &us, const GroupPtrs &g, float *dw, int N, bsmm_dtype t,
-                           int acc, cudaStream_t s)
+bsmm_status launch_up_pair(bsmm_ctx *h, UpPairSched &us, const GroupPtrs &g, void *dw, int N, bsmm_dtype t,
+                           int acc, cudaStream_t s, bsmm_dtype dw_t)
 {
     using G = UpPairGeo;
     const int C = h->R * 32, K = h->S * 32;
@@ -2454,6 +2469,7 @@ bsmm_status launch_up_pair(bsmm_ctx *h, UpPairSched &us, const GroupPtrs &g, flo
     p.N = N;
     p.G = g.G;
     p.accumulate = acc;
+    p.dwt = dw_code(dw_t);
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat_pair<FA, BF16>;
     static std::atomic<int> attr_set{-1};
@@ -2752,8 +2768,8 @@ bsmm_status tc_bprop(bsmm_ctx *h, const void *dy, const void *w, void *dx, int N
     return fb_tc<true>(h, dy, w, dx, N, t, s);
 }
 
-bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dtype t, int accumulate,
-                     cudaStream_t s)
+bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, void *dw, int N, bsmm_dtype t, bsmm_dtype dw_t,
+                     int accumulate, cudaStream_t s)
 {
     TcState *st = state(h);
     const bool bf = t == BSMM_BF16;
@@ -2775,10 +2791,10 @@ bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dty
         }
         if (st->upp->built) {
             if (st->upp->ctas == 0) return BSMM_OK;
-            if (h->fa) return bf ? launch_up_pair<1, true>(h, *st->upp, g, dw, N, t, accumulate, s)
-                                 : launch_up_pair<1, false>(h, *st->upp, g, dw, N, t, accumulate, s);
-            return bf ? launch_up_pair<0, true>(h, *st->upp, g, dw, N, t, accumulate, s)
-                      : launch_up_pair<0, false>(h, *st->upp, g, dw, N, t, accumulate, s);
+            if (h->fa) return bf ? launch_up_pair<1, true>(h, *st->upp, g, dw, N, t, accumulate, s, dw_t)
+                                 : launch_up_pair<1, false>(h, *st->upp, g, dw, N, t, accumulate, s, dw_t);
+            return bf ? launch_up_pair<0, true>(h, *st->upp, g, dw, N, t, accumulate, s, dw_t)
+                      : launch_up_pair<0, false>(h, *st->upp, g, dw, N, t, accumulate, s, dw_t);
         }
     }
     if (dense) {
@@ -2788,10 +2804,10 @@ bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dty
             if (!st->upd->built && !build_up_dense(h, *st->upd)) return BSMM_ERR_OOM;
         }
         if (st->upd->ctas == 0) return BSMM_OK;
-        if (h->fa) return bf ? launch_up_dense<1, true>(h, *st->upd, g, dw, N, t, accumulate, s)
-                             : launch_up_dense<1, false>(h, *st->upd, g, dw, N, t, accumulate, s);
-        return bf ? launch_up_dense<0, true>(h, *st->upd, g, dw, N, t, accumulate, s)
-                  : launch_up_dense<0, false>(h, *st->upd, g, dw, N, t, accumulate, s);
+        if (h->fa) return bf ? launch_up_dense<1, true>(h, *st->upd, g, dw, N, t, accumulate, s, dw_t)
+                             : launch_up_dense<1, false>(h, *st->upd, g, dw, N, t, accumulate, s, dw_t);
+        return bf ? launch_up_dense<0, true>(h, *st->upd, g, dw, N, t, accumulate, s, dw_t)
+                  : launch_up_dense<0, false>(h, *st->upd, g, dw, N, t, accumulate, s, dw_t);
     }
     {
         std::lock_guard<std::mutex> lk(st->mu);
@@ -2800,8 +2816,8 @@ bsmm_status tc_updat(bsmm_ctx *h, const GroupPtrs &g, float *dw, int N, bsmm_dty
     if (st->up.ctas == 0) return BSMM_OK;
 #define UP_CASE(BS_, FA_)                                                                         \
     if (h->bs == BS_ && h->fa == FA_)                                                             \
-        return bf ? launch_up<BS_, FA_, true>(h, st->up, g, dw, N, t, accumulate, s)             \
-                  : launch_up<BS_, FA_, false>(h, st->up, g, dw, N, t, accumulate, s);
+        return bf ? launch_up<BS_, FA_, true>(h, st->up, g, dw, N, t, accumulate, s, dw_t)       \
+                  : launch_up<BS_, FA_, false>(h, st->up, g, dw, N, t, accumulate, s, dw_t);
     UP_CASE(32, 1)
     UP_CASE(32, 0)
     UP_CASE(16, 1)
@@ -2979,8 +2995,8 @@ extern "C" bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *d
     bsmm_status st = BSMM_ERR_UNSUPPORTED;
 #define NA_CASE(BS_, FA_)                                                                      \
     if (h->bs == BS_ && h->fa == FA_)                                                          \
-        st = bf ? launch_up<BS_, FA_, true>(h, us, g, dw, N, t, acc, s, false)                 \
-                : launch_up<BS_, FA_, false>(h, us, g, dw, N, t, acc, s, false);
+        st = bf ? launch_up<BS_, FA_, true>(h, us, g, dw, N, t, acc, s, BSMM_F32, false)       \
+                : launch_up<BS_, FA_, false>(h, us, g, dw, N, t, acc, s, BSMM_F32, false);
     NA_CASE(32, 1)
     NA_CASE(32, 0)
     NA_CASE(16, 1)

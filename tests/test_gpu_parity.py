@@ -164,10 +164,16 @@ def test_parity_small(kernel, bs, fa, dtype):
     m.updat(xc, dyc, dw=dw2, accumulate=True)
     m.sync_status()
     assert rel_fro(cpu64(dw2), 2 * ref_dw) <= TOL_DW[dtype]
-    # 16-bit dW output when the dtype allows it (dw_dtype of the README)
-    if dtype != "f32" and kernel == "simt":
+    # 16-bit dW output (dw_dtype of the README): float32 sums rounded once to the input type, on the
+    # tensor-core kernels under "auto"; accumulating adds in float32 and rounds once more
+    if dtype != "f32":
         dwh = m.updat(xc, dyc, dw_dtype=DT[dtype])
+        m.sync_status()
+        assert dwh.dtype == DT[dtype]
         assert rel_fro(cpu64(dwh), ref_dw) <= TIGHT[dtype]
+        m.updat(xc, dyc, dw=dwh, accumulate=True)
+        m.sync_status()
+        assert rel_fro(cpu64(dwh), 2 * ref_dw) <= TIGHT[dtype]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -348,9 +354,15 @@ def test_updat_variants_bs32(monkeypatch, variant, fa, p, G):
     m.sync_status()
     assert rel_fro(cpu64(dw), 2 * ref) <= TOL_DW["bf16"]
     if G == 1:
+        ref1 = o.updat(L, bs, xs[0], dys[0], fa)
         dw1 = m.updat(xs[0].cuda(), dys[0].cuda())
         m.sync_status()
-        assert rel_fro(cpu64(dw1), o.updat(L, bs, xs[0], dys[0], fa)) <= TOL_DW["bf16"]
+        assert rel_fro(cpu64(dw1), ref1) <= TOL_DW["bf16"]
+        # bf16 dW from the same kernel: one rounding of the float32 sums
+        dwh = m.updat(xs[0].cuda(), dys[0].cuda(), dw_dtype=torch.bfloat16)
+        m.sync_status()
+        assert rel_fro(cpu64(dwh), ref1) <= TIGHT["bf16"]
+        assert np.array_equal(cpu64(dwh), cpu64(dw1.bfloat16()))
 
 
 @pytest.mark.parametrize("fa", [0, 1])
