@@ -696,6 +696,14 @@ bool sp_build(const bsmm_ctx *h, bool bwd, int W, int split, int E, int R, SpSch
         }
     }
     if (longest > kSpSchedWords) return true;                  // built stays false
+    // BSMM_SP_TEST_BAD_ID (tests only): the first record of the first window names block nnz + 5,
+    // which the kernel must refuse (zero-filled, BSMM_ERR_BOUNDS) without touching memory past w
+    if (getenv("BSMM_SP_TEST_BAD_ID") && stream.size() > (size_t)kSpHead + 1 && stream[kSpHead] != 0) {
+        const uint32_t hdr = stream[kSpHead];
+        const size_t r0 = kSpHead + kSpChunkHead + (hdr >> 16);
+        if ((hdr & 0xFFFFu) > 0 && r0 < stream.size())
+            stream[r0] = (stream[r0] & ~kIdMask) | (uint32_t)((h->nnz + 5) & kIdMask);
+    }
     for (int w = 0; w < nwin; ++w) order[w] = w;
     std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return work[a] > work[b]; });
     sc.W = W;

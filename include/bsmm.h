@@ -58,7 +58,9 @@ typedef enum {
     BSMM_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
     BSMM_ERR_TIMEOUT = 5,      /* a device-side bounded wait gave up (sticky) */
     BSMM_ERR_OOM = 6,          /* device allocation failed */
-    BSMM_ERR_BOUNDS = 7        /* a device-side index check failed (sticky) */
+    BSMM_ERR_BOUNDS = 7        /* a device-side index check failed (sticky): a kernel found a
+                                  block id or source out of range in its schedule and skipped the
+                                  access (the sparse-window fprop/bprop kernels check every one) */
 } bsmm_status;
 
 typedef enum { BSMM_F32 = 0, BSMM_F16 = 1, BSMM_BF16 = 2 } bsmm_dtype;

@@ -247,6 +247,21 @@ def test_config_full_size(kernel, name):
         assert rel_fro(cpu64(dw), o.updat(L, wl.bs, inp.x, inp.dy, 1)) <= TOL["f32"]
 
 
+def test_headline_config_every_output():
+    """hidden 4096, block 32, 50% dense, minibatch 1024, bf16: every output of the three passes on
+    the tensor-core path against the float64 oracle over the whole tensors (not a sample)."""
+    wl = wk.CONFIGS["h4096_b32_p50_n1024"]
+    inp = wk.make_inputs(wl)
+    L = inp.layout
+    m = make(L, wl.bs, 1, "auto")
+    x, w, dy = inp.x.cuda(), inp.w.cuda(), inp.dy.cuda()
+    y, dx, dw = m.fprop(x, w), m.bprop(dy, w), m.updat(x, dy)
+    m.sync_status()
+    assert rel_fro(cpu64(y), o.fprop(L, wl.bs, inp.x, inp.w, 1)) <= TIGHT["bf16"]
+    assert rel_fro(cpu64(dx), o.bprop(L, wl.bs, inp.dy, inp.w, 1)) <= TIGHT["bf16"]
+    assert rel_fro(cpu64(dw), o.updat(L, wl.bs, inp.x, inp.dy, 1)) <= TOL_DW["bf16"]
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_config5_recurrent_grouped(kernel):
     """16 timesteps share W: per-step fprop/bprop, weight gradient grouped 8 steps per

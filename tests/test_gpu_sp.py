@@ -107,3 +107,24 @@ def test_sp_integer_inputs_exact(monkeypatch, bs, fa, dtype, split):
     y, dx = _run(L, bs, fa, dtype, x, w, dy, N)
     assert np.array_equal(y, o.fprop(L, bs, x, w, fa))
     assert np.array_equal(dx, o.bprop(L, bs, dy, w, fa))
+
+
+@pytest.mark.parametrize("bs,fa", [(16, 0), (8, 1), (32, 1)])
+def test_sp_refuses_an_out_of_range_block_id(monkeypatch, bs, fa):
+    """Fault injection on the host: a test hook makes the schedule name block nnz + 5.  The kernel
+    checks every block id before its copy, zero-fills that block and records BSMM_ERR_BOUNDS; no
+    memory past w is read, and the next call on a fresh schedule is correct again."""
+    from block_sparse_matrix_gb300 import bsmm
+    monkeypatch.setenv("BSMM_TC_FB", "sp")
+    L, x, w, dy = _problem(bs, fa, "bf16", 12, 11, 0.4, 136)
+    m = BlocksparseMatMul(L, block_size=bs, feature_axis=fa)
+    monkeypatch.setenv("BSMM_SP_TEST_BAD_ID", "1")
+    y = m.fprop(x.cuda(), w.cuda())
+    with pytest.raises(bsmm.BsmmError) as e:
+        m.sync_status()
+    assert e.value.code == bsmm.ERR_BOUNDS
+    assert torch.isfinite(y.float()).all()
+    m.close()
+    monkeypatch.delenv("BSMM_SP_TEST_BAD_ID")
+    y2, _ = _run(L, bs, fa, "bf16", x, w, dy, 136)
+    assert rel_fro(y2, o.fprop(L, bs, x, w, fa)) <= TIGHT["bf16"]
