@@ -515,6 +515,44 @@ def run_configs(dev, peaks, reps):
     return out
 
 
+def run_single_pass(args):
+    """--pass CONFIG:PASS: one pass of one benchmark configuration, launched warmup + steps times
+    (cold: an L2-evicting sweep before each), median microseconds as one JSON line.  For kernel
+    profiles of any configuration (ncu -k ... python bench.py --pass h8192_b16_p10:fprop)."""
+    name, pname = args.single_pass.split(":")
+    dev = torch.device("cuda", 0)
+    peaks, _ = load_peaks()
+    wl = wk.CONFIGS[name]
+    from block_sparse_matrix_gb300 import bsmm
+    inp = wk.make_inputs(wl, steps=min(wl.steps, wl.group) if wl.steps > 1 else None)
+    m = bsmm.BlocksparseMatMul(inp.layout, block_size=wl.bs, feature_axis=wl.feature_axis)
+    x, w, dy = inp.x.to(dev), inp.w.to(dev), inp.dy.to(dev)
+    y = torch.empty(m.o_shape(wl.N), dtype=x.dtype, device=dev)
+    dx = torch.empty(m.i_shape(wl.N), dtype=x.dtype, device=dev)
+    dw = torch.zeros(m.w_shape, dtype=torch.float32, device=dev)
+    calls = {"fprop": lambda: m.fprop(x, w, y), "bprop": lambda: m.bprop(dy, w, dx), "updat": lambda: m.updat(x, dy, dw)}
+    if wl.steps > 1:
+        xs = [a.to(dev) for a in inp.xs]
+        dys = [a.to(dev) for a in inp.dys]
+        calls["updat_grouped_g%d" % wl.group] = lambda: m.updat_grouped(xs, dys, dw=dw, accumulate=True)
+    fn = calls[pname]
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    for _ in range(max(1, args.warmup)):
+        fn()
+    evs = []
+    for _ in range(args.steps):
+        flush.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    m.sync_status()
+    us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1000.0
+    print(json.dumps({"pass": args.single_pass, "us": round(us, 3), "steps": args.steps, "nnz": m.nnz}), flush=True)
+
+
 # ---- CPU oracle --------------------------------------------------------------------------
 
 def oracle_sample(wl, inp, n_rows, n_blocks, nthreads, N):
@@ -699,10 +737,14 @@ def main():
                     help="time a single pass (e.g. fprop_n1024) instead of the whole step; for kernel profiling")
     ap.add_argument("--config-reps", type=int, default=20,
                     help="timed launches per pass for the per-configuration table (0 skips it)")
+    ap.add_argument("--pass", dest="single_pass", default="",
+                    help="CONFIG:PASS -- time one pass of one configuration (e.g. h8192_b16_p10:fprop), for profiles")
     ap.add_argument("--norm", action="store_true",
                     help="time layer_norm, l2_normalize (and its gradient) and SparseProj instead of the step")
     args = ap.parse_args()
-    if args.norm:
+    if args.single_pass:
+        run_single_pass(args)
+    elif args.norm:
         run_norm(args)
     elif args.impl == "reference":
         run_reference(args)
