@@ -366,6 +366,61 @@ void oracle_layer_norm(const double *x, const double *g, const double *b, double
 }
 
 /*
+ * Gradient of layer_norm with respect to x, g and b, for the gradient dy of its output
+ * (training through the layernorm of the README's "blocksparse.norms" section; the page gives
+ * the forward signature only).  Readings, besides those of the forward pass above:
+ *   - with relu the gradient passes where the forward output y is positive and is zero where
+ *     y <= 0 (the relu derivative at 0 taken as 0); y is the forward result the caller holds,
+ *     so the mask is the one its forward pass produced (y is not read without relu);
+ *   - the derivative is that of the forward formula, mean and variance included:
+ *       xh = (x - mean_n) / sd_n,  dz = dy (masked),  a = g * dz
+ *       db[f] = sum_n dz[n][f],  dg[f] = sum_n dz[n][f] * xh[n][f]
+ *       dx[n][f] = (a[n][f] - mean_f' a[n][f'] - xh[n][f] * mean_f' a[n][f'] * xh[n][f']) / sd_n
+ * Statistics as in the forward pass (mean, then the variance of the deviations), float64,
+ * features and samples in increasing order.
+ */
+void oracle_layer_norm_grad(const double *x, const double *y, const double *g, const double *dy,
+                            double *dx, double *dg, double *db, int N, int C, int axis, double epsilon,
+                            int relu)
+{
+    for (int64_t f = 0; f < C; ++f) {
+        dg[f] = 0.0;
+        db[f] = 0.0;
+    }
+    for (int64_t n = 0; n < N; ++n) {
+        double s = 0.0;
+        for (int64_t f = 0; f < C; ++f)
+            s += act(x, n, f, N, C, axis);
+        const double mean = s / (double)C;
+        double v = 0.0;
+        for (int64_t f = 0; f < C; ++f) {
+            const double d = act(x, n, f, N, C, axis) - mean;
+            v += d * d;
+        }
+        const double sd = sqrt(v / (double)C + epsilon);
+        double sa = 0.0, sax = 0.0;
+        for (int64_t f = 0; f < C; ++f) {
+            const double xh = (act(x, n, f, N, C, axis) - mean) / sd;
+            double dz = act(dy, n, f, N, C, axis);
+            if (relu && !(act(y, n, f, N, C, axis) > 0.0))
+                dz = 0.0;
+            db[f] += dz;
+            dg[f] += dz * xh;
+            sa += g[f] * dz;
+            sax += g[f] * dz * xh;
+        }
+        const double ma = sa / (double)C, max_ = sax / (double)C;
+        for (int64_t f = 0; f < C; ++f) {
+            const double xh = (act(x, n, f, N, C, axis) - mean) / sd;
+            double dz = act(dy, n, f, N, C, axis);
+            if (relu && !(act(y, n, f, N, C, axis) > 0.0))
+                dz = 0.0;
+            *act_ptr(dx, n, f, N, C, axis) = (g[f] * dz - ma - xh * max_) / sd;
+        }
+    }
+}
+
+/*
  * l2_normalize(W, gain=None, epsilon=1e-6, dtype)  [blocksparse README, section "API
  * Documentation: blocksparse.matmul": a BlocksparseMatMul method for weight normalisation].
  * The page gives the signature only; the readings taken:

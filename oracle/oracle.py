@@ -60,6 +60,7 @@ def _load():
         lib.oracle_bprop_at.argtypes = [_u8, _c, _c, _c, _d, _d, _c, _c, _i64, _i64, _l, _d]
         lib.oracle_updat_at.argtypes = [_u8, _c, _c, _c, _d, _d, _c, _c, _i64, _i64, _i64, _l, _d]
         lib.oracle_layer_norm.argtypes = [_d, _d, _d, _d, _c, _c, _c, ctypes.c_double, _c]
+        lib.oracle_layer_norm_grad.argtypes = [_d, _d, _d, _d, _d, _d, _d, _c, _c, _c, ctypes.c_double, _c]
         lib.oracle_l2_normalize.argtypes = [_u8, _c, _c, _c, _d, _d, ctypes.c_double, _d]
         lib.oracle_l2_normalize_grad.argtypes = [_u8, _c, _c, _c, _d, _d, ctypes.c_double, _d, _d, _d]
         lib.oracle_proj_default_lut.argtypes = [_c, _c, _c, _i32]
@@ -238,6 +239,23 @@ def layer_norm(x, g, b, axis: int = 1, epsilon: float = 1e-6, relu: bool = False
     y = np.empty_like(x)
     _load().oracle_layer_norm(_p(x, _d), _p(g, _d), _p(b, _d), _p(y, _d), N, C, axis, float(epsilon), int(relu))
     return y
+
+
+def layer_norm_grad(x, g, dy, y=None, axis: int = 1, epsilon: float = 1e-6, relu: bool = False):
+    """Gradient of layer_norm with respect to (x, g, b) for the output gradient dy; with relu the
+    mask is y > 0 for the forward output y (readings in the C source).  Returns (dx, dg, db)."""
+    x, g, dy = _f64(x), _f64(g).reshape(-1), _f64(dy)
+    assert x.ndim == 2 and axis in (0, 1) and dy.shape == x.shape
+    C = x.shape[1] if axis == 1 else x.shape[0]
+    N = x.shape[0] if axis == 1 else x.shape[1]
+    assert g.size == C
+    yv = _f64(y) if relu else np.zeros_like(x)
+    assert yv.shape == x.shape
+    dx = np.empty_like(x)
+    dg, db = np.empty(C), np.empty(C)
+    _load().oracle_layer_norm_grad(_p(x, _d), _p(yv, _d), _p(g, _d), _p(dy, _d), _p(dx, _d), _p(dg, _d),
+                                   _p(db, _d), N, C, axis, float(epsilon), int(relu))
+    return dx, dg, db
 
 
 def _gain(gain, S: int, bs: int):

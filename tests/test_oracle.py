@@ -343,6 +343,78 @@ def test_layer_norm_matches_numpy_definition():
     assert np.allclose(o.layer_norm(x, g, b, axis=1, epsilon=eps), want, rtol=1e-12, atol=1e-12)
 
 
+# ---- layer_norm gradient: pinned to the (pinned) forward pass by finite differences ----------
+
+def _ln_loss(x, g, b, dy, axis, eps, relu):
+    return float((dy * o.layer_norm(x, g, b, axis=axis, epsilon=eps, relu=relu)).sum())
+
+
+@pytest.mark.parametrize("axis", [1, 0])
+@pytest.mark.parametrize("relu", [False, True])
+def test_layer_norm_grad_finite_differences(axis, relu):
+    """dx, dg and db against central differences of sum(dy * layer_norm(x, g, b)); with relu the
+    inputs keep every pre-activation at least 1e-3 from zero, so the mask is locally constant."""
+    N, C, eps = 5, 11, 1e-3
+    x, g, b = _ln_inputs(N, C, 21)
+    if axis == 0:
+        x = x.T.copy()
+    dy = np.random.default_rng(22).standard_normal(x.shape)
+    y = o.layer_norm(x, g, b, axis=axis, epsilon=eps, relu=relu)
+    if relu:
+        z = o.layer_norm(x, g, b, axis=axis, epsilon=eps)
+        assert np.abs(z).min() > 1e-3 and (z < 0).any() and (z > 0).any()
+    dx, dg, db = o.layer_norm_grad(x, g, dy, y=y, axis=axis, epsilon=eps, relu=relu)
+    h = 1e-6
+    for idx in np.ndindex(*x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd = (_ln_loss(xp, g, b, dy, axis, eps, relu) - _ln_loss(xm, g, b, dy, axis, eps, relu)) / (2 * h)
+        assert abs(fd - dx[idx]) <= 1e-6 * max(1.0, abs(fd)), (idx, fd, dx[idx])
+    for f in range(C):
+        for v, grad in ((g, dg), (b, db)):
+            vp, vm = v.copy(), v.copy()
+            vp[f] += h
+            vm[f] -= h
+            args_p = (vp, b) if v is g else (g, vp)
+            args_m = (vm, b) if v is g else (g, vm)
+            fd = (_ln_loss(x, *args_p, dy, axis, eps, relu) - _ln_loss(x, *args_m, dy, axis, eps, relu)) / (2 * h)
+            assert abs(fd - grad[f]) <= 1e-6 * max(1.0, abs(fd)), (f, fd, grad[f])
+
+
+def test_layer_norm_grad_invariances():
+    """The output ignores a shift of a sample, and (epsilon = 0) a scaling of it, so every row
+    of dx sums to zero and is orthogonal to the centred sample; without relu db is the plain sum
+    of dy over samples."""
+    x, g, b = _ln_inputs(7, 29, 23)
+    dy = np.random.default_rng(24).standard_normal(x.shape)
+    dx, dg, db = o.layer_norm_grad(x, g, dy, axis=1, epsilon=0.0)
+    assert np.allclose(dx.sum(axis=1), 0.0, atol=1e-12)
+    xc = x - x.mean(axis=1, keepdims=True)
+    assert np.allclose((dx * xc).sum(axis=1), 0.0, atol=1e-11)
+    assert np.allclose(db, dy.sum(axis=0), rtol=1e-14, atol=1e-14)
+    xh = xc / np.sqrt((xc * xc).mean(axis=1, keepdims=True))
+    assert np.allclose(dg, (dy * xh).sum(axis=0), rtol=1e-12, atol=1e-12)
+
+
+def test_layer_norm_grad_relu_mask_zeroes_and_layouts_agree():
+    """Where the forward output is 0 the gradient does not pass: dy there changes nothing; the
+    (C, N) layout gives the transposed result of the (N, C) one."""
+    x, g, b = _ln_inputs(6, 17, 25)
+    y = o.layer_norm(x, g, b, axis=1, epsilon=1e-6, relu=True)
+    assert (y == 0).any()
+    dy = np.random.default_rng(26).standard_normal(x.shape)
+    dy2 = np.where(y > 0, dy, 100.0)
+    r1 = o.layer_norm_grad(x, g, dy, y=y, axis=1, relu=True)
+    r2 = o.layer_norm_grad(x, g, dy2, y=y, axis=1, relu=True)
+    for a, c in zip(r1, r2):
+        assert np.array_equal(a, c)
+    r0 = o.layer_norm_grad(x.T.copy(), g, dy.T.copy(), y=y.T.copy(), axis=0, relu=True)
+    assert np.allclose(r0[0], r1[0].T, rtol=1e-13, atol=1e-13)
+    assert np.allclose(r0[1], r1[1], rtol=1e-13, atol=1e-13)
+    assert np.allclose(r0[2], r1[2], rtol=1e-13, atol=1e-13)
+
+
 # --- l2_normalize (README, "API Documentation: blocksparse.matmul": weight normalisation) ---
 
 def _wn_inputs(R, S, bs, p, seed, scale=1.0):
