@@ -458,6 +458,33 @@ def config_passes(wl, nnz):
     return out
 
 
+def cold_times(fn, flush, reps):
+    """Device microseconds of fn() launched alone, cold, reps times: each launch follows a 256 MB
+    read-only sweep that evicts the L2, and every sweep, event and launch is queued behind one
+    device sleep that outlasts the host's enqueue time, so the start event fires when the sweep
+    ends with the launch already queued (host latency is not counted).  Median over reps."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(5):
+        flush.sum()
+        fn()
+    host_s = (time.perf_counter() - t0) / 5
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(host_s * 1.5 * reps * 2.1e9) + 200000)     # cycles at <= 2.1 GHz
+    evs = []
+    for _ in range(reps):
+        flush.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs) * 1000.0
+
+
 def run_configs(dev, peaks, reps):
     """Each benchmark configuration on its own: every pass timed alone with CUDA events, cold
     (a 256 MB read-only sweep evicts the L2 before each timed launch), median over reps."""
@@ -479,19 +506,7 @@ def run_configs(dev, peaks, reps):
             calls["updat_grouped_g%d" % wl.group] = lambda: m.updat_grouped(xs, dys, dw=dw, accumulate=True)
         res = {}
         for pname, flops, byts in config_passes(wl, m.nnz):
-            fn = calls[pname]
-            for _ in range(3):
-                fn()
-            evs = []
-            for _ in range(reps):
-                flush.sum()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                fn()
-                b.record()
-                evs.append((a, b))
-            torch.cuda.synchronize()
-            us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1000.0
+            us = cold_times(calls[pname], flush, reps)
             if wl.dtype == "f32":
                 t_c, bound_c = flops / (FFMA_TFLOPS * 1e12), "alu"
             else:
@@ -509,7 +524,8 @@ def run_configs(dev, peaks, reps):
         del x, w, dy, y, dx, dw
     del flush
     out["_timing"] = ("each pass alone between CUDA events on the launching stream, median of %d, after a "
-                      "256 MB read-only sweep that evicts L2; peaks: %s" % (
+                      "256 MB read-only sweep that evicts L2, queued behind a device sleep so host enqueue "
+                      "time is not counted; peaks: %s" % (
                           reps, "tensor = MEASURED_PEAKS bf16_tflops (fp16 the same rate), hbm = hbm_gbs, "
                           "alu = derived fp32 FFMA peak %.1f TFLOP/s" % FFMA_TFLOPS))
     return out
@@ -539,17 +555,8 @@ def run_single_pass(args):
     flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
     for _ in range(max(1, args.warmup)):
         fn()
-    evs = []
-    for _ in range(args.steps):
-        flush.sum()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        evs.append((a, b))
-    torch.cuda.synchronize()
+    us = cold_times(fn, flush, args.steps)
     m.sync_status()
-    us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1000.0
     print(json.dumps({"pass": args.single_pass, "us": round(us, 3), "steps": args.steps, "nnz": m.nnz}), flush=True)
 
 
@@ -652,7 +659,8 @@ def run_norm(args):
     """The normalisations and projections around the step, each on its own.
     layer_norm (README "blocksparse.norms") on the step's activation shape, N = 1024 samples of
     C = 4096 bf16 features, in both layouts; 16 rotating input/output sets (256 MB > L2).  Bytes
-    per launch = read x + write y + g, b.
+    per launch = read x + write y + g, b; its gradient (with relu) reads x, y, dy and writes dx
+    (+ g, dg, db); one launch there is the partial-sum kernel and the reduction kernel.
     l2_normalize (README "blocksparse.matmul", weight normalisation) of the step's float32 weight
     (hidden 4096, block 32, 50% dense) to bf16, and its gradient (bf16 dy -> float32 dw, dgain);
     8 rotating sets (> L2).  Bytes per launch: read w (+ dy) + write y (or dw) + gain (+ dgain).
@@ -678,7 +686,15 @@ def run_norm(args):
         us = _time_launches(lambda i: bsmm.layer_norm(xs[i % sets], g, b, axis=axis, y=ys[i % sets]),
                             args.steps, args.warmup)
         out["layer_norm_axis%d" % axis] = entry(us, 2 * N * C * 2 + 2 * C * 4)
-        del xs, ys
+        # gradient with relu: read x, y, dy, write dx (bf16), read g, write dg, db; the workspace of
+        # per-CTA partial sums is written and read back on top (not counted)
+        dys = [wk.normals(shape, 600 + i, 1.0, "bf16").to(dev) for i in range(sets)]
+        dxs = [torch.empty_like(x) for x in xs]
+        us = _time_launches(lambda i: bsmm.layer_norm_grad(xs[i % sets], g, dys[i % sets], y=ys[i % sets],
+                                                           axis=axis, relu=True, dx=dxs[i % sets]),
+                            args.steps, args.warmup)
+        out["layer_norm_grad_axis%d" % axis] = entry(us, 4 * N * C * 2 + 3 * C * 4)
+        del xs, ys, dys, dxs
 
     wl = wk.CONFIGS["h4096_b32_p50_n1024"]
     lay = wk.make_layout(wl.R, wl.S, wl.layout_kind, wl.density, wl.force_diag, 1000 * wl.seed_ns)
@@ -717,7 +733,7 @@ def run_norm(args):
     print(json.dumps({"metric": "normalisation and projection GB/s (algorithmic bytes) on 1 GB300",
                       "unit": "GB/s",
                       "value": round(min(v["gbs"] for v in out.values()), 1), "dtype": "bf16",
-                      "config": {"workload": "layer_norm: N=1024 x C=4096 bf16, 16 rotating sets; "
+                      "config": {"workload": "layer_norm and its gradient: N=1024 x C=4096 bf16, 16 rotating sets; "
                                              "l2_normalize: hidden 4096, block 32, 50%% dense, %d blocks, "
                                              "float32 w -> bf16, 8 rotating sets; SparseProj: N=1024 x "
                                              "4096 -> 2048 features (runs of 32 every 64), bf16, 16 rotating "

@@ -60,6 +60,8 @@ def lib():
             "bsmm_selftest_wait_timeout": [vp, ctypes.c_uint64, vp],
             "bsmm_updat_noalloc": [vp, vp, vp, vp, i, i, i, vp],
             "bsmm_layer_norm": [vp, vp, vp, vp, i, i, i, ctypes.c_float, i, i, vp],
+            "bsmm_layer_norm_grad": [vp, vp, vp, vp, vp, vp, vp, i, i, i, ctypes.c_float, i, i, vp,
+                                     ctypes.c_size_t, vp],
             "bsmm_l2_normalize": [vp, vp, vp, vp, ctypes.c_float, i, vp],
             "bsmm_l2_normalize_grad": [vp, vp, vp, vp, vp, vp, ctypes.c_float, i, vp],
             "bsmm_proj_create": [ctypes.POINTER(vp), i, i, i, i, pi32],
@@ -74,6 +76,8 @@ def lib():
             f.restype = ctypes.c_int
         L.bsmm_status_string.argtypes = [ctypes.c_int]
         L.bsmm_status_string.restype = ctypes.c_char_p
+        L.bsmm_layer_norm_grad_workspace.argtypes = [i, i, i]
+        L.bsmm_layer_norm_grad_workspace.restype = ctypes.c_size_t
         L.bsmm_launch_count.argtypes = []
         L.bsmm_launch_count.restype = ctypes.c_int64
         _lib = L
@@ -431,6 +435,48 @@ def layer_norm(x, g, b, axis: int = 1, epsilon: float = 1e-6, relu: bool = False
     _want(y, "y", x.shape, x.dtype, x.device)
     bsmm_layer_norm(x, g, b, y, N, C, axis, epsilon, relu, stream)
     return y
+
+
+def bsmm_layer_norm_grad(x, y, g, dy, dx, dg, db, N: int, C: int, axis: int, epsilon: float, relu: bool,
+                         workspace, stream=None):
+    _check(lib().bsmm_layer_norm_grad(_ptr(x), _ptr(y) if y is not None else None, _ptr(g), _ptr(dy), _ptr(dx),
+                                      _ptr(dg), _ptr(db), N, C, axis, float(epsilon), int(relu), _DT[x.dtype],
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(stream)), "bsmm_layer_norm_grad")
+
+
+def layer_norm_grad(x, g, dy, y=None, axis: int = 1, epsilon: float = 1e-6, relu: bool = False, dx=None,
+                    stream=None):
+    """Gradient of layer_norm(x, g, b, axis, epsilon, relu) for the output gradient dy: returns
+    (dx, dg, db), dx in x's dtype, dg and db float32 vectors of C values.  With relu the forward
+    output y is needed (the gradient passes where y > 0).  dx must not share memory with x, y or
+    dy (they are read again after dx is written)."""
+    for t, what in ((x, "x"), (g, "g"), (dy, "dy")):
+        _dev(t, what)
+    if x.dim() != 2 or axis not in (0, 1):
+        raise ValueError("x must be 2-D and axis 0 or 1")
+    C = x.shape[1] if axis == 1 else x.shape[0]
+    N = x.shape[0] if axis == 1 else x.shape[1]
+    if g.dtype != torch.float32 or g.numel() != C or g.device != x.device:
+        raise ValueError("g must be float32 with C = %d values on %s" % (C, x.device))
+    _want(dy, "dy", x.shape, x.dtype, x.device)
+    if relu:
+        if y is None:
+            raise ValueError("relu needs the forward output y")
+        _want(y, "y", x.shape, x.dtype, x.device)
+    else:
+        y = None
+    if dx is None:
+        dx = torch.empty_like(x)
+    _want(dx, "dx", x.shape, x.dtype, x.device)
+    if any(t is not None and t.data_ptr() == dx.data_ptr() for t in (x, y, dy)) and dx.numel() > 0:
+        raise ValueError("dx must not share memory with x, y or dy")
+    dg = torch.empty(C, dtype=torch.float32, device=x.device)
+    db = torch.empty(C, dtype=torch.float32, device=x.device)
+    nbytes = int(lib().bsmm_layer_norm_grad_workspace(N, C, axis))
+    ws = torch.empty(max(16, nbytes), dtype=torch.uint8, device=x.device)
+    bsmm_layer_norm_grad(x, y, g, dy, dx, dg, db, N, C, axis, epsilon, relu, ws, stream)
+    return dx, dg, db
 
 
 # ---- SparseProj -------------------------------------------------------------------------

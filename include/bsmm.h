@@ -42,6 +42,7 @@
 #ifndef BSMM_H
 #define BSMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -187,6 +188,31 @@ bsmm_status bsmm_updat_noalloc(bsmm_t h, const void *x, const void *dy, float *d
  */
 bsmm_status bsmm_layer_norm(const void *x, const float *g, const float *b, void *y, int N, int C, int axis,
                             float epsilon, int relu, bsmm_dtype t, void *stream);
+
+/*
+ * Gradient of bsmm_layer_norm with respect to x, g and b (training through the layernorm of
+ * README section "blocksparse.norms"), for the gradient dy of its output.  With mean_n, rstd_n
+ * the statistics of sample n (recomputed from x as in the forward pass), xh = (x - mean_n) * rstd_n,
+ * dz = dy, or with relu dy where the forward output y > 0 and 0 elsewhere, and a = g * dz:
+ *   dx[n][f] = rstd_n * (a[n][f] - mean_f a[n][.] - xh[n][f] * mean_f (a * xh)[n][.])
+ *   dg[f] = sum_n dz[n][f] * xh[n][f],   db[f] = sum_n dz[n][f]
+ * x, y, dy, dx: DEVICE pointers of dtype t in the layout of bsmm_layer_norm (y, the forward
+ * output, is read only with relu and may be NULL without); g: DEVICE C float32; dg, db: DEVICE
+ * C float32 outputs.  Arithmetic in float32, dx rounded once to t; dg and db are sums of
+ * per-CTA float32 partials added in a fixed order (deterministic).  workspace: DEVICE scratch
+ * of at least bsmm_layer_norm_grad_workspace(N, C, axis) bytes, 16-byte aligned, owned by the
+ * caller and free again when the stream reaches the end of the call.  The outputs must not
+ * overlap the inputs (x, y and dy are read again after dx is written).  N = 0 sets dg = db = 0
+ * and reads nothing else.  Two or three kernels are enqueued on `stream` (dx and per-chunk
+ * partial sums, then their reduction).
+ * Errors: INVALID (null pointers, dg == db, dx equal to x, y or dy, N < 0, C < 1, axis not 0/1,
+ * epsilon negative or NaN, workspace too small), ALIGN (as bsmm_layer_norm, for x, y, dy, dx, g, dg, db, workspace),
+ * UNSUPPORTED (axis = 1 with C > 16384, axis = 0 with C > 327680), CUDA.
+ */
+size_t bsmm_layer_norm_grad_workspace(int N, int C, int axis);
+bsmm_status bsmm_layer_norm_grad(const void *x, const void *y, const float *g, const void *dy, void *dx,
+                                 float *dg, float *db, int N, int C, int axis, float epsilon, int relu,
+                                 bsmm_dtype t, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * l2_normalize(W, gain=None, epsilon=1e-6, dtype) [README, "API Documentation: blocksparse.matmul":

@@ -91,6 +91,44 @@ def test_layer_norm_rejects_bad_arguments_on_host():
     assert L.bsmm_layer_norm(A, A, A, B, 4, 16392, 1, 1e-6, 0, 2, None) == bsmm.ERR_UNSUPPORTED
 
 
+def test_layer_norm_grad_rejects_bad_arguments_on_host():
+    """Every case fails validation before anything is enqueued (the pointers are never used)."""
+    L = bsmm.lib()
+    A, B, D, W = 0x10000, 0x20000, 0x30000, 0x40000   # 16-byte aligned stand-ins, never dereferenced
+    ws = L.bsmm_layer_norm_grad_workspace(4, 8, 1)
+    assert ws == (8 + 1 * 2 * 8) * 4                     # 2N statistics + one chunk of 2C partials
+    assert L.bsmm_layer_norm_grad_workspace(1000, 64, 1) == (2000 + 125 * 2 * 64) * 4   # 8-sample chunks
+    assert L.bsmm_layer_norm_grad_workspace(8000, 64, 1) == (16000 + 500 * 2 * 64) * 4  # at most 512 chunks
+    assert L.bsmm_layer_norm_grad_workspace(1000, 64, 0) == 32 * 2 * 64 * 4             # 32-sample tiles
+    assert L.bsmm_layer_norm_grad_workspace(-1, 8, 1) == 0
+
+    def call(x=A, y=None, g=A, dy=A, dx=B, dg=D, db=D + 0x1000, N=4, C=8, axis=1, eps=1e-6, relu=0, t=2,
+             w=W, wb=ws):
+        return L.bsmm_layer_norm_grad(x, y, g, dy, dx, dg, db, N, C, axis, eps, relu, t, w, wb, None)
+    assert call(x=None) == bsmm.ERR_INVALID
+    assert call(dx=A) == bsmm.ERR_INVALID                   # dx over x (and dy)
+    assert call(relu=1, y=B) == bsmm.ERR_INVALID            # dx over y
+    assert call(relu=1) == bsmm.ERR_INVALID                 # relu needs y
+    assert call(dg=None) == bsmm.ERR_INVALID
+    assert call(db=D) == bsmm.ERR_INVALID                   # dg == db
+    assert call(w=None) == bsmm.ERR_INVALID
+    assert call(wb=ws - 4) == bsmm.ERR_INVALID              # workspace too small
+    assert call(N=-1) == bsmm.ERR_INVALID
+    assert call(C=0) == bsmm.ERR_INVALID
+    assert call(axis=2) == bsmm.ERR_INVALID
+    assert call(eps=-1.0) == bsmm.ERR_INVALID
+    assert call(eps=float("nan")) == bsmm.ERR_INVALID
+    assert call(t=7) == bsmm.ERR_INVALID
+    assert call(x=A + 8) == bsmm.ERR_ALIGN
+    assert call(dx=B + 2) == bsmm.ERR_ALIGN
+    assert call(relu=1, y=A + 4) == bsmm.ERR_ALIGN
+    assert call(w=W + 4) == bsmm.ERR_ALIGN
+    assert call(dg=D + 4) == bsmm.ERR_ALIGN
+    assert call(C=12, wb=1 << 20) == bsmm.ERR_ALIGN          # C * 2 % 16
+    assert call(N=12, axis=0, wb=1 << 20) == bsmm.ERR_ALIGN  # N * 2 % 16
+    assert call(C=16392, wb=1 << 30) == bsmm.ERR_UNSUPPORTED
+
+
 def test_l2_normalize_rejects_null_handle_on_host():
     L = bsmm.lib()
     A = 0x10000

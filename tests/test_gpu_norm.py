@@ -77,3 +77,84 @@ def test_layer_norm_limits():
     g2 = torch.zeros(C + 8, device="cuda")
     with pytest.raises(bsmm.BsmmError):
         bsmm.layer_norm(x2, g2, g2)
+
+
+# ---- gradient --------------------------------------------------------------------------------
+# dx: one float32 evaluation rounded once to the input type; dg, db: float32 sums over samples
+GTOL = {"f32": 2e-5, "f16": 2e-3, "bf16": 8e-3}
+SUMTOL = 1e-4
+
+
+def _grad_case(N, C, axis, dtype, seed, relu, eps):
+    x, g, b = _case(N, C, axis, dtype, seed)
+    dy = wk.normals(x.shape, seed + 7, 1.0, dtype)
+    y = bsmm.layer_norm(x.cuda(), g.cuda(), b.cuda(), axis=axis, epsilon=eps, relu=relu) if relu else None
+    return x, g, dy, y
+
+
+@pytest.mark.parametrize("axis", [1, 0])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("relu", [False, True])
+@pytest.mark.parametrize("N,C", [(200, 4096), (72, 256), (136, 8192), (8, 4104), (1304, 24), (400, 1000)])
+def test_layer_norm_grad_parity(axis, dtype, relu, N, C):
+    eps = 1e-6 if dtype != "f16" else 1e-5
+    x, g, dy, y = _grad_case(N, C, axis, dtype, 17 * N + C + axis, relu, eps)
+    dx = torch.full(x.shape, float("nan"), dtype=DT[dtype], device="cuda")
+    dx, dg, db = bsmm.layer_norm_grad(x.cuda(), g.cuda(), dy.cuda(), y=y, axis=axis, epsilon=eps, relu=relu,
+                                      dx=dx)
+    torch.cuda.synchronize()
+    rdx, rdg, rdb = o.layer_norm_grad(x, g, dy, y=cpu64(y) if relu else None, axis=axis, epsilon=eps, relu=relu)
+    assert rel_fro(cpu64(dx), rdx) <= GTOL[dtype]
+    assert rel_fro(cpu64(dg), rdg) <= SUMTOL
+    assert rel_fro(cpu64(db), rdb) <= SUMTOL
+
+
+@pytest.mark.parametrize("axis", [1, 0])
+def test_layer_norm_grad_large(axis):
+    """The largest supported rows (C = 16384 for axis 1, with more samples than chunks of 8; a
+    (C, N) slice that no longer fits shared memory for axis 0)."""
+    N, C = (4100, 16384) if axis == 1 else (64, 12288)
+    x, g, dy, y = _grad_case(N, C, axis, "bf16", 3 + axis, True, 1e-6)
+    dx, dg, db = bsmm.layer_norm_grad(x.cuda(), g.cuda(), dy.cuda(), y=y, axis=axis, relu=True)
+    torch.cuda.synchronize()
+    rdx, rdg, rdb = o.layer_norm_grad(x, g, dy, y=cpu64(y), axis=axis, relu=True)
+    assert rel_fro(cpu64(dx), rdx) <= GTOL["bf16"]
+    assert rel_fro(cpu64(dg), rdg) <= SUMTOL
+    assert rel_fro(cpu64(db), rdb) <= SUMTOL
+
+
+@pytest.mark.parametrize("axis", [1, 0])
+def test_layer_norm_grad_small_integers_exact_db(axis):
+    """Constant g = 1, dy in {-1, 0, 1} and x whose samples have mean 0 and variance 1 exactly:
+    db is a sum of small integers, exact in float32 in any order."""
+    N, C = 96, 64
+    rng = np.random.default_rng(5)
+    base = np.tile(np.array([-1.0, 1.0]), C // 2)              # mean 0, biased variance 1
+    xs = np.stack([rng.permutation(base) for _ in range(N)])    # (N, C)
+    x = torch.from_numpy(xs.astype(np.float32)).to(torch.bfloat16)
+    dy = wk.small_ints((N, C), 6, "bf16")
+    if axis == 0:
+        x, dy = x.T.contiguous(), dy.T.contiguous()
+    g = torch.ones(C)
+    dx, dg, db = bsmm.layer_norm_grad(x.cuda(), g.cuda(), dy.cuda(), axis=axis, epsilon=0.0)
+    rdx, rdg, rdb = o.layer_norm_grad(x, g, dy, axis=axis, epsilon=0.0)
+    assert np.array_equal(cpu64(db), rdb)
+    assert rel_fro(cpu64(dg), rdg) <= 1e-6
+    assert rel_fro(cpu64(dx), rdx) <= GTOL["bf16"]
+
+
+@pytest.mark.parametrize("axis", [1, 0])
+def test_layer_norm_grad_empty_minibatch(axis):
+    C = 256
+    x = torch.empty((0, C) if axis == 1 else (C, 0), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(C, device="cuda")
+    dx, dg, db = bsmm.layer_norm_grad(x, g, torch.empty_like(x), axis=axis)
+    torch.cuda.synchronize()
+    assert dx.numel() == 0 and torch.equal(dg, torch.zeros(C, device="cuda")) and torch.equal(db, dg)
+
+
+def test_layer_norm_grad_refuses_dx_over_an_input():
+    x, g, dy, _ = _grad_case(16, 256, 1, "bf16", 8, False, 1e-6)
+    xc, dyc = x.cuda(), dy.cuda()
+    with pytest.raises(ValueError):
+        bsmm.layer_norm_grad(xc, g.cuda(), dyc, dx=dyc)
