@@ -23,8 +23,10 @@
 // parallel: warp q owns the output slots s with s % 4 == q, so every accumulator still receives
 // its MMAs from one thread in schedule order (deterministic sums).  Per chunk each MMA warp reads
 // a ready-made list of at most 8 words (accumulator column, panel, block, accumulate flag) with
-// two vector loads and issues from registers, predicated, without branches.  The producers
-// likewise read a chunk's schedule words into registers before issuing its copies.
+// two vector loads and issues from registers, predicated, without branches.  The loaders
+// likewise read a chunk's schedule words into registers before issuing its copies; two loader
+// warps share each chunk (panels 0-3 and blocks 0-15, panels 4-7 and blocks 16-31), which halves
+// the time to issue a stage's copies, the limit on how fast stages refill.
 //
 // Loads.  Weight blocks are gathered with cp.async, 16 bytes per lane, straight into the canonical
 // no-swizzle operand layout: one warp instruction moves one 512-byte block, about 50 bytes per
@@ -56,9 +58,11 @@ using namespace tc;
 
 namespace {
 
-constexpr int kSpProducers = 4;                 // warps 0-3 load
-constexpr int kSpMmaWarps = 4;                  // warps 4-7 issue MMAs (warp 4 allocates tensor memory)
-constexpr int kSpThreads = 32 * (kSpProducers + kSpMmaWarps);   // all eight store the outputs
+constexpr int kSpProducers = 4;                 // chunk c is loaded by producer slot c % 4 ...
+constexpr int kSpLoaders = 2 * kSpProducers;    // ... whose two warps s and s + 4 (warps 0-7) split it
+constexpr int kSpMmaWarps = 4;                  // warps 8-11 issue MMAs (warp 8 allocates tensor memory)
+constexpr int kSpThreads = 32 * (kSpLoaders + kSpMmaWarps);     // all twelve store the outputs
+constexpr int kSpEpiGroups = kSpThreads / 128;  // warp groups sharing the epilogue
 constexpr int kSpMaxStages = 16;
 constexpr int kSpSchedWords = 6144;             // per-unit schedule budget (24 KB)
 constexpr int kSpSmemBudget = 226 * 1024;       // dynamic shared memory limit of one CTA
@@ -163,14 +167,14 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
     if (threadIdx.x == 0) {
         aborted = 0;
         for (int i = 0; i < g.stages; ++i) {
-            mbar_init(&full[i], 1 + 32);        // the loading warp's lane 0 + 32 cp.async arrivals
+            mbar_init(&full[i], 1 + 64);        // the first loading warp's lane 0 + 2 x 32 cp.async arrivals
             mbar_init(&empty[i], kSpMmaWarps);  // one commit per MMA warp
         }
         mbar_init(&acc_full, kSpMmaWarps);
         mbar_init(&sched_full, 1);
         fence_barrier_init();
     }
-    if (warp == kSpProducers) tmem_alloc(&tmem_base, 512);
+    if (warp == kSpLoaders) tmem_alloc(&tmem_base, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -191,8 +195,10 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
     const uint16_t *act = static_cast<const uint16_t *>(p.act);
     const uint16_t *wts = static_cast<const uint16_t *>(p.w);
 
-    if (warp < kSpProducers) {
-        // ---------------- loads: warp w fills chunks w, w+4, ...; chunk c uses stage c % stages ----
+    if (warp < kSpLoaders) {
+        // ---------------- loads: warps s and s + 4 fill chunks s, s+4, ...; chunk c uses stage
+        // c % stages; warp s loads panels 0-3 and blocks 0-15 of the chunk, warp s + 4 the rest ----
+        const int slot = warp % kSpProducers, sub = warp / kSpProducers;
         // Lane-constant offsets of this lane's 16-byte chunks of a weight block: fprop B[K = i][N = j]
         // (MN-major), bprop B[K = j][N = i] (K-major); for bs 8 the lane's 8 x 8 sub-block row.
         uint32_t w_dst[WCH], w_src[WCH];
@@ -215,7 +221,7 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
             if (hdr == 0) break;
             const int ne = (int)(hdr >> 16), nr = (int)(hdr & 0xFFFFu);
             const int next = (pos + kSpChunkHead + ne + nr * RW + 3) & ~3;
-            if (chunk % kSpProducers != warp) {
+            if (chunk % kSpProducers != slot) {
                 pos = next;
                 continue;
             }
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
             if (lane == 0) {
                 if (chunk >= g.stages && !mbar_wait(&empty[st], ((chunk / g.stages) - 1) & 1, p.status))
                     aborted = 1;
-                else
+                else if (sub == 0)
                     mbar_arrive(&full[st]);
             }
             __syncwarp();
@@ -232,17 +238,19 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
             // the chunk's schedule words into registers first, so no copy waits on a load
             const uint32_t *ent = sched + pos + kSpChunkHead;
             const uint32_t *rec = ent + ne;
-            uint32_t srcw[8], rw[32];
+            const int e0 = sub * 4, r0 = sub * 16;                  // this warp's panels and blocks
+            uint32_t srcw[4], rw[16];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) srcw[e] = e < ne ? ent[e] : 0u;
+            for (int e = 0; e < 4; ++e) srcw[e] = e0 + e < ne ? ent[e0 + e] : 0u;
 #pragma unroll
-            for (int r = 0; r < 32; ++r) rw[r] = r < nr ? rec[COARSE ? r * 4 + (lane >> 3) : r] : 0u;
+            for (int r = 0; r < 16; ++r) rw[r] = r0 + r < nr ? rec[COARSE ? (r0 + r) * 4 + (lane >> 3) : r0 + r] : 0u;
             bool bad = false;
             // activation panels: entry e into panel slot e
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
+            for (int ee = 0; ee < 4; ++ee) {
+                const int e = e0 + ee;
                 const uint32_t on = e < ne ? 1u : 0u;
-                uint32_t src = srcw[e] >> 8;
+                uint32_t src = srcw[ee] >> 8;
                 const bool sbad = on && src >= (uint32_t)p.Fsrc;
                 bad |= sbad;
                 src = sbad ? 0u : src;
@@ -268,10 +276,11 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
             }
             // weight blocks into record slots, rearranged into the operand layout
 #pragma unroll
-            for (int r = 0; r < 32; ++r) {
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = r0 + rr;
                 const uint32_t on = r < nr ? 1u : 0u;
                 uint8_t *dst = stage + g.b_off + r * BSLOT;
-                const uint32_t v = rw[r] & kIdMask;
+                const uint32_t v = rw[rr] & kIdMask;
                 if (!COARSE) {
                     const bool ok = v < nnz32;
                     bad |= on && !ok;
@@ -293,10 +302,10 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
         cp_async_wait_all();                                    // no copy outlives the CTA
         __syncwarp();
     } else {
-        // ---------------- MMA warps: warp 4 + q issues the MMAs of the slots s with s % 4 == q --------
+        // ---------------- MMA warps: warp 8 + q issues the MMAs of the slots s with s % 4 == q --------
         // List word: accumulate flag << 31 | block (record) index << 16 | panel (entry) << 12 |
         // accumulator column.
-        const int q = warp - kSpProducers;
+        const int q = warp - kSpLoaders;
         const uint32_t leader = lane == 0 ? 1u : 0u;
         const uint64_t desc0 = sdesc(smem_u32(smem), LBO, SBO, SW_NONE);
         const uint32_t dlo = (uint32_t)desc0, dhi = (uint32_t)(desc0 >> 32);
@@ -342,7 +351,7 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int n = n0 + row;
-    const int half = warp >> 2;
+    const int grp = warp >> 2;                                  // epilogue warp group, 0 .. kSpEpiGroups - 1
     const bool ok = mbar_wait_warp(&acc_full, 0, p.status, 256) && sched_ok;
     tc_fence_after();
     const uint32_t mask_own = sched[0], mask_other = sched[1];
@@ -365,10 +374,32 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
             for (int j = 0; j < BSE; ++j) v[j] = 0.f;
         }
     };
+    // (F, N) outputs go through a [BSE][128] tile per epilogue group in the idle stage memory
+    // (after the split reduction buffer), so that the group's 128 threads store whole 16-byte
+    // pieces of feature rows; without room for the tiles every thread stores its own 2-byte values.
+    const size_t red_bytes = split == 2 ? (size_t)((g.W + 1) / 2) * BSE * 128 * 4 : 0;
+    const bool staged = !FA && red_bytes + (size_t)kSpEpiGroups * BSE * 256 <= (size_t)g.stages * g.stage_bytes;
+    uint16_t *tile_s = reinterpret_cast<uint16_t *>(smem + red_bytes) + grp * (BSE * 128);
     auto store_slot = [&](int slot, const float (&v)[BSE]) {
         const int o = win * g.W + slot;
-        if (n >= p.N || o >= p.Fslots) return;
         const int f0 = o * BSE;
+        if (staged) {
+            // every thread of the group takes part (named barrier 1 + grp over its 128 threads)
+#pragma unroll
+            for (int j = 0; j < BSE; ++j) tile_s[j * 128 + row] = sp_cvt(v[j], p.bf16);
+            named_sync(1 + grp, 128);
+            const int t = (warp & 3) * 32 + lane;
+#pragma unroll
+            for (int c = t; c < BSE * 16; c += 128) {
+                const int fr = c >> 4, nn = n0 + (c & 15) * 8;
+                if (o < p.Fslots && f0 + fr < p.Fout && nn < p.N)
+                    *reinterpret_cast<uint4 *>(out + (size_t)(f0 + fr) * p.N + nn) =
+                        *reinterpret_cast<const uint4 *>(tile_s + fr * 128 + (c & 15) * 8);
+            }
+            named_sync(1 + grp, 128);                           // the tile may be written again
+            return;
+        }
+        if (n >= p.N || o >= p.Fslots) return;
         if (FA) {
             uint16_t *dst = out + (size_t)n * p.Fout + f0;
             if (f0 + BSE <= p.Fout) {
@@ -394,7 +425,7 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
     };
 
     if (split == 1) {
-        for (int s = half; s < g.W; s += 2) {
+        for (int s = grp; s < g.W; s += kSpEpiGroups) {
             float v[BSE];
             load_slot(s, ((mask_own >> s) & 1u) != 0, v);
             store_slot(s, v);
@@ -408,7 +439,7 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
         {
             const int peer = part ^ 1;
             const int lo = peer == 0 ? 0 : Wh, hi = peer == 0 ? Wh : g.W;
-            for (int s = lo + half; s < hi; s += 2) {
+            for (int s = lo + grp; s < hi; s += kSpEpiGroups) {
                 if (!((mask_own >> s) & 1u)) continue;          // the owner reads zeros for it
                 float v[BSE];
                 load_slot(s, true, v);
@@ -422,7 +453,7 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
         cluster_sync();                                         // every partial has landed
         {
             const int lo = part == 0 ? 0 : Wh, hi = part == 0 ? Wh : g.W;
-            for (int s = lo + half; s < hi; s += 2) {
+            for (int s = lo + grp; s < hi; s += kSpEpiGroups) {
                 float v[BSE], pv[BSE];
                 load_slot(s, ((mask_own >> s) & 1u) != 0, v);
                 const bool peer_has = ((mask_other >> s) & 1u) != 0;
@@ -446,7 +477,7 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kSpProducers) tmem_dealloc(tmem, 512);
+    if (warp == kSpLoaders) tmem_dealloc(tmem, 512);
 }
 
 // (F, N) activations -> contiguous panels: pan[tile][source][panel], each panel 128 rows x BSE
@@ -755,7 +786,10 @@ bool sp_plan(const bsmm_ctx *h, bool bwd, int ntiles, SpSched &out)
     const double panel = 128.0 * bse * 2, bslot = bse * bse * 2.0;
     const int sms = std::max(1, h->sm_count);
     const double dens = std::min(1.0, (double)h->nnz / ((double)h->R * h->S) * (h->bs == 8 ? 4.0 : 1.0));
-    const int E = bse == 32 ? 4 : 8;
+    // BSMM_SP_E / BSMM_SP_R pin the panels and blocks per stage (tuning and tests)
+    const char *ee = getenv("BSMM_SP_E"), *er = getenv("BSMM_SP_R");
+    const int E = ee ? std::max(1, std::min(8, atoi(ee))) : (bse == 32 ? 4 : 8);
+    const int r_pin = er ? std::max(1, std::min(32, atoi(er))) : 0;
     const double mma_clk = bse == 32 ? 80.0 : 39.0;
     const int Wmax = std::min(32, 512 / bse);
     struct Cand { double t; int W, split, R; };
@@ -769,7 +803,8 @@ bool sp_plan(const bsmm_ctx *h, bool bwd, int ntiles, SpSched &out)
         // records per chunk: 1.5x the expected blocks of E sources over the window, capped so that
         // four stages fit next to the largest schedule
         const int r_fit = (int)(((kSpSmemBudget - 1024 - kSpSchedWords * 4) / kSpProducers - E * panel) / bslot);
-        const int R = std::max(1, std::min({32, r_fit, std::max(8, (int)std::ceil(1.5 * E * W * dens) + 4)}));
+        const int R = r_pin ? std::min(r_pin, std::max(1, r_fit))
+                            : std::max(1, std::min({32, r_fit, std::max(8, (int)std::ceil(1.5 * E * W * dens) + 4)}));
         const int nwin = (Fslots + W - 1) / W;
         double worst = 0;
         for (int w = 0; w < nwin; ++w) {
