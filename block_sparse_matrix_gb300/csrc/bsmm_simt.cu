@@ -43,6 +43,9 @@ __device__ __forceinline__ void out_coord(int idx, int &n, int &j)
 }
 
 // BWD=false: fprop over the column LUT.  BWD=true: bprop over the row LUT.
+// The operands of entry e + 1 (weight block and input panel) are loaded into registers while
+// entry e is multiplied out of shared memory, so each entry costs one compute phase instead of a
+// memory round trip followed by it.
 template <typename T, int BS, int FA, bool BWD>
 __global__ void __launch_bounds__(kThreads)
 k_simt_fwd_bwd(const T *__restrict__ in, const T *__restrict__ w, T *__restrict__ out,
@@ -50,6 +53,8 @@ k_simt_fwd_bwd(const T *__restrict__ in, const T *__restrict__ w, T *__restrict_
                int N, int Fin, int Fout)
 {
     constexpr int OUT = kTN * BS / kThreads;
+    constexpr int NW = (BS * BS + kThreads - 1) / kThreads;   // weight elements per thread
+    constexpr int NA = kTN * BS / kThreads;                     // panel elements per thread
     __shared__ float sw[BS][BS + 1];
     __shared__ float sa[kTN][BS + 1];
     const int tid = threadIdx.x;
@@ -60,21 +65,43 @@ k_simt_fwd_bwd(const T *__restrict__ in, const T *__restrict__ w, T *__restrict_
     for (int r = 0; r < OUT; ++r) acc[r] = 0.f;
 
     const int e0 = ptr[blk], e1 = ptr[blk + 1];
-    for (int e = e0; e < e1; ++e) {
+    float rw[NW], ra[NA];
+    auto load = [&](int e) {
         int b, src;                     // weight block id, source block index of the input panel
         if (BWD) { b = e; src = ent[e]; }
         else     { b = ent[2 * e]; src = ent[2 * e + 1]; }
         const T *wb = w + (size_t)b * BS * BS;
-        for (int q = tid; q < BS * BS; q += kThreads) sw[q / BS][q % BS] = to_f<T>(wb[q]);
-        for (int q = tid; q < kTN * BS; q += kThreads) {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const int q = tid + k * kThreads;
+            rw[k] = q < BS * BS ? to_f<T>(wb[q]) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < NA; ++k) {
+            const int q = tid + k * kThreads;
             int n, i;
             if (FA) { n = q / BS; i = q % BS; }
             else    { i = q / kTN; n = q % kTN; }
-            float v = 0.f;
-            if (n0 + n < N) v = to_f<T>(in[aidx<FA>(n0 + n, (int64_t)src * BS + i, N, Fin)]);
-            sa[n][i] = v;
+            ra[k] = n0 + n < N ? to_f<T>(in[aidx<FA>(n0 + n, (int64_t)src * BS + i, N, Fin)]) : 0.f;
+        }
+    };
+    if (e0 < e1) load(e0);
+    for (int e = e0; e < e1; ++e) {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const int q = tid + k * kThreads;
+            if (q < BS * BS) sw[q / BS][q % BS] = rw[k];
+        }
+#pragma unroll
+        for (int k = 0; k < NA; ++k) {
+            const int q = tid + k * kThreads;
+            int n, i;
+            if (FA) { n = q / BS; i = q % BS; }
+            else    { i = q / kTN; n = q % kTN; }
+            sa[n][i] = ra[k];
         }
         __syncthreads();
+        if (e + 1 < e1) load(e + 1);    // in flight during the multiply below
 #pragma unroll
         for (int r = 0; r < OUT; ++r) {
             int n, j;
