@@ -176,11 +176,12 @@ def traffic_for(kernel_pass):
 
 
 def source_sha():
-    """Hash of the sources of the step's kernels (the normalisations and projections are not part
-    of the step)."""
+    """Hash of the sources of the step's kernels: every file in csrc/ but the normalisations,
+    the projections, the SIMT and the block-size 16/8 kernels, none of which the step runs."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_sparse_matrix_gb300", "csrc")
-    for name in sorted(n for n in os.listdir(csrc) if n not in ("bsmm_norm.cu", "bsmm_wnorm.cu", "bsmm_proj.cu")):
+    skip = ("bsmm_norm.cu", "bsmm_wnorm.cu", "bsmm_proj.cu", "bsmm_simt.cu", "bsmm_sp.cu")
+    for name in sorted(n for n in os.listdir(csrc) if n not in skip):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
