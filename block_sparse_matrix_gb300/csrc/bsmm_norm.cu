@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 
 #include "bsmm.h"
 #include "bsmm_internal.cuh"
@@ -69,51 +70,90 @@ __device__ __forceinline__ float block_sum(float v, float *red)
     return s;
 }
 
-// axis = 1: one CTA per row of C features.  Thread t holds the 16-byte vectors t, t + 256, ...,
-// IT of them (IT * 256 * VEC >= C, chosen per call so short rows need few registers).
-template <typename T, int IT>
+// RPC sums over the CTA at once (kLnThreads threads); every thread gets the totals.  `red` has
+// RPC slots per warp.  Two barriers for all RPC sums.
+template <int RPC>
+__device__ __forceinline__ void block_sums(float (&v)[RPC], float *red)
+{
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < RPC; ++r)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
+    __syncthreads();                                   // red may still be read by a previous call
+    if (lane == 0)
+#pragma unroll
+        for (int r = 0; r < RPC; ++r) red[warp * RPC + r] = v[r];
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < RPC; ++r) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kLnThreads / 32; ++w) s += red[w * RPC + r];
+        v[r] = s;
+    }
+}
+
+// axis = 1: a CTA normalises RPC consecutive rows of C features.  Thread t holds the 16-byte
+// vectors t, t + 256, ..., IT of them per row (IT * 256 * VEC >= C, chosen per call so short rows
+// need few registers); all RPC rows' loads are issued before the first sum, and the RPC rows'
+// sums share each pair of barriers.
+template <typename T, int IT, int RPC>
 __global__ void __launch_bounds__(kLnThreads) k_ln_rows(const T *__restrict__ x, const float *__restrict__ g,
-                                                        const float *__restrict__ b, T *y, int C, float eps,
+                                                        const float *__restrict__ b, T *y, int N, int C, float eps,
                                                         int relu)
 {
     constexpr int VEC = 16 / sizeof(T);
-    __shared__ float red[kLnThreads / 32];
+    __shared__ float red[RPC * kLnThreads / 32];
     tc::pdl_launch_dependents();                       // holds no tensor memory: the next kernel may start
     tc::pdl_wait();                                    // the previous kernel's writes are visible
-    const T *xr = x + (size_t)blockIdx.x * C;
-    T *yr = y + (size_t)blockIdx.x * C;
-    float v[IT][VEC];
-    float s = 0.f;
+    const int n0 = blockIdx.x * RPC;
+    float v[RPC][IT][VEC];
+    float s[RPC];
 #pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
-        if (f0 < C) {
-            const uint4 raw = *reinterpret_cast<const uint4 *>(xr + f0);
-            const T *e = reinterpret_cast<const T *>(&raw);
+    for (int r = 0; r < RPC; ++r) {
+        s[r] = 0.f;
+        const bool live = n0 + r < N;
+        const T *xr = x + (size_t)(n0 + r) * C;
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                v[it][j] = ld1<T>(e + j);
-                s += v[it][j];
-            }
-        } else {
+        for (int it = 0; it < IT; ++it) {
+            const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
+            if (live && f0 < C) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(xr + f0);
+                const T *e = reinterpret_cast<const T *>(&raw);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) v[it][j] = 0.f;
-        }
-    }
-    const float mean = block_sum(s, red) / (float)C;
-    float q = 0.f;
+                for (int j = 0; j < VEC; ++j) v[r][it][j] = ld1<T>(e + j);
+            } else {
 #pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
-        if (f0 < C) {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                const float d = v[it][j] - mean;
-                q += d * d;
+                for (int j = 0; j < VEC; ++j) v[r][it][j] = 0.f;
             }
         }
     }
-    const float rstd = rsqrtf(block_sum(q, red) / (float)C + eps);
+#pragma unroll
+    for (int r = 0; r < RPC; ++r)
+#pragma unroll
+        for (int it = 0; it < IT; ++it)
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) s[r] += v[r][it][j];
+    block_sums<RPC>(s, red);
+    float mean[RPC], q[RPC];
+#pragma unroll
+    for (int r = 0; r < RPC; ++r) {
+        mean[r] = s[r] / (float)C;
+        q[r] = 0.f;
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
+            if (f0 < C) {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const float d = v[r][it][j] - mean[r];
+                    q[r] += d * d;
+                }
+            }
+        }
+    }
+    block_sums<RPC>(q, red);
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
         const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
@@ -124,15 +164,20 @@ __global__ void __launch_bounds__(kLnThreads) k_ln_rows(const T *__restrict__ x,
                 *reinterpret_cast<float4 *>(gv + j) = *reinterpret_cast<const float4 *>(g + f0 + j);
                 *reinterpret_cast<float4 *>(bv + j) = *reinterpret_cast<const float4 *>(b + f0 + j);
             }
-            uint4 raw;
-            T *e = reinterpret_cast<T *>(&raw);
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                float o = gv[j] * ((v[it][j] - mean) * rstd) + bv[j];
-                if (relu) o = fmaxf(o, 0.f);
-                e[j] = st1<T>(o);
+            for (int r = 0; r < RPC; ++r) {
+                if (n0 + r >= N) continue;
+                const float rstd = rsqrtf(q[r] / (float)C + eps);
+                uint4 raw;
+                T *e = reinterpret_cast<T *>(&raw);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    float o = gv[j] * ((v[r][it][j] - mean[r]) * rstd) + bv[j];
+                    if (relu) o = fmaxf(o, 0.f);
+                    e[j] = st1<T>(o);
+                }
+                *reinterpret_cast<uint4 *>(y + (size_t)(n0 + r) * C + f0) = raw;
             }
-            *reinterpret_cast<uint4 *>(yr + f0) = raw;
         }
     }
 }
@@ -438,6 +483,130 @@ k_lng_rows(const T *__restrict__ x, const T *__restrict__ y, const float *__rest
     if (threadIdx.x == 0) {
         stats[2 * blockIdx.x] = mean;
         stats[2 * blockIdx.x + 1] = rstd;
+    }
+}
+
+// axis = 1 gradient in one pass for rows of at most 4 vectors per thread: CTA p takes the R
+// consecutive samples of chunk p in turn, loading the next sample's x, dy (and y) while it
+// finishes the current one, and keeps the per-feature partial dg, db of its chunk in registers
+// (each thread owns the same features in every row); it writes them to ws[p][f], ws[p][C + f]
+// for k_lng_reduce.  Three two-barrier block sums per sample: mean, variance, (sum a, sum a xh).
+template <typename T, int IT>
+__global__ void __launch_bounds__(kLnThreads)
+k_lng_rows_fused(const T *__restrict__ x, const T *__restrict__ y, const float *__restrict__ g, const T *dy, T *dx,
+                 float *__restrict__ ws, int N, int C, int R, float eps, int relu)
+{
+    constexpr int VEC = 16 / sizeof(T);
+    __shared__ float red[2 * kLnThreads / 32];
+    tc::pdl_launch_dependents();
+    tc::pdl_wait();
+    const int n0 = blockIdx.x * R, n1 = min(N, n0 + R);
+    float pg[IT][VEC], pb[IT][VEC], gv[IT][VEC];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) pg[it][j] = pb[it][j] = gv[it][j] = 0.f;
+        if (f0 < C)
+#pragma unroll
+            for (int j = 0; j < VEC; j += 4)
+                *reinterpret_cast<float4 *>(&gv[it][j]) = *reinterpret_cast<const float4 *>(g + f0 + j);
+    }
+    uint4 cx[IT], cd[IT], cy[IT];                      // the current sample's raw vectors
+    auto load = [&](int n, uint4 (&lx)[IT], uint4 (&ld)[IT], uint4 (&ly)[IT]) {
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
+            lx[it] = ld[it] = ly[it] = make_uint4(0u, 0u, 0u, 0u);
+            if (n < n1 && f0 < C) {
+                const size_t o = (size_t)n * C + f0;
+                lx[it] = *reinterpret_cast<const uint4 *>(x + o);
+                ld[it] = *reinterpret_cast<const uint4 *>(dy + o);
+                if (relu) ly[it] = *reinterpret_cast<const uint4 *>(y + o);
+            }
+        }
+    };
+    load(n0, cx, cd, cy);
+    for (int n = n0; n < n1; ++n) {
+        uint4 nx[IT], nd[IT], ny[IT];
+        load(n + 1, nx, nd, ny);                       // in flight while this sample is finished
+        float xh[IT][VEC], a[IT][VEC];
+        float s1[1] = {0.f};
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const T *ex = reinterpret_cast<const T *>(&cx[it]);
+            const T *ed = reinterpret_cast<const T *>(&cd[it]);
+            const T *ey = reinterpret_cast<const T *>(&cy[it]);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                xh[it][j] = ld1<T>(ex + j);
+                s1[0] += xh[it][j];
+                a[it][j] = (relu && !(ld1<T>(ey + j) > 0.f)) ? 0.f : ld1<T>(ed + j);   // dz, for now
+            }
+        }
+        block_sums<1>(s1, red);
+        const float mean = s1[0] / (float)C;
+        float q1[1] = {0.f};
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
+            if (f0 < C)
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const float d = xh[it][j] - mean;
+                    q1[0] += d * d;
+                }
+        }
+        block_sums<1>(q1, red);
+        const float rstd = rsqrtf(q1[0] / (float)C + eps);
+        float t2[2] = {0.f, 0.f};
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
+            if (f0 < C)
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const float h = (xh[it][j] - mean) * rstd;
+                    const float dz = a[it][j];
+                    xh[it][j] = h;
+                    pg[it][j] += dz * h;
+                    pb[it][j] += dz;
+                    a[it][j] = gv[it][j] * dz;
+                    t2[0] += a[it][j];
+                    t2[1] += a[it][j] * h;
+                }
+        }
+        block_sums<2>(t2, red);
+        const float ma = t2[0] / (float)C, mx = t2[1] / (float)C;
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
+            if (f0 < C) {
+                uint4 raw;
+                T *e = reinterpret_cast<T *>(&raw);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) e[j] = st1<T>(rstd * (a[it][j] - ma - xh[it][j] * mx));
+                *reinterpret_cast<uint4 *>(dx + (size_t)n * C + f0) = raw;
+            }
+        }
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            cx[it] = nx[it];
+            cd[it] = nd[it];
+            cy[it] = ny[it];
+        }
+    }
+    float *w0 = ws + (size_t)blockIdx.x * 2 * C;
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int f0 = (it * kLnThreads + (int)threadIdx.x) * VEC;
+        if (f0 < C)
+#pragma unroll
+            for (int j = 0; j < VEC; j += 4) {
+                *reinterpret_cast<float4 *>(w0 + f0 + j) = make_float4(pg[it][j], pg[it][j + 1], pg[it][j + 2], pg[it][j + 3]);
+                *reinterpret_cast<float4 *>(w0 + C + f0 + j) =
+                    make_float4(pb[it][j], pb[it][j + 1], pb[it][j + 2], pb[it][j + 3]);
+            }
     }
 }
 
@@ -833,12 +1002,30 @@ cudaError_t launch_pdl_ln(void (*kern)(KArgs...), int grid, size_t smem, cudaStr
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Rows per CTA: several when the rows are short enough for their registers and the grid still
+// gives every SM a few CTAs (BSMM_LN_RPC pins 1, 2 or 4 for tuning).
+inline int ln_rows_per_cta(int N, int it)
+{
+    if (const char *e = getenv("BSMM_LN_RPC")) {
+        const int v = atoi(e);
+        if (v == 1 || v == 2 || v == 4) return it <= 4 || v == 1 ? v : 1;
+    }
+    if (it > 4) return 1;
+    return N >= 1024 ? 4 : 1;                          // measured: 2 rows per CTA was slower than 1 at N = 1024
+}
+
 template <typename T, int IT>
 cudaError_t launch_rows(const void *x, const float *g, const float *b, void *y, int N, int C, float eps, int relu,
                         cudaStream_t s)
 {
-    return launch_pdl_ln(k_ln_rows<T, IT>, N, 0, s, static_cast<const T *>(x), g, b, static_cast<T *>(y), C, eps,
-                         relu);
+    const int rpc = ln_rows_per_cta(N, IT);
+    const T *xt = static_cast<const T *>(x);
+    T *yt = static_cast<T *>(y);
+    if (IT <= 4 && rpc == 4)
+        return launch_pdl_ln(k_ln_rows<T, IT, (IT <= 4 ? 4 : 1)>, (N + 3) / 4, 0, s, xt, g, b, yt, N, C, eps, relu);
+    if (IT <= 4 && rpc == 2)
+        return launch_pdl_ln(k_ln_rows<T, IT, (IT <= 4 ? 2 : 1)>, (N + 1) / 2, 0, s, xt, g, b, yt, N, C, eps, relu);
+    return launch_pdl_ln(k_ln_rows<T, IT, 1>, N, 0, s, xt, g, b, yt, N, C, eps, relu);
 }
 
 template <typename T>
@@ -921,24 +1108,37 @@ cudaError_t launch_lng(const void *x, const void *y, const float *g, const void 
     if (axis == 1) {
         const int vec = 16 / (int)sizeof(T);
         const int need = (C + kLnThreads * vec - 1) / (kLnThreads * vec);
-        if (need <= 1) le = launch_lng_rows<T, 1>(x, y, g, dy, dx, ws, N, C, eps, relu, s);
+        // rows of at most 4 vectors per thread: one pass for dx and the chunk partials (the same
+        // chunks as the column-sum kernel); BSMM_LNG_SPLIT=1 forces the three-kernel form
+        const bool fused = need <= 4 && !getenv("BSMM_LNG_SPLIT");
+        if (fused) {
+            const int R = lng_chunk_rows(N), P = lng_parts(N, 1);
+            const T *xt = static_cast<const T *>(x), *yt = static_cast<const T *>(y), *dyt = static_cast<const T *>(dy);
+            T *dxt = static_cast<T *>(dx);
+            if (need <= 1) le = launch_pdl_ln(k_lng_rows_fused<T, 1>, P, 0, s, xt, yt, g, dyt, dxt, parts, N, C, R, eps, relu);
+            else if (need <= 2) le = launch_pdl_ln(k_lng_rows_fused<T, 2>, P, 0, s, xt, yt, g, dyt, dxt, parts, N, C, R, eps, relu);
+            else le = launch_pdl_ln(k_lng_rows_fused<T, 4>, P, 0, s, xt, yt, g, dyt, dxt, parts, N, C, R, eps, relu);
+        } else if (need <= 1) le = launch_lng_rows<T, 1>(x, y, g, dy, dx, ws, N, C, eps, relu, s);
         else if (need <= 2) le = launch_lng_rows<T, 2>(x, y, g, dy, dx, ws, N, C, eps, relu, s);
         else if (need <= 4) le = launch_lng_rows<T, 4>(x, y, g, dy, dx, ws, N, C, eps, relu, s);
         else if (need <= 8) le = launch_lng_rows<T, 8>(x, y, g, dy, dx, ws, N, C, eps, relu, s);
         else le = launch_lng_rows<T, 16>(x, y, g, dy, dx, ws, N, C, eps, relu, s);
-        g_bsmm_launches += 1;
-        if (le != cudaSuccess) return le;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)need, (unsigned)lng_parts(N, 1));
-        cfg.blockDim = dim3(kLnThreads);
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        le = cudaLaunchKernelEx(&cfg, k_lng_colsum<T>, static_cast<const T *>(x), static_cast<const T *>(y),
-                                static_cast<const T *>(dy), (const float *)ws, parts, N, C, lng_chunk_rows(N), relu);
+        if (!fused) {
+            g_bsmm_launches += 1;
+            if (le != cudaSuccess) return le;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)need, (unsigned)lng_parts(N, 1));
+            cfg.blockDim = dim3(kLnThreads);
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            le = cudaLaunchKernelEx(&cfg, k_lng_colsum<T>, static_cast<const T *>(x), static_cast<const T *>(y),
+                                    static_cast<const T *>(dy), (const float *)ws, parts, N, C, lng_chunk_rows(N),
+                                    relu);
+        }
     } else {
         const int tiles = lng_parts(N, 0);
         const int rows = (C + kLnSplit - 1) / kLnSplit;

@@ -44,6 +44,18 @@ def test_layer_norm_parity(axis, dtype, relu, N, C):
     assert rel_fro(cpu64(y), ref) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("rpc", ["1", "2", "4"])
+@pytest.mark.parametrize("dtype,C", [("bf16", 4096), ("f32", 24), ("f16", 2056)])
+def test_layer_norm_rows_per_cta(monkeypatch, rpc, dtype, C):
+    """(N, C) rows normalised 1, 2 or 4 per CTA, with a minibatch that is not a multiple of 4."""
+    monkeypatch.setenv("BSMM_LN_RPC", rpc)
+    N = 1030
+    x, g, b = _case(N, C, 1, dtype, 77 + C)
+    y = bsmm.layer_norm(x.cuda(), g.cuda(), b.cuda(), relu=True)
+    torch.cuda.synchronize()
+    assert rel_fro(cpu64(y), o.layer_norm(x, g, b, relu=True)) <= TOL[dtype]
+
+
 @pytest.mark.parametrize("axis", [1, 0])
 def test_layer_norm_constant_samples_give_shift_exactly(axis):
     N, C = 64, 4096
@@ -104,6 +116,22 @@ def test_layer_norm_grad_parity(axis, dtype, relu, N, C):
                                       dx=dx)
     torch.cuda.synchronize()
     rdx, rdg, rdb = o.layer_norm_grad(x, g, dy, y=cpu64(y) if relu else None, axis=axis, epsilon=eps, relu=relu)
+    assert rel_fro(cpu64(dx), rdx) <= GTOL[dtype]
+    assert rel_fro(cpu64(dg), rdg) <= SUMTOL
+    assert rel_fro(cpu64(db), rdb) <= SUMTOL
+
+
+@pytest.mark.parametrize("form", ["fused", "split"])
+@pytest.mark.parametrize("dtype,N,C", [("bf16", 1030, 4096), ("f32", 7, 1000), ("f16", 5000, 64)])
+def test_layer_norm_grad_rows_forms(monkeypatch, form, dtype, N, C):
+    """(N, C) gradient in one pass (rows in chunks, partials in registers) and in the three-kernel
+    form (dx, then chunked column sums), including chunks of more than 8 samples (N > 4096)."""
+    if form == "split":
+        monkeypatch.setenv("BSMM_LNG_SPLIT", "1")
+    x, g, dy, y = _grad_case(N, C, 1, dtype, 91 + N, True, 1e-5)
+    dx, dg, db = bsmm.layer_norm_grad(x.cuda(), g.cuda(), dy.cuda(), y=y, relu=True, epsilon=1e-5)
+    torch.cuda.synchronize()
+    rdx, rdg, rdb = o.layer_norm_grad(x, g, dy, y=cpu64(y), relu=True, epsilon=1e-5)
     assert rel_fro(cpu64(dx), rdx) <= GTOL[dtype]
     assert rel_fro(cpu64(dg), rdg) <= SUMTOL
     assert rel_fro(cpu64(db), rdb) <= SUMTOL
