@@ -370,8 +370,8 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
 }
 
 
-constexpr int kLngChunks = 512;         // axis = 1: at most this many partial sets (row chunks)
-constexpr int kLngChunkRows = 8;        // axis = 1: at least this many samples per chunk
+constexpr int kLngChunks = 1024;        // axis = 1: at most this many partial sets (row chunks)
+constexpr int kLngChunkRows = 4;        // axis = 1: at least this many samples per chunk
 
 // Two sums over the CTA at once; every thread gets both totals.  `red` has two slots per warp.
 __device__ __forceinline__ float2 block_sum2(float u, float v, float *red)

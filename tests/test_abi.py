@@ -97,8 +97,8 @@ def test_layer_norm_grad_rejects_bad_arguments_on_host():
     A, B, D, W = 0x10000, 0x20000, 0x30000, 0x40000   # 16-byte aligned stand-ins, never dereferenced
     ws = L.bsmm_layer_norm_grad_workspace(4, 8, 1)
     assert ws == (8 + 1 * 2 * 8) * 4                     # 2N statistics + one chunk of 2C partials
-    assert L.bsmm_layer_norm_grad_workspace(1000, 64, 1) == (2000 + 125 * 2 * 64) * 4   # 8-sample chunks
-    assert L.bsmm_layer_norm_grad_workspace(8000, 64, 1) == (16000 + 500 * 2 * 64) * 4  # at most 512 chunks
+    assert L.bsmm_layer_norm_grad_workspace(1000, 64, 1) == (2000 + 250 * 2 * 64) * 4   # 4-sample chunks
+    assert L.bsmm_layer_norm_grad_workspace(8000, 64, 1) == (16000 + 1000 * 2 * 64) * 4  # at most 1024 chunks
     assert L.bsmm_layer_norm_grad_workspace(1000, 64, 0) == 32 * 2 * 64 * 4             # 32-sample tiles
     assert L.bsmm_layer_norm_grad_workspace(-1, 8, 1) == 0
 
