@@ -2378,7 +2378,9 @@ FbStages choose_stages(const bsmm_ctx *h, int N, int64_t units, int W)
     const double density = (double)h->nnz / ((double)h->R * h->S);
     const double coarse_density = h->bs == 8 ? std::min(1.0, 4.0 * density) : density;
     const int expect_r = (int)(1.25 * W * gc * coarse_density) + 1;
-    g.e_slots = h->fa ? (g.half ? 2 : 1) : (h->bs == 32 ? 2 : 4);
+    // (N,C) panels: two per chunk (measured on N = 128 recurrent steps: 14.6 us against 16.9 with one,
+    // 16.0 with four)
+    g.e_slots = h->fa ? 2 : (h->bs == 32 ? 2 : 4);
     const int r_cap = (32 - g.e_slots * a_ops) / b_ops;
     g.r_slots = std::max(2, std::min(r_cap, g.e_slots * expect_r));
     const int budget_two = h->tc_stage_kb >= 32 ? std::min(h->tc_stage_kb, 196) * 1024 : 96 * 1024;
