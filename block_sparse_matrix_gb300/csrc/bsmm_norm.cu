@@ -40,7 +40,7 @@ namespace {
 constexpr int kLnThreads = 256;
 constexpr int kLnMaxC = 16384;          // axis = 1: at most 16 vectors of 16 bytes per thread
 constexpr int kLnSplit = 8;             // axis = 0: CTAs per cluster along the features
-constexpr int kLnCols = 64;             // axis = 0: samples (columns) per cluster
+constexpr int kLnCols = 64;             // axis = 0: samples (columns) per cluster (32 measured slower)
 constexpr int kLnCacheMax = 160 * 1024; // axis = 0: dynamic shared memory of a CTA (slice + g, b)
 constexpr int kLngCacheMax = 66 * 1024;  // axis = 0 gradient: cached slices + g (three CTAs per SM)
 constexpr int kLngCols = 32;            // axis = 0 gradient: samples (columns) per cluster
@@ -227,34 +227,35 @@ template <typename T> __device__ __forceinline__ void unpack8(const Vec8<T> &v, 
     for (int j = 0; j < 8; ++j) f[j] = ld1<T>(e + j);
 }
 
-// axis = 0: (C, N).  A cluster of kLnSplit CTAs owns kLnCols = 64 consecutive samples
-// (columns); CTA r takes rows [r * rows, (r + 1) * rows).  Thread t reads 8 consecutive columns
-// (cc = t % 8) of rows rg, rg + 32, ... (rg = t / 8), so a warp reads 4 rows of 128 bytes per
-// instruction.  The CTA's slice is kept in shared memory (CACHE), so x is read from memory
+// axis = 0: (C, N).  A cluster of kLnSplit CTAs owns COLS consecutive samples (columns); CTA r
+// takes rows [r * rows, (r + 1) * rows).  Thread t reads 8 consecutive columns (cc = t % TPR,
+// TPR = COLS / 8) of rows rg, rg + RG, ... (rg = t / TPR), so a warp reads 32 / TPR rows of
+// 16 * TPR bytes per instruction.  (32-sample tiles, twice the clusters, measured slower than 64:
+// 12.1 against 11.0 us at N = 1024, C = 4096.)  The CTA's slice is kept in shared memory (CACHE), so x is read from memory
 // once; the second and third pass (squared deviations, output) read the slice.
-template <typename T, bool CACHE>
+template <typename T, bool CACHE, int COLS>
 __global__ void __cluster_dims__(kLnSplit, 1, 1) __launch_bounds__(kLnThreads)
 k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__restrict__ b, T *y, int C, int N,
           float eps, int relu)
 {
     extern __shared__ __align__(16) uint8_t ln_smem[];
     Vec8<T> *slice = reinterpret_cast<Vec8<T> *>(ln_smem);          // [rows][8] vectors (CACHE)
-    __shared__ float acc[kLnThreads / 8][kLnCols];                    // per row group, per column
-    __shared__ float part1[kLnCols], part2[kLnCols];                  // this CTA's partial sums
-    __shared__ float stat[2][kLnCols];                                // cluster-wide mean, 1 / std
+    constexpr int TPR = COLS / 8, RG = kLnThreads / TPR;              // threads per row, row groups
+    __shared__ float acc[RG][COLS];                                    // per row group, per column
+    __shared__ float part1[COLS], part2[COLS];                  // this CTA's partial sums
+    __shared__ float stat[2][COLS];                                // cluster-wide mean, 1 / std
     tc::pdl_launch_dependents();                       // holds no tensor memory: the next kernel may start
     tc::pdl_wait();                                    // the previous kernel's writes are visible
     const uint32_t rank = tc::cluster_ctarank();
     const int tile = blockIdx.x / kLnSplit;
-    const int rg = threadIdx.x / 8, cc = threadIdx.x & 7;
-    const int n0 = tile * kLnCols + cc * 8;                            // first of this thread's 8 columns
+    const int rg = threadIdx.x / TPR, cc = threadIdx.x % TPR;
+    const int n0 = tile * COLS + cc * 8;                            // first of this thread's 8 columns
     const bool has = n0 < N;                                           // N % 8 == 0: all 8 or none
     const int rows = (C + kLnSplit - 1) / kLnSplit;
     const int r0 = (int)rank * rows, r1 = min(C, r0 + rows);
     const int nr = max(0, r1 - r0);
-    constexpr int RG = kLnThreads / 8;                                 // 32 row groups
     // g, b of this CTA's rows, staged once so the output pass does not wait on them per row
-    float *sg = reinterpret_cast<float *>(ln_smem + (CACHE ? (size_t)rows * sizeof(Vec8<T>) * 8 : 0));
+    float *sg = reinterpret_cast<float *>(ln_smem + (CACHE ? (size_t)rows * sizeof(Vec8<T>) * TPR : 0));
     float *sb = sg + rows;
     for (int i = threadIdx.x; i < nr; i += kLnThreads) {
         sg[i] = g[r0 + i];
@@ -271,14 +272,14 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
                 const T *src = x + (size_t)(r0 + i) * N + n0;
 #pragma unroll
                 for (int h = 0; h < (int)(sizeof(Vec8<T>) / 16); ++h)
-                    cp_async16(reinterpret_cast<uint8_t *>(&slice[i * 8 + cc]) + 16 * h,
+                    cp_async16(reinterpret_cast<uint8_t *>(&slice[i * TPR + cc]) + 16 * h,
                                reinterpret_cast<const uint8_t *>(src) + 16 * h);
             }
         cp_async_wait_all();                           // this thread's copies have landed
         if (has)
             for (int i = rg; i < nr; i += RG) {        // each thread reads back only its own copies
                 float f[8];
-                unpack8<T>(slice[i * 8 + cc], f);
+                unpack8<T>(slice[i * TPR + cc], f);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) s[j] += f[j];
             }
@@ -307,14 +308,14 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[rg][cc * 8 + j] = s[j];
     __syncthreads();
-    if (threadIdx.x < kLnCols) {
+    if (threadIdx.x < COLS) {
         float t = 0.f;
 #pragma unroll
         for (int w = 0; w < RG; ++w) t += acc[w][threadIdx.x];
         part1[threadIdx.x] = t;
     }
     tc::cluster_sync();                                // every CTA's part1 is written
-    if (threadIdx.x < kLnCols) stat[0][threadIdx.x] = cluster_sum(part1, threadIdx.x) / (float)C;
+    if (threadIdx.x < COLS) stat[0][threadIdx.x] = cluster_sum(part1, threadIdx.x) / (float)C;
     __syncthreads();
     float mean[8];
 #pragma unroll
@@ -325,7 +326,7 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
     if (has)
         for (int i = rg; i < nr; i += RG) {
             float f[8];
-            unpack8<T>(CACHE ? slice[i * 8 + cc] : gload(r0 + i), f);
+            unpack8<T>(CACHE ? slice[i * TPR + cc] : gload(r0 + i), f);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const float d = f[j] - mean[j];
@@ -336,14 +337,14 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[rg][cc * 8 + j] = q[j];
     __syncthreads();
-    if (threadIdx.x < kLnCols) {
+    if (threadIdx.x < COLS) {
         float t = 0.f;
 #pragma unroll
         for (int w = 0; w < RG; ++w) t += acc[w][threadIdx.x];
         part2[threadIdx.x] = t;
     }
     tc::cluster_sync();                                // every CTA's part2 is written
-    if (threadIdx.x < kLnCols) stat[1][threadIdx.x] = rsqrtf(cluster_sum(part2, threadIdx.x) / (float)C + eps);
+    if (threadIdx.x < COLS) stat[1][threadIdx.x] = rsqrtf(cluster_sum(part2, threadIdx.x) / (float)C + eps);
     __syncthreads();
     float rstd[8];
 #pragma unroll
@@ -354,7 +355,7 @@ k_ln_cols(const T *__restrict__ x, const float *__restrict__ g, const float *__r
         for (int i = rg; i < nr; i += RG) {
             const int f = r0 + i;
             float v[8];
-            unpack8<T>(CACHE ? slice[i * 8 + cc] : gload(f), v);
+            unpack8<T>(CACHE ? slice[i * TPR + cc] : gload(f), v);
             const float gf = sg[i], bf = sb[i];
             Vec8<T> o;
             T *e = reinterpret_cast<T *>(&o);
@@ -1046,7 +1047,7 @@ cudaError_t launch_ln(const void *x, const float *g, const float *b, void *y, in
         const size_t slice = (size_t)rows * kLnCols * sizeof(T);
         const size_t gb = (size_t)rows * 2 * sizeof(float);             // staged g, b
         if (slice + gb <= (size_t)kLnCacheMax) {
-            auto kern = k_ln_cols<T, true>;
+            auto kern = k_ln_cols<T, true, kLnCols>;
             static std::atomic<int> attr_set{-1};      // device whose limit has been raised
             int dev = 0;
             cudaError_t e = cudaGetDevice(&dev);
@@ -1059,7 +1060,7 @@ cudaError_t launch_ln(const void *x, const float *g, const float *b, void *y, in
             le = launch_pdl_ln(kern, tiles * kLnSplit, slice + gb, s, static_cast<const T *>(x), g, b,
                                static_cast<T *>(y), C, N, eps, relu);
         } else {
-            auto kern = k_ln_cols<T, false>;
+            auto kern = k_ln_cols<T, false, kLnCols>;
             static std::atomic<int> attr_set{-1};
             int dev = 0;
             cudaError_t e = cudaGetDevice(&dev);
