@@ -1,0 +1,96 @@
+"""Edge cases of the three passes through the C ABI against the float64 oracle: every minibatch
+size around the dispatch boundaries (one 64-row tile, one 128-row tile, 256-row tiles, ragged
+tails), a one-sample minibatch, an empty minibatch, one-block layouts, single block rows and
+columns, and the largest window sizes, on both activation layouts and every block size."""
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_matrix_gb300 import workloads as wk
+from block_sparse_matrix_gb300.bsmm import BlocksparseMatMul
+from oracle import oracle as o
+
+from _util import TOL_DW, cpu64, rand_layout, rel_fro
+
+pytestmark = pytest.mark.gpu
+TIGHT = {"f32": 1e-5, "f16": 2e-3, "bf16": 8e-3}
+DT = wk.DTYPES
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _check(L, bs, fa, dtype, N, seed):
+    R, S = L.shape
+    nnz = int(L.sum())
+    x = wk.normals(wk.act_shape(R * bs, N, fa), seed, 1.0, dtype)
+    dy = wk.normals(wk.act_shape(S * bs, N, fa), seed + 1, 1.0, dtype)
+    w = wk.normals((nnz, bs, bs), seed + 2, float(1 / np.sqrt(max(1, R * bs))), dtype)
+    m = BlocksparseMatMul(L, block_size=bs, feature_axis=fa)
+    y = torch.full(m.o_shape(N), float("nan"), dtype=DT[dtype], device="cuda")
+    dx = torch.full(m.i_shape(N), float("nan"), dtype=DT[dtype], device="cuda")
+    m.fprop(x.cuda(), w.cuda(), y)
+    m.bprop(dy.cuda(), w.cuda(), dx)
+    dw = m.updat(x.cuda(), dy.cuda())
+    m.sync_status()
+    assert rel_fro(cpu64(y), o.fprop(L, bs, x, w, fa)) <= TIGHT[dtype]
+    assert rel_fro(cpu64(dx), o.bprop(L, bs, dy, w, fa)) <= TIGHT[dtype]
+    assert rel_fro(cpu64(dw), o.updat(L, bs, x, dy, fa)) <= TOL_DW[dtype]
+    m.close()
+
+
+@pytest.mark.parametrize("bs,p", [(32, 0.5), (32, 0.1), (16, 0.3), (8, 0.3)])
+@pytest.mark.parametrize("fa", [1, 0])
+@pytest.mark.parametrize("N", [1, 8, 56, 64, 72, 120, 128, 136, 248, 256, 264, 392])
+def test_minibatch_sizes(bs, p, fa, N):
+    """Each minibatch size on both sides of the kernels' tile boundaries (64, 128, 256 rows);
+    (C, N) activations need N to be a multiple of 8, so N = 1 runs for (N, C) only."""
+    if fa == 0 and N % 8:
+        pytest.skip("(C, N) activations need a minibatch that is a multiple of 8")
+    L = rand_layout(12, 11, p, 100 + bs + N)
+    L[0, 0] = 1
+    _check(L, bs, fa, "bf16" if N % 2 else "f16", N, 7 * N + bs)
+
+
+@pytest.mark.parametrize("bs", [32, 16, 8])
+@pytest.mark.parametrize("fa", [1, 0])
+@pytest.mark.parametrize("shape", [(1, 1), (1, 9), (9, 1), (2, 3)])
+def test_tiny_layouts(bs, fa, shape):
+    """One block, one block row, one block column, a dense 2 x 3 layout."""
+    L = np.ones(shape, np.uint8)
+    _check(L, bs, fa, "bf16", 136, 11 * bs + shape[0])
+
+
+@pytest.mark.parametrize("bs", [32, 16, 8])
+@pytest.mark.parametrize("fa", [1, 0])
+def test_widest_windows(bs, fa):
+    """More output blocks than any window holds (512 tensor-memory columns): several windows per
+    tile, the last one partial."""
+    L = rand_layout(6, 70, 0.4, 55 + bs)
+    _check(L, bs, fa, "bf16", 200, 3 * bs)
+
+
+@pytest.mark.parametrize("bs", [32, 16])
+@pytest.mark.parametrize("fa", [1, 0])
+def test_empty_minibatch(bs, fa):
+    """N = 0: fprop and bprop write nothing; updat gives dW = 0, or leaves it unchanged when
+    accumulating."""
+    L = rand_layout(5, 4, 0.5, 3)
+    L[0, 0] = 1
+    m = BlocksparseMatMul(L, block_size=bs, feature_axis=fa)
+    x = torch.empty(m.i_shape(0), dtype=torch.bfloat16, device="cuda")
+    dy = torch.empty(m.o_shape(0), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(m.w_shape, dtype=torch.bfloat16, device="cuda")
+    assert m.fprop(x, w).numel() == 0
+    assert m.bprop(dy, w).numel() == 0
+    dw = torch.full(m.w_shape, 3.0, device="cuda")
+    m.updat(x, dy, dw=dw, accumulate=True)
+    m.sync_status()
+    assert torch.all(dw == 3.0)
+    m.updat(x, dy, dw=dw)
+    m.sync_status()
+    assert torch.all(dw == 0.0)
+    m.close()
