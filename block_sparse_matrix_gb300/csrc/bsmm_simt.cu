@@ -35,31 +35,31 @@ __device__ __forceinline__ size_t aidx(int64_t n, int64_t f, int64_t N, int64_t 
 
 // Output (n, j) handled by slot r of thread tid: feature-fastest for (N,F)
 // storage, minibatch-fastest for (F,N) storage, so stores coalesce.
-template <int BS, int FA>
+template <int BS, int FA, int TN>
 __device__ __forceinline__ void out_coord(int idx, int &n, int &j)
 {
     if (FA) { n = idx / BS; j = idx % BS; }
-    else    { n = idx % kTN; j = idx / kTN; }
+    else    { n = idx % TN; j = idx / TN; }
 }
 
 // BWD=false: fprop over the column LUT.  BWD=true: bprop over the row LUT.
 // The operands of entry e + 1 (weight block and input panel) are loaded into registers while
 // entry e is multiplied out of shared memory, so each entry costs one compute phase instead of a
 // memory round trip followed by it.
-template <typename T, int BS, int FA, bool BWD>
+template <typename T, int BS, int FA, bool BWD, int TN>
 __global__ void __launch_bounds__(kThreads)
 k_simt_fwd_bwd(const T *__restrict__ in, const T *__restrict__ w, T *__restrict__ out,
                const int32_t *__restrict__ ptr, const int32_t *__restrict__ ent,
                int N, int Fin, int Fout)
 {
-    constexpr int OUT = kTN * BS / kThreads;
+    constexpr int OUT = TN * BS / kThreads;
     constexpr int NW = (BS * BS + kThreads - 1) / kThreads;   // weight elements per thread
-    constexpr int NA = kTN * BS / kThreads;                     // panel elements per thread
+    constexpr int NA = TN * BS / kThreads;                     // panel elements per thread
     __shared__ float sw[BS][BS + 1];
-    __shared__ float sa[kTN][BS + 1];
+    __shared__ float sa[TN][BS + 1];
     const int tid = threadIdx.x;
     const int blk = blockIdx.x;         // output block column (fprop) / row (bprop)
-    const int n0 = blockIdx.y * kTN;
+    const int n0 = blockIdx.y * TN;
     float acc[OUT];
 #pragma unroll
     for (int r = 0; r < OUT; ++r) acc[r] = 0.f;
@@ -81,7 +81,7 @@ k_simt_fwd_bwd(const T *__restrict__ in, const T *__restrict__ w, T *__restrict_
             const int q = tid + k * kThreads;
             int n, i;
             if (FA) { n = q / BS; i = q % BS; }
-            else    { i = q / kTN; n = q % kTN; }
+            else    { i = q / TN; n = q % TN; }
             ra[k] = n0 + n < N ? to_f<T>(in[aidx<FA>(n0 + n, (int64_t)src * BS + i, N, Fin)]) : 0.f;
         }
     };
@@ -97,7 +97,7 @@ k_simt_fwd_bwd(const T *__restrict__ in, const T *__restrict__ w, T *__restrict_
             const int q = tid + k * kThreads;
             int n, i;
             if (FA) { n = q / BS; i = q % BS; }
-            else    { i = q / kTN; n = q % kTN; }
+            else    { i = q / TN; n = q % TN; }
             sa[n][i] = ra[k];
         }
         __syncthreads();
@@ -105,7 +105,7 @@ k_simt_fwd_bwd(const T *__restrict__ in, const T *__restrict__ w, T *__restrict_
 #pragma unroll
         for (int r = 0; r < OUT; ++r) {
             int n, j;
-            out_coord<BS, FA>(tid + kThreads * r, n, j);
+            out_coord<BS, FA, TN>(tid + kThreads * r, n, j);
             float s = acc[r];
 #pragma unroll
             for (int i = 0; i < BS; ++i)
@@ -117,7 +117,7 @@ k_simt_fwd_bwd(const T *__restrict__ in, const T *__restrict__ w, T *__restrict_
 #pragma unroll
     for (int r = 0; r < OUT; ++r) {
         int n, j;
-        out_coord<BS, FA>(tid + kThreads * r, n, j);
+        out_coord<BS, FA, TN>(tid + kThreads * r, n, j);
         if (n0 + n < N) out[aidx<FA>(n0 + n, (int64_t)blk * BS + j, N, Fout)] = from_f<T>(acc[r]);
     }
 }
@@ -196,20 +196,28 @@ template <typename T, int BS>
 bsmm_status fwd_bwd_bs(bsmm_ctx *h, const void *in, const void *w, void *out, int N, bool bwd, cudaStream_t s)
 {
     const int C = h->R * BS, K = h->S * BS;
-    dim3 grid(bwd ? h->R : h->S, (N + kTN - 1) / kTN);
+    // 64 minibatch rows per CTA, or 256 / BS when that still leaves the GPU short of CTAs (each
+    // CTA then walks its column's blocks with a quarter of the work per block)
+    const int blocks = bwd ? h->R : h->S;
+    const bool small = (int64_t)blocks * ((N + kTN - 1) / kTN) < h->sm_count;
+    constexpr int TNS = kThreads / BS;
+    dim3 grid(blocks, small ? (N + TNS - 1) / TNS : (N + kTN - 1) / kTN);
     const int32_t *ptr = bwd ? h->d_row_ptr : h->d_col_ptr;
     const int32_t *ent = bwd ? h->d_row_ent : h->d_col_ent;
     int Fin = bwd ? K : C, Fout = bwd ? C : K;
     const T *i_ = (const T *)in;
     const T *w_ = (const T *)w;
     T *o_ = (T *)out;
-    if (h->fa) {
-        if (bwd) k_simt_fwd_bwd<T, BS, 1, true><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout);
-        else     k_simt_fwd_bwd<T, BS, 1, false><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout);
-    } else {
-        if (bwd) k_simt_fwd_bwd<T, BS, 0, true><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout);
-        else     k_simt_fwd_bwd<T, BS, 0, false><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout);
+#define SIMT_FB(TN_)                                                                                     \
+    if (h->fa) {                                                                                         \
+        if (bwd) k_simt_fwd_bwd<T, BS, 1, true, TN_><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout); \
+        else     k_simt_fwd_bwd<T, BS, 1, false, TN_><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout); \
+    } else {                                                                                             \
+        if (bwd) k_simt_fwd_bwd<T, BS, 0, true, TN_><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout); \
+        else     k_simt_fwd_bwd<T, BS, 0, false, TN_><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout); \
     }
+    if (small) { SIMT_FB(TNS) } else { SIMT_FB(kTN) }
+#undef SIMT_FB
     g_bsmm_launches += 1;
     return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
