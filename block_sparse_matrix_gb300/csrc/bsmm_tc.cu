@@ -54,6 +54,11 @@ namespace {
 //                 0 = absent
 // Streams start on 16-byte boundaries and are padded to a multiple of 4 words so a CTA
 // can bulk-copy its window into shared memory.
+// (N,C) activation panels of the window kernel: row bytes and source blocks per row (a 32-feature
+// block alone in a 64-byte row; 16-feature blocks four to a 128-byte row).
+__host__ __device__ constexpr int fb_row_bytes(int bse) { return bse == 32 ? 64 : 128; }
+__host__ __device__ constexpr int fb_row_sources(int fa, int bse) { return fa ? fb_row_bytes(bse) / (2 * bse) : 1; }
+
 struct FbSched {
     int W = 0;                      // output slots per window
     int nwin = 0;                   // windows
@@ -195,7 +200,7 @@ bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W, int e_max, int r_max, i
     const int rw = coarse ? 4 : 1;                      // words per record
     int Fslots, Fsrc, bse;
     fb_shape(h, bwd, Fslots, Fsrc, bse);
-    const int gc = h->fa ? 128 / (2 * bse) : 1;         // source blocks per 128-byte activation row
+    const int gc = fb_row_sources(h->fa, bse);         // source blocks per activation panel row
     W = std::min(W, Fslots);
     const int nwin = (Fslots + W - 1) / W;
     BidLookup bid{h};
@@ -620,12 +625,14 @@ template <> __device__ __forceinline__ uint16_t cvt1<false>(float a)
 template <int BSE, int FA> struct FbGeo {
     static constexpr int B_SLOT = BSE * BSE * 2;                     // one (coarse) weight block
     static constexpr int KSTEPS = BSE / 16;
-    // A operand descriptor parameters.  (N,C) activations: K-major rows of 128 bytes holding
-    // GC = 64/BSE adjacent source blocks; block `sub` starts sub*BSE*2 bytes into the row.
-    // (C,N) activations: MN-major, two 64-row atoms of one block.
-    static constexpr uint32_t A_SWZ = SW_128;
+    // A operand descriptor parameters.  (N,C) activations: K-major rows of ROW bytes holding
+    // ROW / (2 BSE) adjacent source blocks (one 32-feature block for BSE = 32, so no panel carries
+    // a neighbour the window may not need; four 16-feature blocks otherwise); block `sub` starts
+    // sub*BSE*2 bytes into the row.  (C,N) activations: MN-major, two 64-row atoms of one block.
+    static constexpr int ROW = fb_row_bytes(BSE);
+    static constexpr uint32_t A_SWZ = FA ? (ROW == 64 ? SW_64 : SW_128) : SW_128;
     static constexpr uint32_t A_LBO = FA ? 16 : (BSE * 128);         // MN-major: distance of the two 64-row atoms
-    static constexpr uint32_t A_SBO = 1024;
+    static constexpr uint32_t A_SBO = FA ? 8 * ROW : 1024;
     static constexpr uint32_t A_KSTEP = FA ? 32 : (16 * 128);
     static constexpr uint32_t A_SUB = BSE * 2;                       // byte offset of block `sub` in a row
 };
@@ -767,7 +774,7 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
                     const int src = (int)(sched[pos + 1 + e] >> 8);
                     mp = &tm_act;
                     dst = stage + e * g.a_slot + (FA ? 0 : hf * BSE * 128);
-                    cx = FA ? src * 64 : n0 + 64 * hf;
+                    cx = FA ? src * (G::ROW / 2) : n0 + 64 * hf;
                     cy = FA ? n0 : src * BSE;
                     pol = pol_act;
                 } else {
@@ -2279,7 +2286,9 @@ bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const FbStages &geo, const void 
     const int Fin = BWD ? K : C, Fout = BWD ? C : K;
     CUtensorMap m_act, m_w, m_zero;
     bool ok;
-    if (FA) ok = make_map2d(&m_act, act, t, Fin, N, 64, geo.half ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (FA)
+        ok = make_map2d(&m_act, act, t, Fin, N, fb_row_bytes(BSE) / 2, geo.half ? 64 : 128,
+                        fb_row_bytes(BSE) == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
     else ok = make_map2d(&m_act, act, t, N, Fin, 64, BSE, CU_TENSOR_MAP_SWIZZLE_128B);
     const uint64_t wrows = (uint64_t)std::max<int64_t>(h->nnz, 1) * BS;
     const void *wp = h->nnz > 0 ? w : st->d_zero;
@@ -2371,15 +2380,15 @@ FbStages choose_stages(const bsmm_ctx *h, int N, int64_t units, int W)
     const int bse = h->bs == 8 ? 16 : h->bs;
     FbStages g;
     g.half = N <= 64 ? 1 : 0;
-    g.a_slot = (g.half ? 64 : 128) * (h->fa ? 128 : bse * 2);
+    g.a_slot = (g.half ? 64 : 128) * (h->fa ? fb_row_bytes(bse) : bse * 2);
     const int b_slot = bse * bse * 2;
     const int a_ops = (h->fa || g.half) ? 1 : 2, b_ops = h->bs == 8 ? 4 : 1;
-    const int gc = h->fa ? 128 / (2 * bse) : 1;
+    const int gc = fb_row_sources(h->fa, bse);
     const double density = (double)h->nnz / ((double)h->R * h->S);
     const double coarse_density = h->bs == 8 ? std::min(1.0, 4.0 * density) : density;
     const int expect_r = (int)(1.25 * W * gc * coarse_density) + 1;
     // (N,C) panels: two per chunk (measured on N = 128 recurrent steps: 14.6 us against 16.9 with one,
-    // 16.0 with four)
+    // 16.0 with four; with 64-byte rows for bs 32, four per chunk gave the same as two)
     g.e_slots = h->fa ? 2 : (h->bs == 32 ? 2 : 4);
     const int r_cap = (32 - g.e_slots * a_ops) / b_ops;
     g.r_slots = std::max(2, std::min(r_cap, g.e_slots * expect_r));
