@@ -284,6 +284,16 @@ bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W, int e_max, int r_max, i
     return true;
 }
 
+// BSMM_UP_TEST_BAD_ID (tests only): the block id at table word `word` (the first record of
+// the first CTA's first unit) becomes nnz + 5, which the weight-gradient epilogue must refuse
+// (no store, BSMM_ERR_BOUNDS).  `packed` ids keep their sub-block position in bits 24..31.
+void up_test_bad_id(const bsmm_ctx *h, std::vector<int32_t> &table, size_t word, bool packed)
+{
+    if (!getenv("BSMM_UP_TEST_BAD_ID") || table.size() <= word || table[0] == 0) return;
+    const int32_t bad = h->nnz + 5;
+    table[word] = packed ? (int32_t)(((uint32_t)table[word] & 0xFF000000u) | ((uint32_t)bad & 0xFFFFFFu)) : bad;
+}
+
 bool build_up(bsmm_ctx *h, UpSched &us)
 {
     const bool coarse = h->bs == 8;
@@ -327,6 +337,7 @@ bool build_up(bsmm_ctx *h, UpSched &us)
         std::copy(units[u].begin(), units[u].end(), t + 4 + i * kUnitWords);
     }
     us.ctas = nunits ? ctas : 0;
+    up_test_bad_id(h, table, 4 + 2 + 1, false);
     if (!upload(&us.d_table, table)) return false;
     us.built = true;
     return true;
@@ -382,6 +393,7 @@ bool build_up_dense(bsmm_ctx *h, UpDenseSched &us)
         std::copy(units[u].begin(), units[u].end(), t + 4 + i * kDUnitWords);
     }
     us.ctas = nunits ? ctas : 0;
+    up_test_bad_id(h, table, 4 + 3, true);
     if (!upload(&us.d_table, table)) return false;
     us.built = true;
     return true;
@@ -469,6 +481,7 @@ bool build_up_pair(bsmm_ctx *h, UpPairSched &us)
         std::copy(units[u].begin(), units[u].end(), t + 4 + i * kPUnitWords);
     }
     us.ctas = nunits ? 2 * pairs : 0;
+    up_test_bad_id(h, table, 4 + 4, true);
     if (!upload(&us.d_table, table)) return false;
     us.built = true;
     return true;
@@ -928,7 +941,17 @@ struct UpParams {
     int32_t *status;
     int N, G, accumulate;
     int dwt;                    // 0: float32 dW, 1: fp16, 2: bf16
+    int nnz;                    // blocks in dW: every table id is checked against it before a store
 };
+
+// True when block `id` lies inside dW; otherwise records BSMM_ERR_BOUNDS (sticky) and the
+// caller skips the store, so a corrupted table never writes past dW.
+__device__ __forceinline__ bool up_id_ok(int32_t id, const UpParams &p)
+{
+    if ((uint32_t)id < (uint32_t)p.nnz) return true;
+    atomicExch(p.status, (int32_t)BSMM_ERR_BOUNDS);
+    return false;
+}
 
 // Stores 4 consecutive dW values at element `off` in the output type; with accumulate, adds the
 // stored values in float32 first and rounds the sum once.
@@ -1149,7 +1172,7 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
                     const int sl = q * (32 / BSE) + o / BLK;
                     const int r = o / BS, c = (o % BS) / 4;
                     const float4 val = *reinterpret_cast<const float4 *>(stg + r * BS + ((c ^ (r & (CH - 1))) * 4));
-                    if (sl < ut[1] && !aborted)
+                    if (sl < ut[1] && !aborted && up_id_ok(ut[2 + 5 * sl + 1], p))
                         up_store4(p.dw, (size_t)ut[2 + 5 * sl + 1] * (BS * BS) + (o % BLK), val, p.accumulate, p.dwt);
                 }
                 __syncwarp();                                   // reads done before the next unit's writes
@@ -1160,7 +1183,7 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
                         const int32_t id = rec[1 + cs * 2 + ks];
-                        if (id < 0) continue;
+                        if (id < 0 || !up_id_ok(id, p)) continue;
 #pragma unroll
                         for (int j = 0; j < 8; j += 4)
                             up_store4(p.dw, ((size_t)id * 8 + i8) * 8 + j,
@@ -1348,7 +1371,7 @@ k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
                     *reinterpret_cast<float4 *>(stg + lane * 32 + ((c ^ (lane & 7)) * 4)) =
                         make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
                 __syncwarp();
-                if (!aborted) {
+                if (!aborted && up_id_ok(id, p)) {
 #pragma unroll
                     for (int k4 = 0; k4 < 8; ++k4) {
                         const int o = k4 * 128 + lane * 4, r = o / 32, c = (o % 32) / 4;
@@ -1564,7 +1587,7 @@ k_tc_updat_pair(const __grid_constant__ UpMaps maps, const UpParams p)
                     *reinterpret_cast<float4 *>(stg + lane * 32 + ((c ^ (lane & 7)) * 4)) =
                         make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
                 __syncwarp();
-                if (!aborted) {
+                if (!aborted && up_id_ok(id, p)) {
 #pragma unroll
                     for (int k4 = 0; k4 < 8; ++k4) {
                         const int o = k4 * 128 + lane * 4, r = o / 32, c = (o % 32) / 4;
@@ -2354,6 +2377,7 @@ bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, void *dw, in
     p.G = g.G;
     p.accumulate = acc;
     p.dwt = dw_code(dw_t);
+    p.nnz = h->nnz;
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat<BS, FA, BF16>;
     static std::atomic<int> attr_set{-1};
@@ -2441,6 +2465,7 @@ bsmm_status launch_up_dense(bsmm_ctx *h, UpDenseSched &us, const GroupPtrs &g, v
     p.G = g.G;
     p.accumulate = acc;
     p.dwt = dw_code(dw_t);
+    p.nnz = h->nnz;
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat_dense<FA, BF16>;
     static std::atomic<int> attr_set{-1};
@@ -2481,6 +2506,7 @@ bsmm_status launch_up_pair(bsmm_ctx *h, UpPairSched &us, const GroupPtrs &g, voi
     p.G = g.G;
     p.accumulate = acc;
     p.dwt = dw_code(dw_t);
+    p.nnz = h->nnz;
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat_pair<FA, BF16>;
     static std::atomic<int> attr_set{-1};

@@ -399,6 +399,43 @@ def test_updat_pair_tail_split(monkeypatch, fa):
     assert rel_fro(outs["dense"], o.updat(L, bs, x, dy, fa)) <= TOL_DW["bf16"]
 
 
+@pytest.mark.parametrize("variant,bs,fa", [("stack", 32, 1), ("stack", 16, 0), ("stack", 8, 1),
+                                            ("dense1", 32, 0), ("dense", 32, 1)])
+def test_updat_refuses_an_out_of_range_block_id(monkeypatch, variant, bs, fa):
+    """Fault injection on the host: a test hook makes the weight-gradient table name block
+    nnz + 5.  The epilogue checks every block id before its store, skips that block and records
+    BSMM_ERR_BOUNDS.  dW sits at the start of a larger buffer, so an unchecked store would land
+    in the guard blocks after it (inside the allocation): they must keep their sentinel, every
+    other block must match the oracle, and the next call on a fresh table is correct again."""
+    monkeypatch.setenv("BSMM_TC_UPDAT", variant)
+    R, S, N = 10, 13, 136
+    L = rand_layout(R, S, 0.5, 41 + bs)
+    L[0, 0] = 1
+    nnz = int(L.sum())
+    x = wk.normals(wk.act_shape(R * bs, N, fa), 950 + bs, 1.0, "bf16")
+    dy = wk.normals(wk.act_shape(S * bs, N, fa), 960 + bs, 1.0, "bf16")
+    ref = o.updat(L, bs, x, dy, fa)
+    monkeypatch.setenv("BSMM_UP_TEST_BAD_ID", "1")
+    m = make(L, bs, fa, "auto")
+    buf = torch.full((nnz + 8, bs, bs), 7.0, device="cuda")
+    m.updat(x.cuda(), dy.cuda(), dw=buf[:nnz])
+    with pytest.raises(bsmm.BsmmError) as e:
+        m.sync_status()
+    assert e.value.code == bsmm.ERR_BOUNDS
+    got = cpu64(buf)
+    m.close()
+    assert np.all(got[nnz:] == 7.0)
+    err = np.abs(got[:nnz] - ref).max(axis=(1, 2))
+    off = np.flatnonzero(err > 1e-3 * (np.abs(ref).max() + 1.0))
+    assert len(off) <= 1                         # only the block whose id was replaced
+    assert all(np.all(got[b] == 7.0) for b in off)
+    monkeypatch.delenv("BSMM_UP_TEST_BAD_ID")
+    m = make(L, bs, fa, "auto")
+    dw = m.updat(x.cuda(), dy.cuda())
+    m.sync_status()
+    assert rel_fro(cpu64(dw), ref) <= TOL_DW["bf16"]
+
+
 @pytest.mark.parametrize("fa,dtype", [(1, "bf16"), (0, "f16")])
 @pytest.mark.parametrize("R,S,p,N", [(10, 13, 0.5, 392), (7, 9, 0.9, 264), (12, 6, 0.3, 136),
                                      (20, 37, 0.5, 520), (10, 13, 0.5, 64), (9, 7, 0.8, 40)])
