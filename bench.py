@@ -486,28 +486,88 @@ def cold_times(fn, flush, reps):
     return statistics.median(a.elapsed_time(b) for a, b in evs) * 1000.0
 
 
+def stream_times(fn, nsets, launches):
+    """Device microseconds per launch of fn(i) launched `launches` times back to back on one
+    stream (programmatic dependent launch lets each launch overlap the previous one's tail),
+    rotating over nsets input/output sets whose total exceeds twice the L2, so every launch
+    reads cold inputs.  Queued behind a device sleep that outlasts the host's enqueue time."""
+    for i in range(nsets):
+        fn(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(launches):
+        fn(i % nsets)
+    host_s = (time.perf_counter() - t0) / launches
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(host_s * 1.5 * launches * 2.1e9) + 200000)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(launches):
+        fn(i % nsets)
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1000.0 / launches
+
+
+def config_sets(wl, m, inp, dev, min_bytes=300 << 20, max_sets=32):
+    """Copies of a configuration's inputs and outputs on the device, enough of them that their
+    total exceeds min_bytes (more than twice the 129 MB L2)."""
+    def one():
+        d = {"x": inp.x.to(dev), "w": inp.w.to(dev), "dy": inp.dy.to(dev)}
+        d["y"] = torch.empty(m.o_shape(wl.N), dtype=d["x"].dtype, device=dev)
+        d["dx"] = torch.empty(m.i_shape(wl.N), dtype=d["x"].dtype, device=dev)
+        d["dw"] = torch.zeros(m.w_shape, dtype=torch.float32, device=dev)
+        if wl.steps > 1:
+            d["xs"] = [a.to(dev) for a in inp.xs]
+            d["dys"] = [a.to(dev) for a in inp.dys]
+        return d
+    sets = [one()]
+    per = sum(t.numel() * t.element_size() for v in sets[0].values() for t in (v if isinstance(v, list) else [v]))
+    n = min(max_sets, max(2, -(-min_bytes // per)))
+    sets += [one() for _ in range(n - 1)]
+    return sets
+
+
+def launch_floor(dev, flush, reps):
+    """Fixed cost of a launch, timed the two ways the passes are: an empty kernel of 192 CTAs
+    alone between events after the L2 sweep, and back to back; with and without a
+    tensor-memory allocation (a kernel that contains tcgen05 instructions costs more to launch)."""
+    from block_sparse_matrix_gb300 import bsmm
+    h = bsmm.bsmm_create(np.ones((1, 1), np.uint8), 32, 1)
+    try:
+        out = {}
+        for key, tm in (("tensor_memory_kernel", True), ("plain_kernel", False)):
+            fn = lambda i=0: bsmm.bsmm_selftest_empty_launch(h, 192, tm)
+            out[key] = {"alone_us": round(cold_times(fn, flush, reps), 3),
+                        "stream_us": round(stream_times(fn, 1, 200), 3)}
+        bsmm.bsmm_sync_status(h)
+    finally:
+        bsmm.bsmm_destroy(h)
+    return out
+
+
 def run_configs(dev, peaks, reps):
     """Each benchmark configuration on its own: every pass timed alone with CUDA events, cold
-    (a 256 MB read-only sweep evicts the L2 before each timed launch), median over reps."""
+    (a 256 MB read-only sweep evicts the L2 before each timed launch), median over reps; and
+    the same pass launched back to back over rotating input sets larger than the L2."""
     from block_sparse_matrix_gb300 import bsmm
     flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
     out = {}
     for name, wl in wk.CONFIGS.items():
         inp = wk.make_inputs(wl, steps=min(wl.steps, wl.group) if wl.steps > 1 else None)
         m = bsmm.BlocksparseMatMul(inp.layout, block_size=wl.bs, feature_axis=wl.feature_axis)
-        x, w, dy = inp.x.to(dev), inp.w.to(dev), inp.dy.to(dev)
-        y = torch.empty(m.o_shape(wl.N), dtype=x.dtype, device=dev)
-        dx = torch.empty(m.i_shape(wl.N), dtype=x.dtype, device=dev)
-        dw = torch.zeros(m.w_shape, dtype=torch.float32, device=dev)
-        calls = {"fprop": lambda: m.fprop(x, w, y), "bprop": lambda: m.bprop(dy, w, dx),
-                 "updat": lambda: m.updat(x, dy, dw)}
+        sets = config_sets(wl, m, inp, dev)
+        calls = {"fprop": lambda i: m.fprop(sets[i]["x"], sets[i]["w"], sets[i]["y"]),
+                 "bprop": lambda i: m.bprop(sets[i]["dy"], sets[i]["w"], sets[i]["dx"]),
+                 "updat": lambda i: m.updat(sets[i]["x"], sets[i]["dy"], sets[i]["dw"])}
         if wl.steps > 1:
-            xs = [a.to(dev) for a in inp.xs]
-            dys = [a.to(dev) for a in inp.dys]
-            calls["updat_grouped_g%d" % wl.group] = lambda: m.updat_grouped(xs, dys, dw=dw, accumulate=True)
+            calls["updat_grouped_g%d" % wl.group] = lambda i: m.updat_grouped(
+                sets[i]["xs"], sets[i]["dys"], dw=sets[i]["dw"], accumulate=True)
         res = {}
         for pname, flops, byts in config_passes(wl, m.nnz):
-            us = cold_times(calls[pname], flush, reps)
+            fn = calls[pname]
+            us = cold_times(lambda: fn(0), flush, reps)
+            us_stream = stream_times(fn, len(sets), max(40, 4 * len(sets)))
             if wl.dtype == "f32":
                 t_c, bound_c = flops / (FFMA_TFLOPS * 1e12), "alu"
             else:
@@ -516,17 +576,22 @@ def run_configs(dev, peaks, reps):
             tr = max(t_c, t_m)
             res[pname] = {"us": round(us, 3), "tflops": round(flops / (us * 1e-6) / 1e12, 2),
                           "roofline_us": round(tr * 1e6, 3), "bound": bound_c if t_c >= t_m else "hbm",
-                          "roofline_frac": round(tr / (us * 1e-6), 4)}
+                          "roofline_frac": round(tr / (us * 1e-6), 4),
+                          "us_stream": round(us_stream, 3), "roofline_frac_stream": round(tr / (us_stream * 1e-6), 4)}
         m.sync_status()
         out[name] = {"shape": "C=%d K=%d bs=%d density=%s N=%d %s fa=%d nnz=%d%s" % (
             wl.C, wl.K, wl.bs, wl.density, wl.N, wl.dtype, wl.feature_axis, m.nnz,
             (" steps=%d group=%d" % (wl.steps, wl.group)) if wl.steps > 1 else ""), "passes": res}
         m.close()
-        del x, w, dy, y, dx, dw
+        del sets
+    out["_launch_floor_us"] = launch_floor(dev, flush, reps)
     del flush
-    out["_timing"] = ("each pass alone between CUDA events on the launching stream, median of %d, after a "
+    out["_timing"] = ("us: each pass alone between CUDA events on the launching stream, median of %d, after a "
                       "256 MB read-only sweep that evicts L2, queued behind a device sleep so host enqueue "
-                      "time is not counted; peaks: %s" % (
+                      "time is not counted; us_stream: the pass launched back to back on one stream over "
+                      "rotating input/output sets larger than twice the L2 (cold inputs), device time per "
+                      "launch; _launch_floor_us: an empty 192-CTA kernel timed both ways (the alone figure "
+                      "is part of every pass's us); peaks: %s" % (
                           reps, "tensor = MEASURED_PEAKS bf16_tflops (fp16 the same rate), hbm = hbm_gbs, "
                           "alu = derived fp32 FFMA peak %.1f TFLOP/s" % FFMA_TFLOPS))
     return out

@@ -58,6 +58,7 @@ def lib():
             "bsmm_set_kernel": [vp, i],
             "bsmm_sync_status": [vp, vp],
             "bsmm_selftest_wait_timeout": [vp, ctypes.c_uint64, vp],
+            "bsmm_selftest_empty_launch": [vp, ctypes.c_int, ctypes.c_int, vp],
             "bsmm_updat_noalloc": [vp, vp, vp, vp, i, i, i, vp],
             "bsmm_layer_norm": [vp, vp, vp, vp, i, i, i, ctypes.c_float, i, i, vp],
             "bsmm_layer_norm_grad": [vp, vp, vp, vp, vp, vp, vp, i, i, i, ctypes.c_float, i, i, vp,
@@ -214,6 +215,11 @@ def bsmm_sync_status(h, stream=None):
 
 def bsmm_selftest_wait_timeout(h, limit_ns: int, stream=None):
     _check(lib().bsmm_selftest_wait_timeout(h, int(limit_ns), _stream(stream)), "bsmm_selftest_wait_timeout")
+
+
+def bsmm_selftest_empty_launch(h, ctas: int, tensor_memory: bool, stream=None):
+    _check(lib().bsmm_selftest_empty_launch(h, int(ctas), int(bool(tensor_memory)), _stream(stream)),
+           "bsmm_selftest_empty_launch")
 
 
 # ---- README-style object -------------------------------------------------------------

@@ -284,4 +284,11 @@ bsmm_status bsmm_selftest_wait_timeout(bsmm_t h, uint64_t limit_ns, void *stream
     return launch_wait_selftest(h, limit_ns, (cudaStream_t)stream);
 }
 
+bsmm_status bsmm_selftest_empty_launch(bsmm_t h, int ctas, int tensor_memory, void *stream)
+{
+    if (!h || ctas < 1 || ctas > 65535) return BSMM_ERR_INVALID;
+    cudaSetDevice(h->device);
+    return launch_empty_selftest(h, ctas, tensor_memory != 0, (cudaStream_t)stream);
+}
+
 } // extern "C"

@@ -84,3 +84,4 @@ bsmm_status sp_fb(bsmm_ctx *h, bool bwd, const void *act, const void *w, void *o
                   cudaStream_t s);
 void sp_release(bsmm_ctx *h);
 bsmm_status launch_wait_selftest(bsmm_ctx *h, uint64_t limit_ns, cudaStream_t s);
+bsmm_status launch_empty_selftest(bsmm_ctx *h, int ctas, bool tensor_memory, cudaStream_t s);

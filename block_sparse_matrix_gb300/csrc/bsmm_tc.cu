@@ -2755,6 +2755,29 @@ __global__ void k_wait_selftest(int32_t *status, uint64_t limit_ns)
     if (threadIdx.x == 0) mbar_wait(&bar, 0, status, limit_ns);
 }
 
+// Launch-cost self-test: an empty kernel with the launch shape of the window kernel.  The
+// TENSOR_MEMORY form allocates and frees 32 columns per CTA; a kernel that contains tcgen05
+// instructions at all pays a larger fixed launch cost, which this form measures.
+template <bool TENSOR_MEMORY>
+__global__ void __launch_bounds__(kFbThreads, 1) k_empty_selftest(int32_t *status)
+{
+    __shared__ uint32_t tmem_base;
+    if (TENSOR_MEMORY) {
+        if (threadIdx.x < 32) tmem_alloc(&tmem_base, 32);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+    if (TENSOR_MEMORY) {
+        tc_fence_before();
+        __syncthreads();
+        if (threadIdx.x < 32) tmem_dealloc(tmem_base, 32);
+    }
+    (void)status;
+}
+
 } // namespace
 
 bsmm_status launch_wait_selftest(bsmm_ctx *h, uint64_t limit_ns, cudaStream_t s)
@@ -2762,6 +2785,15 @@ bsmm_status launch_wait_selftest(bsmm_ctx *h, uint64_t limit_ns, cudaStream_t s)
     k_wait_selftest<<<1, 32, 0, s>>>(h->d_status, limit_ns);
     g_bsmm_launches += 1;
     return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+}
+
+bsmm_status launch_empty_selftest(bsmm_ctx *h, int ctas, bool tensor_memory, cudaStream_t s)
+{
+    const cudaError_t le = tensor_memory
+                               ? launch_pdl(k_empty_selftest<true>, dim3(ctas), dim3(kFbThreads), 0, s, true, h->d_status)
+                               : launch_pdl(k_empty_selftest<false>, dim3(ctas), dim3(kFbThreads), 0, s, true, h->d_status);
+    g_bsmm_launches += 1;
+    return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
 bool tc_supported(bsmm_ctx *h, bsmm_dtype t)

@@ -312,6 +312,16 @@ int64_t bsmm_launch_count(void);
  */
 bsmm_status bsmm_selftest_wait_timeout(bsmm_t h, uint64_t limit_ns, void *stream);
 
+/*
+ * Launch-cost self-test (no counterpart in the README; computes nothing): enqueues on `stream`
+ * one empty kernel of `ctas` CTAs of 160 threads with the launch attributes of the library's
+ * kernels (programmatic dependent launch).  With tensor_memory != 0 one warp of each CTA
+ * allocates and frees 32 tensor-memory columns, as every tensor-core kernel does.  Timing it
+ * gives the fixed cost that every pass carries when launched alone.
+ * Errors: INVALID (null handle, ctas outside 1 .. 65535), CUDA.
+ */
+bsmm_status bsmm_selftest_empty_launch(bsmm_t h, int ctas, int tensor_memory, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,7 @@ def test_null_handle_rejected():
 def test_selftest_rejects_bad_arguments_on_host():
     L = bsmm.lib()
     assert L.bsmm_selftest_wait_timeout(None, 1000, None) == bsmm.ERR_INVALID
+    assert L.bsmm_selftest_empty_launch(None, 1, 1, None) == bsmm.ERR_INVALID
 
 
 def test_layer_norm_rejects_bad_arguments_on_host():
