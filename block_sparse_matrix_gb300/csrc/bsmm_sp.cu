@@ -326,6 +326,7 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
                 break;
             }
             tc_fence_after();
+            fence_proxy_async_smem();                           // cp.async (generic proxy) writes -> MMA reads
             const uint32_t slo = dlo + ((uint32_t)(st * g.stage_bytes) >> 4);
             const uint32_t blo = slo + ((uint32_t)g.b_off >> 4);
 #pragma unroll
