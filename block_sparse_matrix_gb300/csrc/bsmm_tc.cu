@@ -134,6 +134,20 @@ bool make_map2d(CUtensorMap *m, const void *base, bsmm_dtype t, uint64_t cols, u
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same over any element type (float32 dW for the weight-gradient epilogue).
+bool make_map2d_dt(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, uint64_t cols,
+                   uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * (uint64_t)esize};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 CUtensorMapSwizzle swz_for_row_bytes(int bytes)
 {
     return bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
@@ -933,6 +947,7 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
 struct UpMaps {
     CUtensorMap x[8];
     CUtensorMap dy[8];
+    CUtensorMap dw;             // [nnz * bs rows][bs] in dW's type, one block per box (TMA epilogue)
 };
 
 struct UpParams {
@@ -942,6 +957,7 @@ struct UpParams {
     int N, G, accumulate;
     int dwt;                    // 0: float32 dW, 1: fp16, 2: bf16
     int nnz;                    // blocks in dW: every table id is checked against it before a store
+    int tma;                    // 1: the epilogue writes dW blocks by TMA store (reduce-add to accumulate)
 };
 
 // True when block `id` lies inside dW; otherwise records BSMM_ERR_BOUNDS (sticky) and the
@@ -990,7 +1006,7 @@ template <int BSE, int FA> struct UpGeo {
     static constexpr int PANEL = TK * BSE * 2;                      // one stacked panel
     static constexpr int STAGES = 4;                                 // a multiple of kProducers
     static constexpr int TAB_OFF = STAGES * (A_BYTES + B_BYTES);
-    static constexpr int OUT_OFF = (TAB_OFF + kTableWords * 4 + 127) / 128 * 128;
+    static constexpr int OUT_OFF = (TAB_OFF + kTableWords * 4 + 1023) / 1024 * 1024;   // swizzled staging
     static constexpr int OUT_BYTES = 4 * 32 * 32 * 4;              // per epilogue warp: 32 rows of up to 32 fp32
     static constexpr int SMEM = OUT_OFF + OUT_BYTES;
     // fa=1: A MN-major (rows n, BSE features contiguous); fa=0: A K-major (rows = features, n contiguous).
@@ -1007,8 +1023,10 @@ template <int BSE, int FA> struct UpGeo {
 // Persistent weight-gradient kernel: each CTA walks its unit table; TMA loads stream
 // through the stage ring across unit boundaries; two TMEM accumulators let the epilogue of
 // one unit overlap the MMAs of the next.
+// Two CTAs share an SM: their 18 warps leave five on some SM sub-partitions, whose 16384 registers
+// then allow at most 102 per thread, so the kernel is held to 96.
 template <int BS, int FA, bool BF16>
-__global__ void __launch_bounds__(kUpThreads, 1)
+__global__ void __maxnreg__(96)
 k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
 {
     constexpr int BSE = BS == 8 ? 16 : BS;
@@ -1153,7 +1171,52 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
             const int32_t *ut = tab + 4 + u * kUnitWords;
-            if (!COARSE) {
+            if (!COARSE && p.tma) {
+                // The warp's 32 rows are 32 / BSE whole blocks.  Each lane writes its row into the
+                // warp's staging buffer in the layout of the dW tensor map (rows of ROWB bytes,
+                // 16-byte piece c of a row at c ^ (row address bits 7..), as TMA reads it), and
+                // lane 0 issues one TMA store per present block -- a reduce-add (float32 sum in
+                // L2, one rounding) when accumulating.  The buffer is rewritten only after the
+                // previous unit's stores have read it.
+                uint8_t *stg = reinterpret_cast<uint8_t *>(sout + q * 32 * 32);
+                const int eb = p.dwt == 0 ? 4 : 2, rowb = BS * eb;
+                const uint32_t ro = (uint32_t)(lane * rowb);
+                const uint32_t swm = rowb == 128 ? 7u : rowb == 64 ? 3u : 1u;
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
+                if (p.dwt == 0) {
+#pragma unroll
+                    for (int c = 0; c < BS / 4; ++c)
+                        *reinterpret_cast<float4 *>(stg + ro + ((c ^ ((ro >> 7) & swm)) << 4)) =
+                            make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BS / 8; ++c) {
+                        uint4 pk;
+                        const bool b16 = p.dwt == 2;
+                        pk.x = b16 ? pack2<true>(v[c * 8], v[c * 8 + 1]) : pack2<false>(v[c * 8], v[c * 8 + 1]);
+                        pk.y = b16 ? pack2<true>(v[c * 8 + 2], v[c * 8 + 3]) : pack2<false>(v[c * 8 + 2], v[c * 8 + 3]);
+                        pk.z = b16 ? pack2<true>(v[c * 8 + 4], v[c * 8 + 5]) : pack2<false>(v[c * 8 + 4], v[c * 8 + 5]);
+                        pk.w = b16 ? pack2<true>(v[c * 8 + 6], v[c * 8 + 7]) : pack2<false>(v[c * 8 + 6], v[c * 8 + 7]);
+                        *reinterpret_cast<uint4 *>(stg + ro + ((c ^ ((ro >> 7) & swm)) << 4)) = pk;
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && !aborted) {
+#pragma unroll
+                    for (int b = 0; b < 32 / BSE; ++b) {
+                        const int sl = q * (32 / BSE) + b;
+                        if (sl >= ut[1]) continue;
+                        const int32_t id = ut[2 + 5 * sl + 1];
+                        if (!up_id_ok(id, p)) continue;
+                        const uint8_t *src = stg + b * BS * rowb;
+                        if (p.accumulate) tma_reduce_add_2d(&maps.dw, src, 0, id * BS);
+                        else tma_store_2d(&maps.dw, src, 0, id * BS);
+                    }
+                    bulk_commit();
+                }
+            } else if (!COARSE) {
                 // The warp's 32 rows are 32 / BSE whole blocks, [row][BS] fp32 like the blocks in
                 // dw.  Pass them through shared memory so that each store instruction writes 512
                 // contiguous bytes of one block; 16-byte chunk c of row r sits at chunk
@@ -1193,6 +1256,7 @@ k_tc_updat(const __grid_constant__ UpMaps maps, const UpParams p)
                 }
             }
         }
+        if (p.tma && lane == 0) bulk_wait_all();        // every dW store has completed before the CTA exits
     }
     tc_fence_before();
     __syncthreads();
@@ -2378,6 +2442,20 @@ bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, void *dw, in
     p.accumulate = acc;
     p.dwt = dw_code(dw_t);
     p.nnz = h->nnz;
+    // bs 32 / 16: dW blocks leave by TMA stores, or TMA reduce-adds when accumulating a float32 dW
+    // (a 16-bit dW accumulates through registers: the sum is formed in float32, then rounded once);
+    // BSMM_UP_EPI=stores keeps the per-thread stores
+    const char *ue = getenv("BSMM_UP_EPI");
+    p.tma = BS != 8 && h->nnz > 0 && (p.dwt == 0 || !acc) && !(ue && !strcmp(ue, "stores")) ? 1 : 0;
+    if (p.tma) {
+        const int eb = p.dwt == 0 ? 4 : 2;
+        const CUtensorMapDataType dt = p.dwt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : p.dwt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        const int rowb = BS * eb;
+        const CUtensorMapSwizzle sw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : swz_for_row_bytes(rowb);
+        if (!make_map2d_dt(&maps.dw, dw, dt, eb, BS, (uint64_t)h->nnz * BS, BS, BS, sw)) return BSMM_ERR_CUDA;
+    }
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat<BS, FA, BF16>;
     static std::atomic<int> attr_set{-1};

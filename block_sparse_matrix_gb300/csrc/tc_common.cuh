@@ -155,7 +155,20 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *s
                  : "memory");
 }
 
+// TMA tensor reduce-add shared -> global: global += shared elementwise in the tensor map's type,
+// performed in L2; tracked by the bulk async-group of the issuing thread.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *m, const void *src, int32_t x, int32_t y)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until every committed bulk store of this thread has completed (its writes are done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Wait until the shared-memory source of this thread's committed bulk stores may be reused.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

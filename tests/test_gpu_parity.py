@@ -399,6 +399,38 @@ def test_updat_pair_tail_split(monkeypatch, fa):
     assert rel_fro(outs["dense"], o.updat(L, bs, x, dy, fa)) <= TOL_DW["bf16"]
 
 
+@pytest.mark.parametrize("bs,fa", [(32, 1), (32, 0), (16, 1), (16, 0), (8, 1)])
+@pytest.mark.parametrize("N,G", [(64, 1), (136, 3), (8, 1)])
+def test_updat_epilogue_forms_bit_identical(monkeypatch, bs, fa, N, G):
+    """The stacked weight-gradient kernel writes dW blocks either by TMA (store, or reduce-add in L2
+    when accumulating) from a swizzled staging tile, or by per-thread stores: the same float32 sums,
+    the same single rounding, so the same bits -- float32 dW written and accumulated, a bf16 dW
+    written -- and the oracle within tolerance."""
+    monkeypatch.setenv("BSMM_TC_UPDAT", "stack")
+    R, S = 11, 9
+    L = rand_layout(R, S, 0.45, 90 + bs + N)
+    L[0, 0] = 1
+    xs = [wk.normals(wk.act_shape(R * bs, N, fa), 300 + t + N, 1.0, "bf16") for t in range(G)]
+    dys = [wk.normals(wk.act_shape(S * bs, N, fa), 400 + t + N, 1.0, "bf16") for t in range(G)]
+    xg, dyg = [a.cuda() for a in xs], [a.cuda() for a in dys]
+    outs = {}
+    for form in ("tma", "stores"):
+        monkeypatch.setenv("BSMM_UP_EPI", form)
+        m = make(L, bs, fa, "auto")
+        dw = m.updat_grouped(xg, dyg)
+        dw_first = dw.clone()
+        m.updat_grouped(xg, dyg, dw=dw, accumulate=True)
+        dwh = m.updat(xg[0], dyg[0], dw_dtype=torch.bfloat16)
+        m.sync_status()
+        outs[form] = (dw_first, dw, dwh)
+    for a, b in zip(outs["tma"], outs["stores"]):
+        assert torch.equal(a, b)
+    ref = o.updat_grouped(L, bs, xs, dys, fa)
+    assert rel_fro(cpu64(outs["tma"][0]), ref) <= TOL_DW["bf16"]
+    assert rel_fro(cpu64(outs["tma"][1]), 2 * ref) <= TOL_DW["bf16"]
+    assert rel_fro(cpu64(outs["tma"][2]), o.updat(L, bs, xs[0], dys[0], fa)) <= TIGHT["bf16"]
+
+
 @pytest.mark.parametrize("variant,bs,fa", [("stack", 32, 1), ("stack", 16, 0), ("stack", 8, 1),
                                             ("dense1", 32, 0), ("dense", 32, 1)])
 def test_updat_refuses_an_out_of_range_block_id(monkeypatch, variant, bs, fa):
