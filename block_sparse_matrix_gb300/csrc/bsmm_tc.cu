@@ -969,6 +969,7 @@ __device__ __forceinline__ bool up_id_ok(int32_t id, const UpParams &p)
     return false;
 }
 
+
 // Stores 4 consecutive dW values at element `off` in the output type; with accumulate, adds the
 // stored values in float32 first and rounds the sum once.
 __device__ __forceinline__ void up_store4(void *dw, size_t off, float4 v, int accumulate, int dwt)
@@ -997,6 +998,62 @@ __device__ __forceinline__ void up_store4(void *dw, size_t off, float4 v, int ac
     o.x = dwt == 2 ? pack2<true>(v.x, v.y) : pack2<false>(v.x, v.y);
     o.y = dwt == 2 ? pack2<true>(v.z, v.w) : pack2<false>(v.z, v.w);
     *reinterpret_cast<uint2 *>(d) = o;
+}
+
+// Writes one 32 x 32 dW block whose row `lane` this lane holds in v, through the warp's 4 KB
+// staging tile stg (1024-byte aligned).  With p.tma the rows go into stg in the layout of the dW
+// tensor map (16-byte piece c of row r at c ^ (r mod 8) for 128-byte float32 rows, at
+// c ^ ((r / 2) mod 4) for 64-byte 16-bit rows) and lane 0 issues one TMA store, or a TMA
+// reduce-add when accumulating (float32 sum in L2, one rounding); the tile is rewritten only after
+// the previous store has read it.  Otherwise the tile is read back so that each store
+// instruction writes 512 contiguous bytes.  Nothing is written when skip is set or id is out of range.
+__device__ __forceinline__ void up_block32_out(const CUtensorMap *dwm, const UpParams &p, float *stg, int lane,
+                                               int32_t id, const float (&v)[32], bool skip)
+{
+    if (p.tma) {
+        uint8_t *sb = reinterpret_cast<uint8_t *>(stg);
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+        if (p.dwt == 0) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float4 *>(sb + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                    make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
+        } else {
+            const bool b16 = p.dwt == 2;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint4 pk;
+                pk.x = b16 ? pack2<true>(v[c * 8], v[c * 8 + 1]) : pack2<false>(v[c * 8], v[c * 8 + 1]);
+                pk.y = b16 ? pack2<true>(v[c * 8 + 2], v[c * 8 + 3]) : pack2<false>(v[c * 8 + 2], v[c * 8 + 3]);
+                pk.z = b16 ? pack2<true>(v[c * 8 + 4], v[c * 8 + 5]) : pack2<false>(v[c * 8 + 4], v[c * 8 + 5]);
+                pk.w = b16 ? pack2<true>(v[c * 8 + 6], v[c * 8 + 7]) : pack2<false>(v[c * 8 + 6], v[c * 8 + 7]);
+                *reinterpret_cast<uint4 *>(sb + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = pk;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && !skip && up_id_ok(id, p)) {
+            if (p.accumulate) tma_reduce_add_2d(dwm, sb, 0, id * 32);
+            else tma_store_2d(dwm, sb, 0, id * 32);
+            bulk_commit();
+        }
+        return;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4 *>(stg + lane * 32 + ((c ^ (lane & 7)) * 4)) =
+            make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
+    __syncwarp();
+    if (!skip && up_id_ok(id, p)) {
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4) {
+            const int o = k4 * 128 + lane * 4, r = o / 32, c = (o % 32) / 4;
+            up_store4(p.dw, (size_t)id * 1024 + o, *reinterpret_cast<const float4 *>(stg + r * 32 + ((c ^ (r & 7)) * 4)),
+                      p.accumulate, p.dwt);
+        }
+    }
+    __syncwarp();                                   // reads done before the next block's writes
 }
 
 template <int BSE, int FA> struct UpGeo {
@@ -1276,7 +1333,7 @@ struct UpDenseGeo {
     static constexpr int B_BYTES = 256 * TK * 2;                     // 32 KB
     static constexpr int STAGES = 4;                                 // a multiple of kProducers
     static constexpr int TAB_OFF = STAGES * (A_BYTES + B_BYTES);
-    static constexpr int OUT_OFF = (TAB_OFF + kDTableWords * 4 + 127) / 128 * 128;
+    static constexpr int OUT_OFF = (TAB_OFF + kDTableWords * 4 + 1023) / 1024 * 1024;  // swizzled staging
     static constexpr int SMEM = OUT_OFF + 4 * 32 * 32 * 4;           // + a 32 x 32 fp32 block per epilogue warp
 };
 
@@ -1427,29 +1484,13 @@ k_tc_updat_dense(const __grid_constant__ UpMaps maps, const UpParams p)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) v[c0 + j] = __uint_as_float(r[j]);
                 }
-                // through shared memory so that each store writes 512 contiguous bytes of the block;
-                // 16-byte chunk c of row r sits at chunk c ^ (r mod 8) (conflict-free both ways)
-                float *stg = sout + q * 32 * 32;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<float4 *>(stg + lane * 32 + ((c ^ (lane & 7)) * 4)) =
-                        make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
-                __syncwarp();
-                if (!aborted && up_id_ok(id, p)) {
-#pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4) {
-                        const int o = k4 * 128 + lane * 4, r = o / 32, c = (o % 32) / 4;
-                        up_store4(p.dw, (size_t)id * 1024 + o,
-                                  *reinterpret_cast<const float4 *>(stg + r * 32 + ((c ^ (r & 7)) * 4)), p.accumulate,
-                                  p.dwt);
-                    }
-                }
-                __syncwarp();                                   // reads done before the next block's writes
+                up_block32_out(&maps.dw, p, sout + q * 32 * 32, lane, id, v, aborted != 0);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
+        if (p.tma && lane == 0) bulk_wait_all();        // every dW store has completed before the CTA exits
     }
     tc_fence_before();
     __syncthreads();
@@ -1474,7 +1515,7 @@ struct UpPairGeo {
     static constexpr int PROD = 3;                                   // producer warps; warp w owns stages w, w + 3
     static constexpr int STAGES = 6;
     static constexpr int TAB_OFF = STAGES * STAGE;
-    static constexpr int OUT_OFF = (TAB_OFF + kPTableWords * 4 + 127) / 128 * 128;
+    static constexpr int OUT_OFF = (TAB_OFF + kPTableWords * 4 + 1023) / 1024 * 1024;  // swizzled staging
     static constexpr int SMEM = OUT_OFF + 4 * 32 * 32 * 4;           // + a 32 x 32 fp32 block per epilogue warp
 };
 
@@ -1643,29 +1684,13 @@ k_tc_updat_pair(const __grid_constant__ UpMaps maps, const UpParams p)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) v[c0 + j] = __uint_as_float(r[j]);
                 }
-                // through shared memory so that each store writes 512 contiguous bytes of the block;
-                // 16-byte chunk c of row r sits at chunk c ^ (r mod 8) (conflict-free both ways)
-                float *stg = sout + q * 32 * 32;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<float4 *>(stg + lane * 32 + ((c ^ (lane & 7)) * 4)) =
-                        make_float4(v[c * 4], v[c * 4 + 1], v[c * 4 + 2], v[c * 4 + 3]);
-                __syncwarp();
-                if (!aborted && up_id_ok(id, p)) {
-#pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4) {
-                        const int o = k4 * 128 + lane * 4, r = o / 32, c = (o % 32) / 4;
-                        up_store4(p.dw, (size_t)id * 1024 + o,
-                                  *reinterpret_cast<const float4 *>(stg + r * 32 + ((c ^ (r & 7)) * 4)), p.accumulate,
-                                  p.dwt);
-                    }
-                }
-                __syncwarp();                                   // reads done before the next block's writes
+                up_block32_out(&maps.dw, p, sout + q * 32 * 32, lane, id, v, aborted != 0);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc_empty0 + (uint32_t)buf * 8u);
         }
+        if (p.tma && lane == 0) bulk_wait_all();        // every dW store has completed before the CTA exits
     }
     if (aborted) {
         // copies of the pair may still be landing in this CTA: give them time (bounded)
@@ -2413,6 +2438,24 @@ bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const FbStages &geo, const void 
 
 int dw_code(bsmm_dtype dw_t) { return dw_t == BSMM_F32 ? 0 : dw_t == BSMM_F16 ? 1 : 2; }
 
+// bs 32 / 16: the weight-gradient epilogues write dW blocks by TMA store, or TMA reduce-add when
+// accumulating a float32 dW (a 16-bit dW accumulates through registers: the sum is formed in
+// float32, then rounded once); sets p.tma and the dW tensor map (one block per box, rows swizzled
+// by their byte width).  BSMM_UP_EPI=stores keeps the per-thread stores.  p.dwt, p.accumulate set.
+bool set_dw_map(const bsmm_ctx *h, UpMaps &maps, UpParams &p, void *dw, int BS)
+{
+    const char *ue = getenv("BSMM_UP_EPI");
+    p.tma = BS != 8 && h->nnz > 0 && (p.dwt == 0 || !p.accumulate) && !(ue && !strcmp(ue, "stores")) ? 1 : 0;
+    if (!p.tma) return true;
+    const int eb = p.dwt == 0 ? 4 : 2;
+    const CUtensorMapDataType dt = p.dwt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : p.dwt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int rowb = BS * eb;
+    const CUtensorMapSwizzle sw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : swz_for_row_bytes(rowb);
+    return make_map2d_dt(&maps.dw, dw, dt, eb, BS, (uint64_t)h->nnz * BS, BS, BS, sw);
+}
+
 template <int BS, int FA, bool BF16>
 bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, void *dw, int N, bsmm_dtype t, int acc,
                       cudaStream_t s, bsmm_dtype dw_t = BSMM_F32, bool pdl = true)
@@ -2442,20 +2485,7 @@ bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, void *dw, in
     p.accumulate = acc;
     p.dwt = dw_code(dw_t);
     p.nnz = h->nnz;
-    // bs 32 / 16: dW blocks leave by TMA stores, or TMA reduce-adds when accumulating a float32 dW
-    // (a 16-bit dW accumulates through registers: the sum is formed in float32, then rounded once);
-    // BSMM_UP_EPI=stores keeps the per-thread stores
-    const char *ue = getenv("BSMM_UP_EPI");
-    p.tma = BS != 8 && h->nnz > 0 && (p.dwt == 0 || !acc) && !(ue && !strcmp(ue, "stores")) ? 1 : 0;
-    if (p.tma) {
-        const int eb = p.dwt == 0 ? 4 : 2;
-        const CUtensorMapDataType dt = p.dwt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                       : p.dwt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-        const int rowb = BS * eb;
-        const CUtensorMapSwizzle sw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : swz_for_row_bytes(rowb);
-        if (!make_map2d_dt(&maps.dw, dw, dt, eb, BS, (uint64_t)h->nnz * BS, BS, BS, sw)) return BSMM_ERR_CUDA;
-    }
+    if (!set_dw_map(h, maps, p, dw, BS)) return BSMM_ERR_CUDA;
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat<BS, FA, BF16>;
     static std::atomic<int> attr_set{-1};
@@ -2544,6 +2574,7 @@ bsmm_status launch_up_dense(bsmm_ctx *h, UpDenseSched &us, const GroupPtrs &g, v
     p.accumulate = acc;
     p.dwt = dw_code(dw_t);
     p.nnz = h->nnz;
+    if (!set_dw_map(h, maps, p, dw, 32)) return BSMM_ERR_CUDA;
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat_dense<FA, BF16>;
     static std::atomic<int> attr_set{-1};
@@ -2585,6 +2616,7 @@ bsmm_status launch_up_pair(bsmm_ctx *h, UpPairSched &us, const GroupPtrs &g, voi
     p.accumulate = acc;
     p.dwt = dw_code(dw_t);
     p.nnz = h->nnz;
+    if (!set_dw_map(h, maps, p, dw, 32)) return BSMM_ERR_CUDA;
     const int smem = G::SMEM + 1024;
     auto kern = k_tc_updat_pair<FA, BF16>;
     static std::atomic<int> attr_set{-1};

@@ -399,14 +399,16 @@ def test_updat_pair_tail_split(monkeypatch, fa):
     assert rel_fro(outs["dense"], o.updat(L, bs, x, dy, fa)) <= TOL_DW["bf16"]
 
 
-@pytest.mark.parametrize("bs,fa", [(32, 1), (32, 0), (16, 1), (16, 0), (8, 1)])
+@pytest.mark.parametrize("variant,bs,fa", [("stack", 32, 1), ("stack", 32, 0), ("stack", 16, 1), ("stack", 16, 0),
+                                            ("stack", 8, 1), ("dense1", 32, 1), ("dense1", 32, 0), ("dense", 32, 1),
+                                            ("dense", 32, 0)])
 @pytest.mark.parametrize("N,G", [(64, 1), (136, 3), (8, 1)])
-def test_updat_epilogue_forms_bit_identical(monkeypatch, bs, fa, N, G):
-    """The stacked weight-gradient kernel writes dW blocks either by TMA (store, or reduce-add in L2
-    when accumulating) from a swizzled staging tile, or by per-thread stores: the same float32 sums,
-    the same single rounding, so the same bits -- float32 dW written and accumulated, a bf16 dW
-    written -- and the oracle within tolerance."""
-    monkeypatch.setenv("BSMM_TC_UPDAT", "stack")
+def test_updat_epilogue_forms_bit_identical(monkeypatch, variant, bs, fa, N, G):
+    """The weight-gradient kernels (stacked, dense one-CTA, CTA pair) write dW blocks either by TMA
+    (store, or reduce-add in L2 when accumulating) from a swizzled staging tile, or by per-thread
+    stores: the same float32 sums, the same single rounding, so the same bits -- float32 dW written
+    and accumulated, a bf16 dW written -- and the oracle within tolerance."""
+    monkeypatch.setenv("BSMM_TC_UPDAT", variant)
     R, S = 11, 9
     L = rand_layout(R, S, 0.45, 90 + bs + N)
     L[0, 0] = 1
