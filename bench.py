@@ -528,6 +528,50 @@ def config_sets(wl, m, inp, dev, min_bytes=300 << 20, max_sets=32):
     return sets
 
 
+def recurrent_layer(wl, dev, flush, reps):
+    """The recurrent layer's training pass as a user runs it: `steps` timesteps of fprop and bprop
+    through one weight, then the weight gradient of all steps in groups of `group` accumulated into
+    one float32 dW -- launched eagerly on one stream, and captured once in a CUDA graph and
+    replayed.  Device microseconds per layer (median over reps, each after the L2 sweep, queued
+    behind a device sleep), with effective TFLOP/s."""
+    from block_sparse_matrix_gb300 import bsmm
+    inp = wk.make_inputs(wl)
+    m = bsmm.BlocksparseMatMul(inp.layout, block_size=wl.bs, feature_axis=wl.feature_axis)
+    T, G, N = wl.steps, wl.group, wl.N
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        w = inp.w.to(dev)
+        xs = [a.to(dev) for a in inp.xs]
+        dys = [a.to(dev) for a in inp.dys]
+        ys = [torch.empty(m.o_shape(N), dtype=w.dtype, device=dev) for _ in range(T)]
+        dxs = [torch.empty(m.i_shape(N), dtype=w.dtype, device=dev) for _ in range(T)]
+        dw = torch.empty(m.w_shape, dtype=torch.float32, device=dev)
+
+        def layer():
+            for t in range(T):
+                m.fprop(xs[t], w, ys[t])
+                m.bprop(dys[t], w, dxs[t])
+            for g0 in range(0, T, G):
+                m.updat_grouped(xs[g0:g0 + G], dys[g0:g0 + G], dw=dw, accumulate=g0 > 0)
+
+        layer()
+        eager = cold_times(layer, flush, reps)
+        g = torch.cuda.CUDAGraph()
+    s.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        layer()
+    with torch.cuda.stream(s):
+        graph = cold_times(g.replay, flush, reps)
+    s.synchronize()
+    m.sync_status()
+    f = 2 * T * wk.effective_flops(N, m.nnz, wl.bs) + T * wk.effective_flops(N, m.nnz, wl.bs)
+    m.close()
+    return {"what": "%d steps of fprop and bprop, then the grouped weight gradient (groups of %d) into "
+                    "float32 dW; %d launches" % (T, G, 2 * T + (T + G - 1) // G),
+            "eager_us": round(eager, 3), "graph_us": round(graph, 3),
+            "tflops_eager": round(f / (eager * 1e-6) / 1e12, 2), "tflops_graph": round(f / (graph * 1e-6) / 1e12, 2)}
+
+
 def launch_floor(dev, flush, reps):
     """Fixed cost of a launch, timed the two ways the passes are: an empty kernel of 192 CTAs
     alone between events after the L2 sweep, and back to back; with and without a
@@ -584,6 +628,8 @@ def run_configs(dev, peaks, reps):
             (" steps=%d group=%d" % (wl.steps, wl.group)) if wl.steps > 1 else ""), "passes": res}
         m.close()
         del sets
+        if wl.steps > 1:
+            out[name]["layer"] = recurrent_layer(wl, dev, flush, reps)
     out["_launch_floor_us"] = launch_floor(dev, flush, reps)
     del flush
     out["_timing"] = ("us: each pass alone between CUDA events on the launching stream, median of %d, after a "
