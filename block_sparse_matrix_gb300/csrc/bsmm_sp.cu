@@ -85,7 +85,7 @@ struct SpParams {
     const void *w;
     void *out;
     const uint32_t *stream;
-    const int32_t *off, *len, *order;
+    const int4 *desc;           // per (launch position, part): window, stream offset, length
     int32_t *status;
     int N, Fin, Fout, Fsrc, Fslots, ntiles;
     int64_t nnz;
@@ -152,10 +152,10 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
     const int split = g.split;
     const int part = split > 1 ? (int)cluster_ctarank() : 0;
     const int unit = blockIdx.x / split;
-    const int win = p.order[unit / p.ntiles];
+    const int4 desc = __ldg(p.desc + (unit / p.ntiles) * split + part);
+    const int win = desc.x;
     const int tile = unit % p.ntiles;
     const int n0 = tile * 128;
-    const int sidx = win * split + part;
 
     if (g.stages < kSpProducers || g.stages > kSpMaxStages || g.stages % kSpProducers != 0 || g.W < 1 ||
         g.W > 32 || g.W * BSE > 512 || g.E < 1 || g.E > 8 || g.R < 1 || g.R > 32) {
@@ -183,9 +183,9 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
     // that waits for it in tcgen05.alloc waits only on CTAs that will finish.
     pdl_launch_dependents();
     if (warp == 0 && lane == 0) {
-        const int len = p.len[sidx];
+        const int len = desc.z;
         mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
-        bulk_load(sched, p.stream + p.off[sidx], (uint32_t)len * 4u, &sched_full, policy_evict_last());
+        bulk_load(sched, p.stream + desc.y, (uint32_t)len * 4u, &sched_full, policy_evict_last());
     }
     pdl_wait();
     const bool sched_ok = mbar_wait_warp(&sched_full, 0, p.status, 64);
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(256) k_sp_panelize(const uint16_t *act, uint16
 struct SpSched {
     int W = 0, split = 1, E = 0, R = 0, nwin = 0;
     uint32_t *d_stream = nullptr;
-    int32_t *d_off = nullptr, *d_len = nullptr, *d_order = nullptr;
+    int4 *d_desc = nullptr;     // per (launch position, part): window, stream offset, length, 0
     int max_words = 0;
     bool built = false;
 };
@@ -744,8 +744,13 @@ bool sp_build(const bsmm_ctx *h, bool bwd, int W, int split, int E, int R, SpSch
     sc.R = R;
     sc.nwin = nwin;
     sc.max_words = longest;
-    if (!sp_upload(&sc.d_stream, stream) || !sp_upload(&sc.d_off, off) || !sp_upload(&sc.d_len, len) ||
-        !sp_upload(&sc.d_order, order))
+    std::vector<int4> desc((size_t)nwin * split);
+    for (int j = 0; j < nwin; ++j)
+        for (int pt = 0; pt < split; ++pt) {
+            const int w = order[j];
+            desc[(size_t)j * split + pt] = make_int4(w, off[w * split + pt], len[w * split + pt], 0);
+        }
+    if (!sp_upload(&sc.d_stream, stream) || !sp_upload(&sc.d_desc, desc))
         return false;
     sc.built = true;
     return true;
@@ -837,9 +842,7 @@ bool sp_plan(const bsmm_ctx *h, bool bwd, int ntiles, SpSched &out)
         int smem;
         if (!sp_geometry(h, sc, g, smem)) {
             cudaFree(sc.d_stream);
-            cudaFree(sc.d_off);
-            cudaFree(sc.d_len);
-            cudaFree(sc.d_order);
+            cudaFree(sc.d_desc);
             continue;
         }
         out = sc;
@@ -896,9 +899,7 @@ bsmm_status sp_launch_kernel(bsmm_ctx *h, const SpSched &sc, const void *act, co
     p.w = w;
     p.out = out;
     p.stream = sc.d_stream;
-    p.off = sc.d_off;
-    p.len = sc.d_len;
-    p.order = sc.d_order;
+    p.desc = sc.d_desc;
     p.status = h->d_status;
     p.N = N;
     p.Fin = (BWD ? h->S : h->R) * h->bs;
@@ -1002,9 +1003,7 @@ void sp_release(bsmm_ctx *h)
     SpState *st = static_cast<SpState *>(h->sp);
     for (auto &kv : st->plans) {
         cudaFree(kv.second.d_stream);
-        cudaFree(kv.second.d_off);
-        cudaFree(kv.second.d_len);
-        cudaFree(kv.second.d_order);
+        cudaFree(kv.second.d_desc);
     }
     for (auto &kv : st->scratch) cudaFree(kv.second.ptr);
     delete st;

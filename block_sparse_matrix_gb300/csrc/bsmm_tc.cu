@@ -65,10 +65,10 @@ struct FbSched {
     int Fslots = 0;                 // output blocks (coarse) of the pass
     int max_words = 0;              // longest window stream
     uint32_t *d_stream = nullptr;
-    int32_t *d_win_off = nullptr;   // nwin: word offset of each window stream
-    int32_t *d_win_len = nullptr;   // nwin: padded length in words
-    int32_t *d_win_order = nullptr; // nwin: windows by decreasing work
-    uint32_t *d_win_mask = nullptr; // nwin: slots that receive at least one block
+    // nwin descriptors in launch order (windows by decreasing work): window, word offset of its
+    // stream, padded length in words, slots that receive at least one block -- one 16-byte load
+    // gives a CTA everything it needs before the stream's bulk copy
+    int4 *d_win_desc = nullptr;
     bool built = false;
     bool too_big = false;           // a window stream exceeds the shared-memory budget
 };
@@ -291,9 +291,12 @@ bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W, int e_max, int r_max, i
     fs.nwin = nwin;
     fs.Fslots = Fslots;
     fs.max_words = longest;
-    if (!upload(&fs.d_stream, stream) || !upload(&fs.d_win_off, off) || !upload(&fs.d_win_len, len) ||
-        !upload(&fs.d_win_order, order) || !upload(&fs.d_win_mask, mask))
-        return false;
+    std::vector<int4> desc(nwin);
+    for (int j = 0; j < nwin; ++j) {
+        const int w = order[j];
+        desc[j] = make_int4(w, off[w], len[w], (int)mask[w]);
+    }
+    if (!upload(&fs.d_stream, stream) || !upload(&fs.d_win_desc, desc)) return false;
     fs.built = true;
     return true;
 }
@@ -681,8 +684,7 @@ struct FbStages {
 struct FbParams {
     void *out;
     const uint32_t *stream;
-    const int32_t *win_off, *win_len, *win_order;
-    const uint32_t *win_mask;
+    const int4 *win_desc;       // per launch position: window, stream offset, length, slot mask
     int32_t *status;
     int N;          // minibatch
     int Fout;       // output features (C for bprop, K for fprop)
@@ -727,7 +729,8 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     const int unit = blockIdx.x;
-    const int win = p.win_order[unit / p.n_tiles];
+    const int4 desc = __ldg(p.win_desc + unit / p.n_tiles);
+    const int win = desc.x;
     const int n0 = (unit % p.n_tiles) * 128;
     const int ncols = p.W * BSE;
     const uint32_t alloc_cols = ncols <= 32 ? 32 : ncols <= 64 ? 64 : ncols <= 128 ? 128 : 256;
@@ -752,9 +755,9 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
     pdl_launch_dependents();
     // The window schedule belongs to the handle: fetch it before waiting for the previous kernel.
     if (warp == 0 && lane == 0) {
-        const int len = p.win_len[win];
+        const int len = desc.z;
         mbar_arrive_expect_tx(&sched_full, (uint32_t)len * 4u);
-        if (len > 0) bulk_load((void *)sched, p.stream + p.win_off[win], (uint32_t)len * 4u, &sched_full, policy_evict_last());
+        if (len > 0) bulk_load((void *)sched, p.stream + desc.y, (uint32_t)len * 4u, &sched_full, policy_evict_last());
         prefetch_tmap(&tm_act);
         prefetch_tmap(&tm_w);
     }
@@ -889,7 +892,7 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
         const int n = n0 + row;
         const bool ok = mbar_wait_warp(&acc_full, 0, p.status, 256);
         tc_fence_after();
-        const uint32_t mask = p.win_mask[win];
+        const uint32_t mask = (uint32_t)desc.w;
         uint16_t *out = static_cast<uint16_t *>(p.out);
         for (int s = 0; s < p.W; ++s) {
             const int o = win * p.W + s;
@@ -2411,10 +2414,7 @@ bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const FbStages &geo, const void 
     FbParams p;
     p.out = out;
     p.stream = fs.d_stream;
-    p.win_off = fs.d_win_off;
-    p.win_len = fs.d_win_len;
-    p.win_order = fs.d_win_order;
-    p.win_mask = fs.d_win_mask;
+    p.win_desc = fs.d_win_desc;
     p.status = h->d_status;
     p.N = N;
     p.Fout = Fout;
@@ -3014,10 +3014,7 @@ void tc_release(bsmm_ctx *h)
     for (auto &kv : st->fb) {
         FbSched &f = kv.second;
         cudaFree(f.d_stream);
-        cudaFree(f.d_win_off);
-        cudaFree(f.d_win_len);
-        cudaFree(f.d_win_order);
-        cudaFree(f.d_win_mask);
+        cudaFree(f.d_win_desc);
     }
     cudaFree(st->up.d_table);
     if (st->upd) {
