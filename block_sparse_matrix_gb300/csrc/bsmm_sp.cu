@@ -484,22 +484,36 @@ __global__ void __launch_bounds__(kSpThreads, 1) k_tc_sp(const SpParams p)
 // (F, N) activations -> contiguous panels: pan[tile][source][panel], each panel 128 rows x BSE
 // features in the K-major operand layout, chunk (row r, 8 features h) at
 // (r / 8) * BSE * 16 + h * 128 + (r % 8) * 16 bytes.  Rows >= N and features >= Fin are zero.
-// A CTA transposes 64 features x 128 rows through shared memory.
+// A CTA transposes 64 features x 128 rows through shared memory, holding each pair of feature
+// rows interleaved as 32-bit words t[pair][sample] (padded rows), so that an output chunk -- 8
+// features of one sample -- is four 32-bit reads without bank conflicts.
 template <int BSE>
 __global__ void __launch_bounds__(256) k_sp_panelize(const uint16_t *act, uint16_t *pan, int N, int Fin, int Fsrc)
 {
-    __shared__ __align__(16) uint16_t t[64][128];
+    constexpr int LD = 128 + 4;                        // words per padded row of t
+    __shared__ __align__(16) uint32_t t[32][LD];       // t[p][n]: features f0 + 2p, f0 + 2p + 1 of sample n0 + n
     const int tile = blockIdx.x, f0 = blockIdx.y * 64, n0 = tile * 128;
     pdl_launch_dependents();
     pdl_wait();
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int c = k * 256 + threadIdx.x;           // 16-byte chunk: feature row fr, columns 8cc..
-        const int fr = c >> 4, cc = c & 15;
-        const int f = f0 + fr, nn = n0 + cc * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (f < Fin && nn < N) v = *reinterpret_cast<const uint4 *>(act + (size_t)f * N + nn);
-        *reinterpret_cast<uint4 *>(&t[fr][cc * 8]) = v;
+    for (int k = 0; k < 2; ++k) {
+        const int c = k * 256 + threadIdx.x;           // feature pair p, 8 samples from 8 cc
+        const int p = c >> 4, cc = c & 15;
+        const int f = f0 + 2 * p, nn = n0 + cc * 8;
+        uint4 va = make_uint4(0, 0, 0, 0), vb = va;
+        if (nn < N) {
+            if (f < Fin) va = *reinterpret_cast<const uint4 *>(act + (size_t)f * N + nn);
+            if (f + 1 < Fin) vb = *reinterpret_cast<const uint4 *>(act + (size_t)(f + 1) * N + nn);
+        }
+        const uint32_t a4[4] = {va.x, va.y, va.z, va.w}, b4[4] = {vb.x, vb.y, vb.z, vb.w};
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {                  // samples 2j, 2j + 1: low halves of a, b, then high
+            w[2 * j] = (a4[j] & 0xFFFFu) | (b4[j] << 16);
+            w[2 * j + 1] = (a4[j] >> 16) | (b4[j] & 0xFFFF0000u);
+        }
+        *reinterpret_cast<uint4 *>(&t[p][cc * 8]) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4 *>(&t[p][cc * 8 + 4]) = make_uint4(w[4], w[5], w[6], w[7]);
     }
     __syncthreads();
     constexpr int CPR = BSE / 8;
@@ -510,12 +524,9 @@ __global__ void __launch_bounds__(256) k_sp_panelize(const uint16_t *act, uint16
         const int r = rg * 8 + r8;
         const int s = f0 / BSE + pi;
         if (s >= Fsrc) continue;
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            w[i] = (uint32_t)t[pi * BSE + h * 8 + 2 * i][r] | ((uint32_t)t[pi * BSE + h * 8 + 2 * i + 1][r] << 16);
+        const int p0 = (pi * BSE + h * 8) / 2;         // pairs p0 .. p0 + 3: features h*8 .. h*8 + 7
         uint16_t *dst = pan + ((size_t)tile * Fsrc + s) * (128 * BSE) + rg * (BSE * 8) + h * 64 + r8 * 8;
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(t[p0][r], t[p0 + 1][r], t[p0 + 2][r], t[p0 + 3][r]);
     }
 }
 
