@@ -101,6 +101,17 @@ def normals(shape, seed: int, std: float = 1.0, dtype: str = "f32") -> torch.Ten
     return torch.from_numpy(a).to(DTYPES[dtype])
 
 
+def device_normals(shape, seed: int, std: float = 1.0, dtype: str = "f32", device="cuda") -> torch.Tensor:
+    """N(0, std^2) draws made on the device by torch's seeded CUDA generator (for inputs of several
+    GB, where host generation and upload would dominate), in `dtype`.  Deterministic per seed."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(DTYPES[dtype])
+
+
 def small_ints(shape, seed: int, dtype: str = "f32", lo: int = -1, hi: int = 1) -> torch.Tensor:
     """Integers uniform in [lo, hi] (exactly representable in every dtype here)."""
     rng = np.random.default_rng(seed)
