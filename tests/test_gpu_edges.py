@@ -143,3 +143,44 @@ def test_activations_past_2_31_elements():
         got = cpu64(dw[b][torch.from_numpy(i_idx).cuda(), torch.from_numpy(j_idx).cuda()])
         assert rel_fro(got, ref) <= 2e-3
     m.close()
+
+
+def test_activations_past_2_31_elements_cn_bs16():
+    """The same maximum sizes for (C, N) activations at block size 16 -- the sparse-window kernel
+    with its panel transpose (whose scratch also exceeds 2^31 elements) and the stacked weight
+    gradient: C = K = 8192, a 10 % layout, N = 2^18 + 200 samples (4.3 GB per activation tensor)."""
+    R = S = 512
+    bs, N, fa = 16, (1 << 18) + 200, 0
+    C = K = R * bs
+    assert N * C > 2 ** 31
+    L = rand_layout(R, S, 0.1, 32)
+    L[0, 0] = L[-1, -1] = 1
+    m = BlocksparseMatMul(L, block_size=bs, feature_axis=fa)
+    x = wk.device_normals((C, N), 4, 1.0, "f16")
+    dy = wk.device_normals((K, N), 5, 1.0, "f16")
+    w = wk.device_normals(m.w_shape, 6, float(1 / np.sqrt(R * bs * 0.1)), "f16")
+    y = m.fprop(x, w)
+    dx = m.bprop(dy, w)
+    dw = m.updat(x, dy)
+    m.sync_status()
+    rng = np.random.default_rng(8)
+    n_idx = np.concatenate([rng.integers(2 ** 31 // C, N, 48), rng.integers(0, N, 16), [N - 1]])
+    f_idx = rng.integers(0, C, len(n_idx))
+    f_idx[-1] = C - 1
+    cols = torch.from_numpy(n_idx).cuda()
+    fi = torch.from_numpy(f_idx).cuda()
+    loc = np.arange(len(n_idx))
+    wc = w.cpu()
+    ref_y = o.fprop_at(L, bs, wc, x[:, cols].cpu(), fa, loc, f_idx)
+    ref_dx = o.bprop_at(L, bs, wc, dy[:, cols].cpu(), fa, loc, f_idx)
+    assert rel_fro(cpu64(y[fi, cols]), ref_y) <= TIGHT["f16"]
+    assert rel_fro(cpu64(dx[fi, cols]), ref_dx) <= TIGHT["f16"]
+    for b in (0, m.nnz // 2, m.nnz - 1):
+        c, k = m.block_coord(b)
+        i_idx, j_idx = rng.integers(0, bs, 24), rng.integers(0, bs, 24)
+        xs = x[c * bs:(c + 1) * bs].cpu()
+        dys = dy[k * bs:(k + 1) * bs].cpu()
+        ref = o.updat_at(np.ones((1, 1), np.uint8), bs, xs, dys, fa, np.zeros(24, np.int64), i_idx, j_idx)
+        got = cpu64(dw[b][torch.from_numpy(i_idx).cuda(), torch.from_numpy(j_idx).cuda()])
+        assert rel_fro(got, ref) <= 2e-3               # 262344 products per element, as above
+    m.close()
