@@ -10,6 +10,7 @@
 // updat  (gradient w.r.t. W, dw_dtype):  dw[b] = sum_t x_t[:, c_b blk]^T . dy_t[:, k_b blk]
 //        (t over the G <= 8 timesteps of group_param_grads; G = 1 for a plain updat)
 #include "bsmm_internal.cuh"
+#include "tc_common.cuh"
 
 namespace {
 
@@ -43,74 +44,112 @@ __device__ __forceinline__ void out_coord(int idx, int &n, int &j)
 }
 
 // BWD=false: fprop over the column LUT.  BWD=true: bprop over the row LUT.
-// The operands of entry e + 1 (weight block and input panel) are loaded into registers while
-// entry e is multiplied out of shared memory, so each entry costs one compute phase instead of a
-// memory round trip followed by it.
-template <typename T, int BS, int FA, bool BWD, int TN>
-__global__ void __launch_bounds__(kThreads)
+// A CTA walks its LUT entries D at a time.  The schedule (LUT entries: fixed once the handle
+// exists) is read before the wait on the previous kernel; the D weight blocks and input panels of
+// a group are then loaded into registers together, so a group costs one memory round trip, and
+// the next group's loads are in flight while the current group is multiplied out of shared memory.
+// Panel rows have a 16-byte pitch, so a thread reads four reduction terms with one vector load.
+// Every output sums its entries in LUT order and each entry's terms in increasing index order.
+template <typename T, int BS, int FA, bool BWD, int TN, int D>
+__global__ void __launch_bounds__(kThreads, 1)
 k_simt_fwd_bwd(const T *__restrict__ in, const T *__restrict__ w, T *__restrict__ out,
                const int32_t *__restrict__ ptr, const int32_t *__restrict__ ent,
                int N, int Fin, int Fout)
 {
     constexpr int OUT = TN * BS / kThreads;
-    constexpr int NW = (BS * BS + kThreads - 1) / kThreads;   // weight elements per thread
-    constexpr int NA = TN * BS / kThreads;                     // panel elements per thread
-    __shared__ float sw[BS][BS + 1];
-    __shared__ float sa[TN][BS + 1];
+    constexpr int NW = (BS * BS + kThreads - 1) / kThreads;   // weight elements per thread and entry
+    constexpr int NA = TN * BS / kThreads;                     // panel elements per thread and entry
+    constexpr int PA = BS + 4;                                 // panel row pitch (floats)
+    __shared__ float sw[D][BS][BS + 1];
+    __shared__ __align__(16) float sa[D][TN][PA];
+    tc::pdl_launch_dependents();        // holds no tensor memory: the next kernel may start
     const int tid = threadIdx.x;
     const int blk = blockIdx.x;         // output block column (fprop) / row (bprop)
     const int n0 = blockIdx.y * TN;
+    const int e0 = ptr[blk], e1 = ptr[blk + 1];
+
+    int bid[D], src[D];                 // weight block id and source block index of each entry
+    auto sched = [&](int e) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+            bid[d] = 0;
+            src[d] = 0;
+            if (e + d < e1) {
+                if (BWD) { bid[d] = e + d; src[d] = ent[e + d]; }
+                else     { bid[d] = ent[2 * (e + d)]; src[d] = ent[2 * (e + d) + 1]; }
+            }
+        }
+    };
+    float rw[D][NW], ra[D][NA];
+    auto load = [&](int e) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+            const bool live = e + d < e1;
+            const T *wb = w + (size_t)bid[d] * BS * BS;
+#pragma unroll
+            for (int k = 0; k < NW; ++k) {
+                const int q = tid + k * kThreads;
+                rw[d][k] = live && q < BS * BS ? to_f<T>(wb[q]) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < NA; ++k) {
+                const int q = tid + k * kThreads;
+                int n, i;
+                if (FA) { n = q / BS; i = q % BS; }
+                else    { i = q / TN; n = q % TN; }
+                ra[d][k] = live && n0 + n < N
+                               ? to_f<T>(in[aidx<FA>(n0 + n, (int64_t)src[d] * BS + i, N, Fin)]) : 0.f;
+            }
+        }
+    };
+
     float acc[OUT];
 #pragma unroll
     for (int r = 0; r < OUT; ++r) acc[r] = 0.f;
 
-    const int e0 = ptr[blk], e1 = ptr[blk + 1];
-    float rw[NW], ra[NA];
-    auto load = [&](int e) {
-        int b, src;                     // weight block id, source block index of the input panel
-        if (BWD) { b = e; src = ent[e]; }
-        else     { b = ent[2 * e]; src = ent[2 * e + 1]; }
-        const T *wb = w + (size_t)b * BS * BS;
-#pragma unroll
-        for (int k = 0; k < NW; ++k) {
-            const int q = tid + k * kThreads;
-            rw[k] = q < BS * BS ? to_f<T>(wb[q]) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < NA; ++k) {
-            const int q = tid + k * kThreads;
-            int n, i;
-            if (FA) { n = q / BS; i = q % BS; }
-            else    { i = q / TN; n = q % TN; }
-            ra[k] = n0 + n < N ? to_f<T>(in[aidx<FA>(n0 + n, (int64_t)src * BS + i, N, Fin)]) : 0.f;
-        }
-    };
+    sched(e0);
+    tc::pdl_wait();                     // the previous kernel's writes (in, w, out) are settled
     if (e0 < e1) load(e0);
-    for (int e = e0; e < e1; ++e) {
+    for (int e = e0; e < e1; e += D) {
 #pragma unroll
-        for (int k = 0; k < NW; ++k) {
-            const int q = tid + k * kThreads;
-            if (q < BS * BS) sw[q / BS][q % BS] = rw[k];
-        }
+        for (int d = 0; d < D; ++d) {
 #pragma unroll
-        for (int k = 0; k < NA; ++k) {
-            const int q = tid + k * kThreads;
-            int n, i;
-            if (FA) { n = q / BS; i = q % BS; }
-            else    { i = q / TN; n = q % TN; }
-            sa[n][i] = ra[k];
+            for (int k = 0; k < NW; ++k) {
+                const int q = tid + k * kThreads;
+                if (q < BS * BS) sw[d][q / BS][q % BS] = rw[d][k];
+            }
+#pragma unroll
+            for (int k = 0; k < NA; ++k) {
+                const int q = tid + k * kThreads;
+                int n, i;
+                if (FA) { n = q / BS; i = q % BS; }
+                else    { i = q / TN; n = q % TN; }
+                sa[d][n][i] = ra[d][k];
+            }
         }
         __syncthreads();
-        if (e + 1 < e1) load(e + 1);    // in flight during the multiply below
+        if (e + D < e1) {               // the next group, in flight during the multiply below
+            sched(e + D);
+            load(e + D);
+        }
 #pragma unroll
-        for (int r = 0; r < OUT; ++r) {
-            int n, j;
-            out_coord<BS, FA, TN>(tid + kThreads * r, n, j);
-            float s = acc[r];
+        for (int d = 0; d < D; ++d) {
+            if (e + d >= e1) break;     // uniform over the CTA
 #pragma unroll
-            for (int i = 0; i < BS; ++i)
-                s = fmaf(sa[n][i], BWD ? sw[j][i] : sw[i][j], s);
-            acc[r] = s;
+            for (int i = 0; i < BS; i += 4) {
+#pragma unroll
+                for (int r = 0; r < OUT; ++r) {
+                    int n, j;
+                    out_coord<BS, FA, TN>(tid + kThreads * r, n, j);
+                    const float4 a = *reinterpret_cast<const float4 *>(&sa[d][n][i]);
+                    float s = acc[r];
+                    s = fmaf(a.x, BWD ? sw[d][j][i + 0] : sw[d][i + 0][j], s);
+                    s = fmaf(a.y, BWD ? sw[d][j][i + 1] : sw[d][i + 1][j], s);
+                    s = fmaf(a.z, BWD ? sw[d][j][i + 2] : sw[d][i + 2][j], s);
+                    s = fmaf(a.w, BWD ? sw[d][j][i + 3] : sw[d][i + 3][j], s);
+                    acc[r] = s;
+                }
+            }
         }
         __syncthreads();
     }
@@ -124,7 +163,9 @@ k_simt_fwd_bwd(const T *__restrict__ in, const T *__restrict__ w, T *__restrict_
 
 // Weight gradient, one CTA per block.  Outputs (i, j) are spread over the
 // threads; for bs=8 the 64 outputs are replicated over 4 thread groups that
-// split the minibatch and are summed at the end.
+// split the minibatch and are summed at the end.  For bs=32 a thread owns four
+// consecutive i of one j, so one vector read of x serves four outputs.  Every
+// output sums over the timesteps and the minibatch in increasing order.
 template <typename T, typename TD, int BS, int FA>
 __global__ void __launch_bounds__(kThreads)
 k_simt_updat(GroupPtrs g, TD *__restrict__ dw, const int32_t *__restrict__ coord,
@@ -133,16 +174,28 @@ k_simt_updat(GroupPtrs g, TD *__restrict__ dw, const int32_t *__restrict__ coord
     constexpr int NOUT = BS * BS;
     constexpr int OUT = NOUT >= kThreads ? NOUT / kThreads : 1;
     constexpr int SPLIT = NOUT >= kThreads ? 1 : kThreads / NOUT;
-    __shared__ float sx[kTN][BS + 1];
+    constexpr bool QUAD = OUT % 4 == 0;
+    constexpr int PX = BS + 4;                   // x row pitch (floats): rows start on 16 bytes
+    __shared__ __align__(16) float sx[kTN][PX];
     __shared__ float sd[kTN][BS + 1];
     __shared__ float red[SPLIT > 1 ? kThreads : 1];
+    tc::pdl_launch_dependents();                 // holds no tensor memory: the next kernel may start
     const int tid = threadIdx.x;
     const int64_t b = blockIdx.x;
     const int c = coord[2 * b], k = coord[2 * b + 1];
     const int part = SPLIT > 1 ? tid / NOUT : 0;   // minibatch split index
+    int oi[OUT], oj[OUT];
+#pragma unroll
+    for (int r = 0; r < OUT; ++r) {
+        const int o = QUAD ? (tid / BS) * OUT * BS + r * BS + tid % BS
+                           : (SPLIT > 1 ? tid % NOUT : tid + kThreads * r);
+        oi[r] = o / BS;
+        oj[r] = o % BS;
+    }
     float acc[OUT];
 #pragma unroll
     for (int r = 0; r < OUT; ++r) acc[r] = 0.f;
+    tc::pdl_wait();                              // the previous kernel's writes (x, dy, dw) are settled
 
     for (int t = 0; t < g.G; ++t) {
         const T *x = (const T *)g.x[t];
@@ -161,13 +214,27 @@ k_simt_updat(GroupPtrs g, TD *__restrict__ dw, const int32_t *__restrict__ coord
                 sd[n][i] = vd;
             }
             __syncthreads();
+            if (QUAD) {
+                const int i0 = oi[0], j = oj[0];
+#pragma unroll 4
+                for (int n = 0; n < kTN; ++n) {
+                    const float d = sd[n][j];
 #pragma unroll
-            for (int r = 0; r < OUT; ++r) {
-                int o = (SPLIT > 1 ? tid % NOUT : tid + kThreads * r);
-                int i = o / BS, j = o % BS;
-                float s = acc[r];
-                for (int n = part; n < kTN; n += SPLIT) s = fmaf(sx[n][i], sd[n][j], s);
-                acc[r] = s;
+                    for (int r = 0; r < OUT; r += 4) {
+                        const float4 a = *reinterpret_cast<const float4 *>(&sx[n][i0 + r]);
+                        acc[r + 0] = fmaf(a.x, d, acc[r + 0]);
+                        acc[r + 1] = fmaf(a.y, d, acc[r + 1]);
+                        acc[r + 2] = fmaf(a.z, d, acc[r + 2]);
+                        acc[r + 3] = fmaf(a.w, d, acc[r + 3]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < OUT; ++r) {
+                    float s = acc[r];
+                    for (int n = part; n < kTN; n += SPLIT) s = fmaf(sx[n][oi[r]], sd[n][oj[r]], s);
+                    acc[r] = s;
+                }
             }
             __syncthreads();
         }
@@ -183,13 +250,58 @@ k_simt_updat(GroupPtrs g, TD *__restrict__ dw, const int32_t *__restrict__ coord
     }
 #pragma unroll
     for (int r = 0; r < OUT; ++r) {
-        int o = tid + kThreads * r;
-        if (o >= NOUT) break;
-        TD *p = dw + b * NOUT + o;
+        if (SPLIT > 1 && tid >= NOUT) break;
+        TD *p = dw + b * NOUT + oi[r] * BS + oj[r];
         float v = acc[r];
         if (accumulate) v += to_f<TD>(*p);
         *p = from_f<TD>(v);
     }
+}
+
+// Every SIMT pass launches with programmatic dependent launch: it reads its schedule while the
+// previous kernel on the stream finishes, and waits in pdl_wait() before touching activations,
+// weights or outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_simt(void (*kern)(KArgs...), dim3 grid, cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// LUT entries staged per group: as many as fit in 45 KB of static shared memory, at most 8 for
+// the short tiles (few CTAs: a block column should take one round trip) and 4 for 64-row tiles
+// (enough CTAs to hide the latency).
+template <int BS, int TN>
+constexpr int simt_group()
+{
+    return (45 * 1024) / ((BS * (BS + 1) + TN * (BS + 4)) * 4) >= (TN == kTN ? 4 : 8)
+               ? (TN == kTN ? 4 : 8)
+               : (45 * 1024) / ((BS * (BS + 1) + TN * (BS + 4)) * 4);
+}
+
+template <typename T, int BS, int TN>
+cudaError_t launch_fb(bsmm_ctx *h, dim3 grid, bool bwd, const T *in, const T *w, T *out, int N, int Fin, int Fout,
+                      cudaStream_t s)
+{
+    constexpr int D = simt_group<BS, TN>();
+    static_assert(D >= 1, "one LUT entry must fit in shared memory");
+    const int32_t *ptr = bwd ? h->d_row_ptr : h->d_col_ptr;
+    const int32_t *ent = bwd ? h->d_row_ent : h->d_col_ent;
+    if (h->fa) {
+        if (bwd) return launch_simt(k_simt_fwd_bwd<T, BS, 1, true, TN, D>, grid, s, in, w, out, ptr, ent, N, Fin, Fout);
+        return launch_simt(k_simt_fwd_bwd<T, BS, 1, false, TN, D>, grid, s, in, w, out, ptr, ent, N, Fin, Fout);
+    }
+    if (bwd) return launch_simt(k_simt_fwd_bwd<T, BS, 0, true, TN, D>, grid, s, in, w, out, ptr, ent, N, Fin, Fout);
+    return launch_simt(k_simt_fwd_bwd<T, BS, 0, false, TN, D>, grid, s, in, w, out, ptr, ent, N, Fin, Fout);
 }
 
 template <typename T, int BS>
@@ -202,24 +314,14 @@ bsmm_status fwd_bwd_bs(bsmm_ctx *h, const void *in, const void *w, void *out, in
     const bool small = (int64_t)blocks * ((N + kTN - 1) / kTN) < h->sm_count;
     constexpr int TNS = kThreads / BS;
     dim3 grid(blocks, small ? (N + TNS - 1) / TNS : (N + kTN - 1) / kTN);
-    const int32_t *ptr = bwd ? h->d_row_ptr : h->d_col_ptr;
-    const int32_t *ent = bwd ? h->d_row_ent : h->d_col_ent;
-    int Fin = bwd ? K : C, Fout = bwd ? C : K;
+    const int Fin = bwd ? K : C, Fout = bwd ? C : K;
     const T *i_ = (const T *)in;
     const T *w_ = (const T *)w;
     T *o_ = (T *)out;
-#define SIMT_FB(TN_)                                                                                     \
-    if (h->fa) {                                                                                         \
-        if (bwd) k_simt_fwd_bwd<T, BS, 1, true, TN_><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout); \
-        else     k_simt_fwd_bwd<T, BS, 1, false, TN_><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout); \
-    } else {                                                                                             \
-        if (bwd) k_simt_fwd_bwd<T, BS, 0, true, TN_><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout); \
-        else     k_simt_fwd_bwd<T, BS, 0, false, TN_><<<grid, kThreads, 0, s>>>(i_, w_, o_, ptr, ent, N, Fin, Fout); \
-    }
-    if (small) { SIMT_FB(TNS) } else { SIMT_FB(kTN) }
-#undef SIMT_FB
+    const cudaError_t le = small ? launch_fb<T, BS, TNS>(h, grid, bwd, i_, w_, o_, N, Fin, Fout, s)
+                                 : launch_fb<T, BS, kTN>(h, grid, bwd, i_, w_, o_, N, Fin, Fout, s);
     g_bsmm_launches += 1;
-    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+    return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
 template <typename T>
@@ -244,11 +346,12 @@ template <typename T, typename TD, int BS>
 bsmm_status updat_bs(bsmm_ctx *h, const GroupPtrs &g, void *dw, int N, int acc, cudaStream_t s)
 {
     const int C = h->R * BS, K = h->S * BS;
-    dim3 grid((unsigned)h->nnz);
-    if (h->fa) k_simt_updat<T, TD, BS, 1><<<grid, kThreads, 0, s>>>(g, (TD *)dw, h->d_coord, N, C, K, acc);
-    else       k_simt_updat<T, TD, BS, 0><<<grid, kThreads, 0, s>>>(g, (TD *)dw, h->d_coord, N, C, K, acc);
+    const dim3 grid((unsigned)h->nnz);
+    const cudaError_t le =
+        h->fa ? launch_simt(k_simt_updat<T, TD, BS, 1>, grid, s, g, (TD *)dw, (const int32_t *)h->d_coord, N, C, K, acc)
+              : launch_simt(k_simt_updat<T, TD, BS, 0>, grid, s, g, (TD *)dw, (const int32_t *)h->d_coord, N, C, K, acc);
     g_bsmm_launches += 1;
-    return cudaGetLastError() == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
+    return le == cudaSuccess ? BSMM_OK : BSMM_ERR_CUDA;
 }
 
 template <typename T, typename TD>
