@@ -36,6 +36,8 @@ struct bsmm_ctx {
     void *sp = nullptr;        // sparse-window kernel plans and (F, N) panel scratch (bsmm_sp.cu)
     int tc_wlog = -1;   // fprop/bprop window size override (log2), from BSMM_TC_WLOG; -1 = automatic
     int tc_stage_kb = -1;  // fprop/bprop per-CTA stage budget override (KB), from BSMM_TC_STAGE_KB
+    int tc_rows = -1;      // window-kernel minibatch tile height override (64 or 128), from BSMM_TC_ROWS
+    int tc_bins = -1;      // window kernel: 1 forces binned windows, 0 forbids them, from BSMM_TC_BINS
 };
 
 extern std::atomic<int64_t> g_bsmm_launches;

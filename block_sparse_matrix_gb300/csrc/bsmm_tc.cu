@@ -69,6 +69,9 @@ struct FbSched {
     // stream, padded length in words, slots that receive at least one block -- one 16-byte load
     // gives a CTA everything it needs before the stream's bulk copy
     int4 *d_win_desc = nullptr;
+    // binned windows only: nwin * W output blocks (slot s of window w at w * W + s, -1 = unused);
+    // null for windows of W consecutive output blocks
+    int32_t *d_win_out = nullptr;
     bool built = false;
     bool too_big = false;           // a window stream exceeds the shared-memory budget
 };
@@ -206,7 +209,7 @@ int choose_wlog(const bsmm_ctx *h, bool bwd, int n_tiles)
 // loads (a_ops per entry, b_ops per record), one per lane of the producer warp.  Sets
 // too_big when a window's stream would exceed max_words.
 bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W, int e_max, int r_max, int a_ops, int b_ops,
-              int max_words)
+              int max_words, const std::vector<std::vector<int>> *bins = nullptr)
 {
     if (e_max < 1 || r_max < 1 || a_ops + r_max * b_ops > 32) return false;
     const bool coarse = h->bs == 8;
@@ -216,7 +219,23 @@ bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W, int e_max, int r_max, i
     fb_shape(h, bwd, Fslots, Fsrc, bse);
     const int gc = fb_row_sources(h->fa, bse);         // source blocks per activation panel row
     W = std::min(W, Fslots);
-    const int nwin = (Fslots + W - 1) / W;
+    int nwin = (Fslots + W - 1) / W;
+    std::vector<int32_t> win_out;
+    if (bins) {
+        nwin = (int)bins->size();
+        W = 0;
+        for (const auto &b : *bins) W = std::max(W, (int)b.size());
+        if (W < 1 || W > 32) return false;
+        win_out.assign((size_t)nwin * W, -1);
+        for (int w = 0; w < nwin; ++w)
+            for (size_t sl = 0; sl < (*bins)[w].size(); ++sl) win_out[(size_t)w * W + sl] = (*bins)[w][sl];
+    }
+    // output block of slot sl in window w, or -1
+    auto slot_out = [&](int w, int sl) -> int {
+        if (bins) return win_out[(size_t)w * W + sl];
+        const int o = w * W + sl;
+        return o < Fslots ? o : -1;
+    };
     BidLookup bid{h};
 
     std::vector<uint32_t> stream, mask(nwin, 0);
@@ -236,8 +255,8 @@ bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W, int e_max, int r_max, i
                 const int src = grp * gc + sub;
                 if (src >= Fsrc) break;
                 for (int sl = 0; sl < W; ++sl) {
-                    const int o = w * W + sl;
-                    if (o >= Fslots) break;
+                    const int o = slot_out(w, sl);
+                    if (o < 0) continue;
                     const int cc = bwd ? o : src, kc = bwd ? src : o;   // coarse (c', k')
                     bool any = false;
                     for (int cs = 0; cs < f; ++cs)
@@ -297,6 +316,7 @@ bool build_fb(bsmm_ctx *h, FbSched &fs, bool bwd, int W, int e_max, int r_max, i
         desc[j] = make_int4(w, off[w], len[w], (int)mask[w]);
     }
     if (!upload(&fs.d_stream, stream) || !upload(&fs.d_win_desc, desc)) return false;
+    if (bins && !upload(&fs.d_win_out, win_out)) return false;
     fs.built = true;
     return true;
 }
@@ -676,7 +696,8 @@ constexpr int kSchedWords = 3072;                                    // window s
 // is 64 rows: the MMA still reads 128 rows, the upper 64 come from the next slot (or the
 // padding after the last stage) and only feed accumulator rows that are never stored.
 struct FbStages {
-    int e_slots, r_slots, stages, half;
+    int e_slots, r_slots, stages;
+    int half;           // 1: 64-row minibatch tiles (activation panels of 64 rows), else 128
     int a_slot, stage_bytes, b_off;
     int producers;      // producer warps (1, 2 or 4), a divisor of stages
 };
@@ -685,6 +706,7 @@ struct FbParams {
     void *out;
     const uint32_t *stream;
     const int4 *win_desc;       // per launch position: window, stream offset, length, slot mask
+    const int32_t *win_out;     // binned windows: output block of each slot (-1 = unused); else null
     int32_t *status;
     int N;          // minibatch
     int Fout;       // output features (C for bprop, K for fprop)
@@ -731,7 +753,8 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
     const int unit = blockIdx.x;
     const int4 desc = __ldg(p.win_desc + unit / p.n_tiles);
     const int win = desc.x;
-    const int n0 = (unit % p.n_tiles) * 128;
+    const int tile_rows = g.half ? 64 : 128;
+    const int n0 = (unit % p.n_tiles) * tile_rows;
     const int ncols = p.W * BSE;
     const uint32_t alloc_cols = ncols <= 32 ? 32 : ncols <= 64 ? 64 : ncols <= 128 ? 128 : 256;
 
@@ -889,14 +912,15 @@ k_tc_fb(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUte
         // ---------------- epilogue (producer warps 0..3, one TMEM lane quarter each) ----
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
-        const int n = n0 + row;
+        // rows past a 64-row tile hold products of the neighbouring shared memory: never stored
+        const int n = row < tile_rows ? n0 + row : p.N;
         const bool ok = mbar_wait_warp(&acc_full, 0, p.status, 256);
         tc_fence_after();
         const uint32_t mask = (uint32_t)desc.w;
         uint16_t *out = static_cast<uint16_t *>(p.out);
         for (int s = 0; s < p.W; ++s) {
-            const int o = win * p.W + s;
-            if (o >= p.Fslots) break;
+            const int o = p.win_out ? __ldg(p.win_out + win * p.W + s) : win * p.W + s;
+            if (o < 0 || o >= p.Fslots) continue;
             float v[BSE];
             if (ok && ((mask >> s) & 1u)) {
 #pragma unroll
@@ -2415,12 +2439,13 @@ bsmm_status launch_fb(bsmm_ctx *h, FbSched &fs, const FbStages &geo, const void 
     p.out = out;
     p.stream = fs.d_stream;
     p.win_desc = fs.d_win_desc;
+    p.win_out = fs.d_win_out;
     p.status = h->d_status;
     p.N = N;
     p.Fout = Fout;
     p.W = fs.W;
     p.Fslots = fs.Fslots;
-    p.n_tiles = (N + 127) / 128;
+    p.n_tiles = geo.half ? (N + 63) / 64 : (N + 127) / 128;
     p.g = geo;
     const int smem = geo.stages * geo.stage_bytes + geo.a_slot + kSchedWords * 4 + 1024;
     auto kern = k_tc_fb<BS, FA, BWD, BF16>;
@@ -2507,11 +2532,11 @@ bsmm_status launch_up(bsmm_ctx *h, UpSched &us, const GroupPtrs &g, void *dw, in
 // there are more units than SMs and two stages fit in half of shared memory (one CTA's
 // prologue and epilogue then overlap the other's main loop); otherwise one CTA takes most
 // of shared memory.
-FbStages choose_stages(const bsmm_ctx *h, int N, int64_t units, int W)
+FbStages choose_stages(const bsmm_ctx *h, int N, int64_t units, int W, bool rows64)
 {
     const int bse = h->bs == 8 ? 16 : h->bs;
     FbStages g;
-    g.half = N <= 64 ? 1 : 0;
+    g.half = (N <= 64 || rows64) ? 1 : 0;
     g.a_slot = (g.half ? 64 : 128) * (h->fa ? fb_row_bytes(bse) : bse * 2);
     const int b_slot = bse * bse * 2;
     const int a_ops = (h->fa || g.half) ? 1 : 2, b_ops = h->bs == 8 ? 4 : 1;
@@ -2803,14 +2828,87 @@ bsmm_status fbd_try(bsmm_ctx *h, const void *act, const void *w, void *out, int 
               : launch_fbd<0, BWD, false>(h, *fs, act, w, out, N, t, s);
 }
 
+// Work of output block o in a window pass: its source blocks (fine blocks for bs 8).
+int64_t fb_block_work(const bsmm_ctx *h, bool bwd, int o)
+{
+    const int f = h->bs == 8 ? 2 : 1;
+    int64_t w = 0;
+    for (int q = 0; q < f; ++q) {
+        const int fine = o * f + q;
+        if (bwd && fine < h->R) w += h->h_row_ptr[fine + 1] - h->h_row_ptr[fine];
+        if (!bwd && fine < h->S) w += h->h_col_ptr[fine + 1] - h->h_col_ptr[fine];
+    }
+    return w;
+}
+
+// Binned windows: output blocks dealt to one bin per SM (per minibatch tile), heaviest first,
+// each to the bin with the least work so far; a bin's blocks are its window's slots.  Used when
+// one-block windows give more CTAs than SMs but fewer than two per SM and the blocks' work is
+// uneven (the heaviest at least 1.5 x the mean): the heaviest blocks then run alone on an SM
+// with the deepest pipeline, and the light ones share bins instead of sharing those SMs.  With
+// even work (every block the same number of sources) two CTAs per SM measured faster.
+bool fb_binned(const bsmm_ctx *h, bool bwd, int n_tiles)
+{
+    if (h->tc_bins == 0) return false;
+    int Fslots, Fsrc, bse;
+    fb_shape(h, bwd, Fslots, Fsrc, bse);
+    const int nbins = std::max(1, h->sm_count / n_tiles);
+    if (Fslots <= nbins || (Fslots + nbins - 1) / nbins * bse > 256) return false;
+    if (h->tc_bins == 1) return true;
+    if (Fslots >= 2 * nbins) return false;
+    int64_t total = 0, most = 0;
+    for (int o = 0; o < Fslots; ++o) {
+        const int64_t w = fb_block_work(h, bwd, o);
+        total += w;
+        most = std::max(most, w);
+    }
+    return 2 * most * Fslots >= 3 * total;
+}
+
+std::vector<std::vector<int>> fb_bins(const bsmm_ctx *h, bool bwd, int n_tiles)
+{
+    int Fslots, Fsrc, bse;
+    fb_shape(h, bwd, Fslots, Fsrc, bse);
+    const int nbins = std::min(Fslots, std::max(1, h->sm_count / n_tiles));
+    const int wmax = std::min(256 / bse, 2 * ((Fslots + nbins - 1) / nbins));
+    std::vector<int64_t> work(Fslots, 0);
+    for (int o = 0; o < Fslots; ++o) work[o] = fb_block_work(h, bwd, o);
+    std::vector<int> idx(Fslots);
+    for (int o = 0; o < Fslots; ++o) idx[o] = o;
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return work[a] > work[b]; });
+    std::vector<std::vector<int>> bins(nbins);
+    std::vector<int64_t> load(nbins, 0);
+    for (int o : idx) {
+        int best = -1;
+        for (int b = 0; b < nbins; ++b)
+            if ((int)bins[b].size() < wmax && (best < 0 || load[b] < load[best])) best = b;
+        bins[best].push_back(o);
+        load[best] += work[o] + 2;
+    }
+    for (auto &b : bins) std::sort(b.begin(), b.end());
+    return bins;
+}
+
+// Window kernel tile height for N > 64: 64-row tiles halve each CTA's activation bytes and
+// double the units the hardware scheduler can balance over the SMs.
+bool fb_rows64(const bsmm_ctx *h, int N)
+{
+    if (h->tc_rows == 64) return true;
+    if (h->tc_rows == 128) return false;
+    (void)N;
+    return false;
+}
+
 template <bool BWD>
 bsmm_status fb_dispatch(bsmm_ctx *h, const void *act, const void *w, void *out, int N, bsmm_dtype t, cudaStream_t s)
 {
     TcState *st = state(h);
-    const int a_ops = (h->fa || N <= 64) ? 1 : 2, b_ops = h->bs == 8 ? 4 : 1;
+    const bool rows64 = N > 64 && fb_rows64(h, N);
+    const int a_ops = (h->fa || N <= 64 || rows64) ? 1 : 2, b_ops = h->bs == 8 ? 4 : 1;
     const int wl_max = h->bs == 32 ? 3 : 4;
-    const int n_tiles = (N + 127) / 128;
+    const int n_tiles = rows64 ? (N + 63) / 64 : (N + 127) / 128;
     int wl = h->tc_wlog >= 0 ? std::min(h->tc_wlog, wl_max) : choose_wlog(h, BWD, n_tiles);
+    bool binned = wl == 0 && fb_binned(h, BWD, n_tiles);
     FbSched *fs = nullptr;
     FbStages geo{};
     {
@@ -2823,17 +2921,30 @@ bsmm_status fb_dispatch(bsmm_ctx *h, const void *act, const void *w, void *out, 
         for (; wl >= 0; --wl) {
             int Fslots, Fsrc, bse;
             fb_shape(h, BWD, Fslots, Fsrc, bse);
-            const int W = std::min(1 << wl, Fslots);
-            geo = choose_stages(h, N, (int64_t)((Fslots + W - 1) / W) * n_tiles, W);
+            std::vector<std::vector<int>> bins;
+            if (binned) bins = fb_bins(h, BWD, n_tiles);
+            int W = std::min(1 << wl, Fslots), nwin = (Fslots + W - 1) / W;
+            if (binned) {
+                W = 0;
+                for (const auto &b : bins) W = std::max(W, (int)b.size());
+                nwin = (int)bins.size();
+            }
+            geo = choose_stages(h, N, (int64_t)nwin * n_tiles, W, rows64);
             const uint64_t key = (uint64_t)BWD | ((uint64_t)wl << 1) | ((uint64_t)geo.e_slots << 8) |
-                                 ((uint64_t)geo.r_slots << 16) | ((uint64_t)a_ops << 24);
+                                 ((uint64_t)geo.r_slots << 16) | ((uint64_t)a_ops << 24) |
+                                 ((uint64_t)binned << 32);
             FbSched &c = st->fb[key];
             if (!c.built && !c.too_big &&
-                !build_fb(h, c, BWD, 1 << wl, geo.e_slots, geo.r_slots, a_ops, b_ops, kSchedWords))
+                !build_fb(h, c, BWD, 1 << wl, geo.e_slots, geo.r_slots, a_ops, b_ops, kSchedWords,
+                          binned ? &bins : nullptr))
                 return BSMM_ERR_OOM;
             if (c.built) {
                 fs = &c;
                 break;
+            }
+            if (binned) {                      // a bin's stream is too long: plain windows instead
+                binned = false;
+                ++wl;
             }
         }
     }
@@ -3015,6 +3126,7 @@ void tc_release(bsmm_ctx *h)
         FbSched &f = kv.second;
         cudaFree(f.d_stream);
         cudaFree(f.d_win_desc);
+        cudaFree(f.d_win_out);
     }
     cudaFree(st->up.d_table);
     if (st->upd) {

@@ -313,22 +313,58 @@ def test_errors_reported():
 
 @pytest.mark.parametrize("bs,fa,dtype", [(32, 1, "bf16"), (16, 0, "f16"), (8, 0, "bf16"), (8, 1, "f16")])
 def test_window_sizes_bit_identical(monkeypatch, bs, fa, dtype):
-    """The tensor-core fprop/bprop split output blocks into windows; each output is
-    accumulated over its source blocks in the same order for every window size, so
-    every window size gives the same bits (and matches the oracle)."""
+    """The tensor-core fprop/bprop split output blocks into windows and the minibatch into
+    tiles of 128 or 64 rows; each output is accumulated over its source blocks in the same
+    order for every window size and tile height, so all give the same bits (and match the
+    oracle).  N = 200 leaves a ragged last tile either way."""
     L, x, w, dy, ref_y, ref_dx, _ = small_case(bs, fa, dtype)
     xc, wc, dyc = x.cuda(), w.cuda(), dy.cuda()
     outs = []
     monkeypatch.setenv("BSMM_TC_FB", "window")
-    for wlog in range(0, 5):
-        monkeypatch.setenv("BSMM_TC_WLOG", str(wlog))
-        m = make(L, bs, fa, "auto")
-        outs.append((m.fprop(xc, wc), m.bprop(dyc, wc)))
-        m.sync_status()
+    for rows in (128, 64):
+        monkeypatch.setenv("BSMM_TC_ROWS", str(rows))
+        for wlog in range(0, 5):
+            monkeypatch.setenv("BSMM_TC_WLOG", str(wlog))
+            m = make(L, bs, fa, "auto")
+            outs.append((m.fprop(xc, wc), m.bprop(dyc, wc)))
+            m.sync_status()
     for y, dx in outs[1:]:
         assert torch.equal(y, outs[0][0]) and torch.equal(dx, outs[0][1])
     assert rel_fro(cpu64(outs[0][0]), ref_y) <= TIGHT[dtype]
     assert rel_fro(cpu64(outs[0][1]), ref_dx) <= TIGHT[dtype]
+
+
+@pytest.mark.parametrize("bs,fa,dtype,R,N", [(32, 1, "bf16", 200, 136), (16, 0, "f16", 200, 200),
+                                             (8, 0, "bf16", 400, 136), (32, 0, "bf16", 170, 72)])
+def test_window_bins_bit_identical(monkeypatch, bs, fa, dtype, R, N):
+    """With more output blocks than SMs per minibatch tile, the window kernel may deal the blocks
+    to one bin per SM (heaviest first) and treat each bin as a window of arbitrary output blocks.
+    Every output still sums its sources in increasing order, so binned and plain one-block windows
+    give the same bits, and both match the oracle.  Columns and rows of 1 to ~30 blocks."""
+    L = rand_layout(R, R, 0.05, 900 + bs)
+    L[:, 5] = 0                                          # an empty output block column
+    L[7, :] = 0                                          # an empty input block row
+    L[:, 9] = 1                                          # a full block column
+    nnz = int(L.sum())
+    x = wk.normals(wk.act_shape(R * bs, N, fa), 61 + bs, 1.0, dtype)
+    dy = wk.normals(wk.act_shape(R * bs, N, fa), 62 + bs, 1.0, dtype)
+    w = wk.normals((nnz, bs, bs), 63 + bs, float(1 / np.sqrt(R * bs * 0.05)), dtype)
+    xc, wc, dyc = x.cuda(), w.cuda(), dy.cuda()
+    monkeypatch.setenv("BSMM_TC_FB", "window")
+    monkeypatch.setenv("BSMM_TC_WLOG", "0")
+    outs = []
+    for bins in ("0", "1"):
+        monkeypatch.setenv("BSMM_TC_BINS", bins)
+        m = make(L, bs, fa, "auto")
+        y = torch.full(m.o_shape(N), float("nan"), dtype=DT[dtype], device="cuda")
+        dx = torch.full(m.i_shape(N), float("nan"), dtype=DT[dtype], device="cuda")
+        m.fprop(xc, wc, y)
+        m.bprop(dyc, wc, dx)
+        m.sync_status()
+        outs.append((y, dx))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert rel_fro(cpu64(outs[1][0]), o.fprop(L, bs, x, w, fa)) <= TIGHT[dtype]
+    assert rel_fro(cpu64(outs[1][1]), o.bprop(L, bs, dy, w, fa)) <= TIGHT[dtype]
 
 
 def test_bounded_wait_times_out_and_context_survives():
