@@ -7,15 +7,22 @@ at minibatch N = 1024 and N = 64 (six passes).  The metric is effective
 TFLOP/s = 2 * N * nnz * bs^2 per pass, summed over the step, divided by the
 device time of the step.
 
+Streams: the minibatch-1024 and minibatch-64 problems are independent, so a step
+runs the three minibatch-64 passes on a second stream, forked from and joined
+back into the timing stream inside the step: they fill the SMs that the
+dense-tile kernels of the minibatch-1024 passes leave idle.
+
 Timing: W warm-up steps, then exactly K timed steps.  Four input/output sets
 (each ~83 MB, together > 2x the 129 MB L2) rotate between steps, so every step
-reads cold inputs.  Steps are enqueued in chunks behind a short device sleep so
-that the host never starves the GPU inside a chunk.  CUDA events on the
-launching stream bracket every step; the reported device time is the sum of
-the per-step event intervals (consecutive kernels of a step overlap their
-prologues under programmatic dependent launch).  A second pass over the same K
-steps brackets every kernel with events, which gives each kernel's own duration
-for the per-pass table and the roofline object.
+reads cold inputs.  Steps are enqueued in chunks of 50 behind a short device
+sleep so that the host never starves the GPU inside a chunk.  CUDA events on
+the timing stream bracket every chunk of back-to-back steps (an event between
+steps would keep a step's first kernel from overlapping the previous step's
+last one under programmatic dependent launch, which back-to-back training steps
+do); the reported device time is the sum of the chunk intervals, the sleeps
+outside them.  A second pass over the same K steps runs the passes on one
+stream and brackets every kernel with events, which gives each kernel's own
+duration for the per-pass table and the roofline object.
 
 With --gpus N under torchrun every rank holds its own minibatch rows (a global minibatch of N
 times as many rows, weak scaling) and the replicated weight; each weight gradient is summed over
@@ -240,11 +247,33 @@ def run_ours(args):
         if ws > 1 and name.startswith("updat"):
             dp.allreduce_dw(d["dw%s" % name.split("_n")[1]])
 
+    side = torch.cuda.Stream(device=dev)
+    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
+    big = [p for p in passes if p[1] == max(Ns)]
+    small = [p for p in passes if p[1] != max(Ns)]
+
     def step(i):
+        # The two minibatches are independent problems: the small one's passes (and their weight
+        # gradient all-reduce) run on the side stream, forked from and joined back into the
+        # current stream inside the step.
         d = sets[i % NSETS]
-        for p in passes:
-            launch_pass(p[0], d)
-            exchange(p[0], d)
+        cur = torch.cuda.current_stream()
+        if small and big:
+            ev_fork.record(cur)
+            side.wait_event(ev_fork)
+            with torch.cuda.stream(side):
+                for p in small:
+                    launch_pass(p[0], d)
+                    exchange(p[0], d)
+            for p in big:
+                launch_pass(p[0], d)
+                exchange(p[0], d)
+            ev_join.record(side)
+            cur.wait_event(ev_join)
+        else:
+            for p in passes:
+                launch_pass(p[0], d)
+                exchange(p[0], d)
 
     # Warm-up (W steps), then count our launches per step.
     warm = max(3, args.warmup)
@@ -270,27 +299,29 @@ def run_ours(args):
 
     def timed(per_pass):
         # Steps are queued in chunks behind a device sleep so the host never starves the GPU.
-        # The step events bracket whole steps only, so consecutive kernels of a step may overlap
-        # (programmatic dependent launch); the per-pass run brackets every kernel with events,
-        # which gives each kernel's own duration.
-        ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(K_steps)]
+        # Without per_pass, events bracket each chunk of back-to-back steps (streams as in a real
+        # training loop); with per_pass, the passes run on one stream and events bracket every
+        # kernel, which gives each kernel's own duration.
+        ev_chunk = []
         ev_pass = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in passes]
                    for _ in range(K_steps)] if per_pass else None
         for c0 in range(0, K_steps, chunk):
             torch.cuda._sleep(sleep_cycles)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
             for i in range(c0, min(K_steps, c0 + chunk)):
                 d = sets[i % NSETS]
-                ev_step[i][0].record(stream)
+                if not per_pass:
+                    step(i)
+                    continue
                 for j, p in enumerate(passes):
-                    if per_pass:
-                        ev_pass[i][j][0].record(stream)
+                    ev_pass[i][j][0].record(stream)
                     launch_pass(p[0], d)
-                    if per_pass:
-                        ev_pass[i][j][1].record(stream)
+                    ev_pass[i][j][1].record(stream)
                     exchange(p[0], d)
-                ev_step[i][1].record(stream)
-        return ev_step, ev_pass
+            b.record(stream)
+            ev_chunk.append((a, b))
+        return ev_chunk, ev_pass
 
     sampler = ClockSampler(local)
     if ws > 1:
@@ -299,7 +330,7 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.3)
     wall0 = time.perf_counter()
-    ev_step, _ = timed(False)
+    ev_chunk, _ = timed(False)
     torch.cuda.synchronize()
     wall1 = time.perf_counter()
     if ws > 1:
@@ -309,8 +340,7 @@ def run_ours(args):
     clocks = sampler.stop()
     m.sync_status()
 
-    step_ms = [a.elapsed_time(b) for a, b in ev_step]
-    dev_ms = sum(step_ms)
+    dev_ms = sum(a.elapsed_time(b) for a, b in ev_chunk)
     pass_us = {}
     for j, p in enumerate(passes):
         pass_us[p[0]] = 1000.0 * sum(ev_pass[i][j][0].elapsed_time(ev_pass[i][j][1]) for i in range(K_steps)) / K_steps
@@ -366,6 +396,9 @@ def run_ours(args):
                 "warmup": warm, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normals)",
                 "config": {"workload": WORKLOAD, "nnz": nnz, "l2": "4 rotating input/output sets, ~330 MB > 2x L2",
+                           "streams": "minibatch-64 passes on a second stream, forked and joined inside each step",
+                           "timing": "CUDA events around chunks of %d back-to-back steps; sleeps between chunks "
+                                     "are outside the timed intervals" % chunk,
                            "parallelism": ("data parallel over the minibatch: %d rows per GPU, weight gradients "
                                            "all-reduced over NCCL inside the step" % max(Ns)) if ws > 1
                            else "single GPU"},
