@@ -573,11 +573,14 @@ def config_sets(wl, m, inp, dev, min_bytes=300 << 20, max_sets=32):
 
 
 def recurrent_layer(wl, dev, flush, reps):
-    """The recurrent layer's training pass as a user runs it: `steps` timesteps of fprop and bprop
-    through one weight, then the weight gradient of all steps in groups of `group` accumulated into
-    one float32 dW -- launched eagerly on one stream, and captured once in a CUDA graph and
-    replayed.  Device microseconds per layer (median over reps, each after the L2 sweep, queued
-    behind a device sleep), with effective TFLOP/s."""
+    """The recurrent layer's training pass as a user runs it, in backpropagation-through-time
+    order: `steps` fprops through one weight (t = 0, 1, ...), then the bprops in reverse
+    (t = steps-1, ..., 0); each group of `group` steps' weight gradient is accumulated into one
+    float32 dW on a side stream as soon as the backward pass has produced that group's last dy
+    (the group of the latest steps first), so it overlaps the remaining bprops; the side stream is
+    joined at the end.  Launched eagerly, and captured once in a CUDA graph and replayed.  Device
+    microseconds per layer (median over reps, each after the L2 sweep, queued behind a device
+    sleep), with effective TFLOP/s."""
     from block_sparse_matrix_gb300 import bsmm
     inp = wk.make_inputs(wl)
     m = bsmm.BlocksparseMatMul(inp.layout, block_size=wl.bs, feature_axis=wl.feature_axis)
@@ -591,12 +594,24 @@ def recurrent_layer(wl, dev, flush, reps):
         dxs = [torch.empty(m.i_shape(N), dtype=w.dtype, device=dev) for _ in range(T)]
         dw = torch.empty(m.w_shape, dtype=torch.float32, device=dev)
 
+        side = torch.cuda.Stream(device=dev)
+        groups = list(range(0, T, G))[::-1]             # the latest steps' group completes first
+
         def layer():
+            cur = torch.cuda.current_stream()
             for t in range(T):
                 m.fprop(xs[t], w, ys[t])
+            for t in reversed(range(T)):
                 m.bprop(dys[t], w, dxs[t])
-            for g0 in range(0, T, G):
-                m.updat_grouped(xs[g0:g0 + G], dys[g0:g0 + G], dw=dw, accumulate=g0 > 0)
+                if t in groups:                          # every dy of the group t .. t+G-1 is known
+                    ev = torch.cuda.Event()
+                    ev.record(cur)
+                    side.wait_event(ev)
+                    with torch.cuda.stream(side):
+                        m.updat_grouped(xs[t:t + G], dys[t:t + G], dw=dw, accumulate=t != groups[0])
+            ev = torch.cuda.Event()
+            ev.record(side)
+            cur.wait_event(ev)
 
         layer()
         eager = cold_times(layer, flush, reps)
@@ -610,8 +625,9 @@ def recurrent_layer(wl, dev, flush, reps):
     m.sync_status()
     f = 2 * T * wk.effective_flops(N, m.nnz, wl.bs) + T * wk.effective_flops(N, m.nnz, wl.bs)
     m.close()
-    return {"what": "%d steps of fprop and bprop, then the grouped weight gradient (groups of %d) into "
-                    "float32 dW; %d launches" % (T, G, 2 * T + (T + G - 1) // G),
+    return {"what": "%d fprops, then %d bprops in reverse step order, each group of %d steps' weight "
+                    "gradient accumulated into float32 dW on a side stream once its dys are known "
+                    "(overlapping the remaining bprops); %d launches" % (T, T, G, 2 * T + (T + G - 1) // G),
             "eager_us": round(eager, 3), "graph_us": round(graph, 3),
             "tflops_eager": round(f / (eager * 1e-6) / 1e12, 2), "tflops_graph": round(f / (graph * 1e-6) / 1e12, 2)}
 
