@@ -71,3 +71,68 @@ def test_layer_replays_in_a_cuda_graph(bs, fa, dtype, R, S, p, N):
         assert rel_fro(cpu64(eager[T + t]), o.bprop(L, bs, dys_h[t], w_h, fa)) <= TIGHT[dtype]
     assert rel_fro(cpu64(eager[2 * T]), o.updat_grouped(L, bs, xs_h, dys_h, fa)) <= TOL_DW[dtype]
     m.close()
+
+
+def _bptt_layer(m, w, xs, dys, ys, dxs, dw, side, G):
+    """fprops, then bprops in reverse step order; each group's weight gradient on `side` once the
+    backward pass has reached the group's first step, the latest group first (writes dw), the
+    others accumulating; `side` joined back at the end."""
+    T = len(xs)
+    cur = torch.cuda.current_stream()
+    groups = list(range(0, T, G))[::-1]
+    for t in range(T):
+        m.fprop(xs[t], w, ys[t])
+    for t in reversed(range(T)):
+        m.bprop(dys[t], w, dxs[t])
+        if t in groups:
+            ev = torch.cuda.Event()
+            ev.record(cur)
+            side.wait_event(ev)
+            with torch.cuda.stream(side):
+                m.updat_grouped(xs[t:t + G], dys[t:t + G], dw=dw, accumulate=t != groups[0])
+    ev = torch.cuda.Event()
+    ev.record(side)
+    cur.wait_event(ev)
+
+
+@pytest.mark.parametrize("bs,fa,dtype,R,S,p,N", [(32, 1, "bf16", 24, 24, 0.2, 128), (16, 0, "f16", 40, 36, 0.1, 256)])
+def test_two_stream_layer_replays_in_a_cuda_graph(bs, fa, dtype, R, S, p, N):
+    """The backpropagation-through-time layer with its weight-gradient groups forked to a second
+    stream (as the recurrent benchmark runs it): captured across both streams, replayed twice, equal
+    to eager execution bit for bit; the eager results match the float64 oracle."""
+    T, G = 6, 2
+    L = rand_layout(R, S, p, 160 + bs + N)
+    np.fill_diagonal(L[:min(R, S), :min(R, S)], 1)
+    m = BlocksparseMatMul(L, block_size=bs, feature_axis=fa)
+    xs_h = [wk.normals(wk.act_shape(R * bs, N, fa), 170 + t, 1.0, dtype) for t in range(T)]
+    dys_h = [wk.normals(wk.act_shape(S * bs, N, fa), 180 + t, 1.0, dtype) for t in range(T)]
+    w_h = wk.normals(m.w_shape, 190, float(1 / np.sqrt(R * bs * p)), dtype)
+    s, side = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        xs = [a.cuda() for a in xs_h]
+        dys = [a.cuda() for a in dys_h]
+        w = w_h.cuda()
+        ys = [torch.full(m.o_shape(N), float("nan"), dtype=wk.DTYPES[dtype], device="cuda") for _ in range(T)]
+        dxs = [torch.full(m.i_shape(N), float("nan"), dtype=wk.DTYPES[dtype], device="cuda") for _ in range(T)]
+        dw = torch.full(m.w_shape, float("nan"), device="cuda")
+        _bptt_layer(m, w, xs, dys, ys, dxs, dw, side, G)    # eager, and the warm-up of both streams
+        eager = [a.clone() for a in ys + dxs + [dw]]
+    s.synchronize()
+    m.sync_status()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        _bptt_layer(m, w, xs, dys, ys, dxs, dw, side, G)
+    for _ in range(2):
+        for a in ys + dxs + [dw]:
+            a.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(ys + dxs + [dw], eager):
+            assert torch.equal(a, b)
+    m.sync_status()
+    for t in range(T):
+        assert rel_fro(cpu64(eager[t]), o.fprop(L, bs, xs_h[t], w_h, fa)) <= TIGHT[dtype]
+        assert rel_fro(cpu64(eager[T + t]), o.bprop(L, bs, dys_h[t], w_h, fa)) <= TIGHT[dtype]
+    assert rel_fro(cpu64(eager[2 * T]), o.updat_grouped(L, bs, xs_h, dys_h, fa)) <= TOL_DW[dtype]
+    m.close()
