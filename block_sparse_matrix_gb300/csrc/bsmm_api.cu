@@ -74,6 +74,7 @@ bsmm_status bsmm_create(bsmm_t *out, const uint8_t *layout_host, int R, int S, i
     if (const char *e = getenv("BSMM_TC_STAGE_KB")) h->tc_stage_kb = atoi(e);
     if (const char *e = getenv("BSMM_TC_ROWS")) h->tc_rows = atoi(e);
     if (const char *e = getenv("BSMM_TC_BINS")) h->tc_bins = atoi(e);
+    if (const char *e = getenv("BSMM_TC_ESLOTS")) h->tc_eslots = atoi(e);
     if (cudaGetDevice(&h->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
         delete h;

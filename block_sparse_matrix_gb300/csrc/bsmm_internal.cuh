@@ -38,6 +38,7 @@ struct bsmm_ctx {
     int tc_stage_kb = -1;  // fprop/bprop per-CTA stage budget override (KB), from BSMM_TC_STAGE_KB
     int tc_rows = -1;      // window-kernel minibatch tile height override (64 or 128), from BSMM_TC_ROWS
     int tc_bins = -1;      // window kernel: 1 forces binned windows, 0 forbids them, from BSMM_TC_BINS
+    int tc_eslots = -1;    // window kernel: activation panels per chunk override (1..8), from BSMM_TC_ESLOTS
 };
 
 extern std::atomic<int64_t> g_bsmm_launches;

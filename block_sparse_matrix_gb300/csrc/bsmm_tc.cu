@@ -2544,21 +2544,36 @@ FbStages choose_stages(const bsmm_ctx *h, int N, int64_t units, int W, bool rows
     const double density = (double)h->nnz / ((double)h->R * h->S);
     const double coarse_density = h->bs == 8 ? std::min(1.0, 4.0 * density) : density;
     const int expect_r = (int)(1.25 * W * gc * coarse_density) + 1;
-    // (N,C) panels: two per chunk (measured on N = 128 recurrent steps: 14.6 us against 16.9 with one,
-    // 16.0 with four; with 64-byte rows for bs 32, four per chunk gave the same as two)
-    g.e_slots = h->fa ? 2 : (h->bs == 32 ? 2 : 4);
-    const int r_cap = (32 - g.e_slots * a_ops) / b_ops;
-    g.r_slots = std::max(2, std::min(r_cap, g.e_slots * expect_r));
+    // Activation panels per chunk.  Fewer, larger chunks cost less per byte: each chunk is one TMA
+    // issue of a few hundred ns and one barrier round trip.  Measured on the recurrent step (bs 32,
+    // (N,C), N = 128), back to back: one CTA per SM (binned fprop) with 2 / 4 / 8 panels 7.93 /
+    // 7.59 / 7.11 us; two CTAs per SM (bprop) with 2 / 4 panels 7.57 / 7.26 us, while 8 panels
+    // leave room for one CTA per SM only (10.85 us).  (N,C) activations therefore take the largest
+    // of 8, 4, 2, 1 panels that keeps two stages and, with more units than SMs, two CTAs per SM.
+    // (C,N) activations keep 2 panels (bs 32) or 4, and any count (also one pinned for tests) is
+    // halved while two stages do not fit.
+    const bool want_two = units > h->sm_count;
+    int e_first = h->fa ? 8 : (h->bs == 32 ? 2 : 4);
+    if (h->tc_eslots >= 1 && h->tc_eslots <= 8) e_first = h->tc_eslots;
     const int budget_two = h->tc_stage_kb >= 32 ? std::min(h->tc_stage_kb, 196) * 1024 : 96 * 1024;
     const int budget_one = h->tc_stage_kb >= 32 ? std::min(h->tc_stage_kb, 196) * 1024 : 196 * 1024;
-    for (;;) {
-        g.b_off = g.e_slots * g.a_slot;
-        g.stage_bytes = (g.b_off + g.r_slots * b_slot + 1023) & ~1023;
-        const bool two = units > h->sm_count && 2 * g.stage_bytes + g.a_slot <= budget_two;
-        const int budget = two ? budget_two : budget_one;
-        g.stages = std::min(kMaxStages, (budget - g.a_slot) / g.stage_bytes);
-        if (g.stages >= 2 || g.r_slots <= 1) break;
-        --g.r_slots;                                   // shrink the chunk until two stages fit
+    for (g.e_slots = e_first;; g.e_slots = g.e_slots > 2 ? g.e_slots / 2 : g.e_slots - 1) {
+        const int r_cap = (32 - g.e_slots * a_ops) / b_ops;
+        g.r_slots = std::max(2, std::min(r_cap, g.e_slots * expect_r));
+        bool two = false;
+        for (;;) {
+            g.b_off = g.e_slots * g.a_slot;
+            g.stage_bytes = (g.b_off + g.r_slots * b_slot + 1023) & ~1023;
+            two = want_two && 2 * g.stage_bytes + g.a_slot <= budget_two;
+            const int budget = two ? budget_two : budget_one;
+            g.stages = std::min(kMaxStages, (budget - g.a_slot) / g.stage_bytes);
+            if (g.stages >= 2 || g.r_slots <= 1) break;
+            --g.r_slots;                               // shrink the chunk until two stages fit
+        }
+        const bool fits = g.stages >= 2 && (two || !want_two);
+        if (fits || g.e_slots <= 1) break;
+        // (C,N) activations and a pinned panel count only need two stages to fit
+        if (g.stages >= 2 && (!h->fa || h->tc_eslots >= 1)) break;
     }
     g.stages = std::max(g.stages, 2);
     if (g.stages >= kProducers) {

@@ -313,10 +313,11 @@ def test_errors_reported():
 
 @pytest.mark.parametrize("bs,fa,dtype", [(32, 1, "bf16"), (16, 0, "f16"), (8, 0, "bf16"), (8, 1, "f16")])
 def test_window_sizes_bit_identical(monkeypatch, bs, fa, dtype):
-    """The tensor-core fprop/bprop split output blocks into windows and the minibatch into
-    tiles of 128 or 64 rows; each output is accumulated over its source blocks in the same
-    order for every window size and tile height, so all give the same bits (and match the
-    oracle).  N = 200 leaves a ragged last tile either way."""
+    """The tensor-core fprop/bprop split output blocks into windows, the minibatch into tiles of
+    128 or 64 rows and a window's sources into chunks of 1 to 8 panels; each output is
+    accumulated over its source blocks in the same order for every window size, tile height and
+    chunk size, so all give the same bits (and match the oracle).  N = 200 leaves a ragged last
+    tile either way."""
     L, x, w, dy, ref_y, ref_dx, _ = small_case(bs, fa, dtype)
     xc, wc, dyc = x.cuda(), w.cuda(), dy.cuda()
     outs = []
@@ -328,6 +329,12 @@ def test_window_sizes_bit_identical(monkeypatch, bs, fa, dtype):
             m = make(L, bs, fa, "auto")
             outs.append((m.fprop(xc, wc), m.bprop(dyc, wc)))
             m.sync_status()
+    monkeypatch.delenv("BSMM_TC_ROWS")
+    for eslots in (1, 3, 8):                   # activation panels per chunk
+        monkeypatch.setenv("BSMM_TC_ESLOTS", str(eslots))
+        m = make(L, bs, fa, "auto")
+        outs.append((m.fprop(xc, wc), m.bprop(dyc, wc)))
+        m.sync_status()
     for y, dx in outs[1:]:
         assert torch.equal(y, outs[0][0]) and torch.equal(dx, outs[0][1])
     assert rel_fro(cpu64(outs[0][0]), ref_y) <= TIGHT[dtype]
