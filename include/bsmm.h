@@ -38,6 +38,11 @@
  *     written as zeros.
  *   - A handle may be used from several streams at once (its tables are read
  *     only after creation), but not while bsmm_destroy runs.
+ *   - The passes launch with programmatic dependent launch: a kernel may start
+ *     while the previous kernel on `stream` finishes and read the handle's own
+ *     tables (fixed once bsmm_create returns), but it waits for that kernel to
+ *     complete before it reads or writes any caller buffer, so stream order
+ *     holds as for ordinary launches.
  */
 #ifndef BSMM_H
 #define BSMM_H
