@@ -342,7 +342,8 @@ def test_window_sizes_bit_identical(monkeypatch, bs, fa, dtype):
 
 
 @pytest.mark.parametrize("bs,fa,dtype,R,N", [(32, 1, "bf16", 200, 136), (16, 0, "f16", 200, 200),
-                                             (8, 0, "bf16", 400, 136), (32, 0, "bf16", 170, 72)])
+                                             (8, 0, "bf16", 400, 136), (32, 0, "bf16", 170, 72),
+                                             (16, 1, "f16", 200, 40), (32, 0, "bf16", 170, 64)])
 def test_window_bins_bit_identical(monkeypatch, bs, fa, dtype, R, N):
     """With more output blocks than SMs per minibatch tile, the window kernel may deal the blocks
     to one bin per SM (heaviest first) and treat each bin as a window of arbitrary output blocks.
