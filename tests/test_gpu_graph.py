@@ -1,7 +1,8 @@
-"""The passes captured in a CUDA graph: a recurrent-style layer -- per-step fprop and bprop and
-the grouped weight gradient of the steps -- is warmed up on one stream (the handle builds its
-schedules and per-stream scratch there), captured on that stream, replayed twice, and must equal
-eager execution bit for bit; the eager results match the float64 oracle."""
+"""The passes captured in a CUDA graph (tensor-core kernels, and the float32 SIMT kernels, which
+also launch with programmatic dependent launch): a recurrent-style layer -- per-step fprop and
+bprop and the grouped weight gradient of the steps -- is warmed up on one stream (the handle
+builds its schedules and per-stream scratch there), captured on that stream, replayed twice,
+and must equal eager execution bit for bit; the eager results match the float64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +14,7 @@ from oracle import oracle as o
 from _util import TOL_DW, cpu64, rand_layout, rel_fro
 
 pytestmark = pytest.mark.gpu
-TIGHT = {"f16": 2e-3, "bf16": 8e-3}
+TIGHT = {"f16": 2e-3, "bf16": 8e-3, "f32": 1e-5}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -32,7 +33,8 @@ def _layer(m, w, xs, dys, ys, dxs, dw):
 
 @pytest.mark.parametrize("bs,fa,dtype,R,S,p,N", [(32, 1, "bf16", 24, 24, 0.2, 128), (32, 1, "bf16", 16, 16, 0.5, 64),
                                                  (32, 1, "bf16", 16, 16, 0.5, 256), (16, 0, "f16", 40, 36, 0.1, 256),
-                                                 (8, 0, "bf16", 41, 37, 0.08, 136)])
+                                                 (8, 0, "bf16", 41, 37, 0.08, 136), (32, 1, "f32", 8, 8, 0.5, 64),
+                                                 (16, 0, "f32", 12, 10, 0.4, 200)])
 def test_layer_replays_in_a_cuda_graph(bs, fa, dtype, R, S, p, N):
     T = 4
     L = rand_layout(R, S, p, 60 + bs + N)
@@ -95,7 +97,8 @@ def _bptt_layer(m, w, xs, dys, ys, dxs, dw, side, G):
     cur.wait_event(ev)
 
 
-@pytest.mark.parametrize("bs,fa,dtype,R,S,p,N", [(32, 1, "bf16", 24, 24, 0.2, 128), (16, 0, "f16", 40, 36, 0.1, 256)])
+@pytest.mark.parametrize("bs,fa,dtype,R,S,p,N", [(32, 1, "bf16", 24, 24, 0.2, 128), (16, 0, "f16", 40, 36, 0.1, 256),
+                                                 (32, 1, "f32", 8, 8, 0.5, 64)])
 def test_two_stream_layer_replays_in_a_cuda_graph(bs, fa, dtype, R, S, p, N):
     """The backpropagation-through-time layer with its weight-gradient groups forked to a second
     stream (as the recurrent benchmark runs it): captured across both streams, replayed twice, equal
